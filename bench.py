@@ -1,0 +1,370 @@
+"""Reshard executor benchmark: destination GB/s on one GB300 (device-timed) and % of HBM roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--mode direct|packed] [--suite FILE]
+
+A step is one reshard of the whole workload (every tensor, one batched plan, one execute) with
+inputs resident in HBM. The plan is built once before timing (the descriptor cache a refit
+reuses every step). Multi-GPU runs (torchrun, one rank per GPU) run independent replicas of the
+same workload: the path has no exchange step on one node with every shard on one GPU.
+Prints ONE JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "reshard GB/s (dst bytes, device-timed) on 1 GB300; % of HBM roofline"
+DEFAULT_WORKLOAD = "dense_ffn_32x14336x4096_tp8_to_dp2tp2"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("execute.cu", "plan.h"):
+        with open(os.path.join(ROOT, "dtensor_resharding_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str, mode: str):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        recs = json.load(f)
+    for r in recs:
+        if (r.get("kernel") == kernel and r.get("workload") == workload and r.get("mode") == mode
+                and r.get("source_hash") == kernel_source_hash()):
+            return r.get("traffic_bytes_per_launch")
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while the bench runs."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        self.path = os.path.join("/tmp", f"reshard_clocks_{os.getpid()}.csv")
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 8:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        busy = [r for r in rows if (num(r[3]) or 0) > 0] or rows
+        sm = [num(r[0]) for r in busy if num(r[0]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in busy for i in range(4) if r[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(rows[0][1]),
+                "power_w_max": max((num(r[2]) or 0) for r in rows), "reasons": reasons, "samples": len(busy)}
+
+
+# ----------------------------------------------------------------------------- oracle timing
+
+def time_oracle_sample(wl, src_host, src_off, budget_s: float, max_tensors: int):
+    """Run the C oracle over the first tensors of the workload until ~budget_s of host time.
+
+    Returns (dst bytes produced, seconds, tensors used). Single thread."""
+    import numpy as np
+    from oracle import coracle
+    es_of = {"u8": 1, "bf16": 2, "f16": 2, "f32": 4, "i32": 4, "i64": 8}
+    done_bytes, spent, used = 0, 0.0, 0
+    for ti, t in enumerate(wl.tensors[:max_tensors]):
+        es = es_of[t.dtype]
+        dst = []
+        for v in t.dst_views:
+            n = wl.dst_buffer_numel[v.buffer] * (1 if wl.quant == "mxfp8" else es)
+            dst.append(np.empty(n, np.uint8))
+        sc = [np.empty(wl.dst_buffer_numel[v.buffer] // 32, np.uint8) for v in t.dst_views] if wl.quant == "mxfp8" else None
+        sb = [src_host[src_off[v.buffer]: src_off[v.buffer] + wl.src_buffer_numel[v.buffer] * es] for v in t.src_views]
+        t0 = time.perf_counter()
+        coracle.reshard_tensor(t, sb, dst, wl.quant, sc)
+        spent += time.perf_counter() - t0
+        done_bytes += sum(d.size for d in dst) + (sum(s.size for s in sc) if sc else 0)
+        used += 1
+        if spent >= budget_s:
+            break
+    return done_bytes, spent, used
+
+
+def reference_arm(args, rank: int) -> None:
+    """The oracle as it stands, timed on the host cores over a bounded sample per step."""
+    if rank != 0:
+        return
+    import numpy as np
+    import synthetic as S
+    from oracle import coracle
+    coracle.build()
+    wl = S.workload_by_name(args.workload)
+    # one step = the oracle over the first n tensors; n sized so the whole run stays ~2 minutes
+    probe = S.Workload(wl.name, wl.tensors[:1], wl.quant, wl.values)
+    probe = S.workloads._size_buffers(probe, len(wl.src_buffer_numel), len(wl.dst_buffer_numel))
+    lay = S.allocate(probe, "cpu")
+    S.fill_sources(probe, lay)
+    src = lay.src_slab.numpy()
+    b1, s1, _ = time_oracle_sample(probe, src, lay.src_off, 0.0, 1)
+    steps_total = args.steps + args.warmup
+    per_step_budget = max(0.05, 120.0 / steps_total)
+    n = max(1, min(len(wl.tensors), int(per_step_budget / max(s1, 1e-6))))
+    sample = S.Workload(wl.name, wl.tensors[:n], wl.quant, wl.values)
+    sample = S.workloads._size_buffers(sample, len(wl.src_buffer_numel), len(wl.dst_buffer_numel))
+    lay = S.allocate(sample, "cpu")
+    S.fill_sources(sample, lay)
+    src = lay.src_slab.numpy()
+    times, nbytes = [], 0
+    for i in range(steps_total):
+        b, s, _ = time_oracle_sample(sample, src, lay.src_off, 1e30, n)
+        if i >= args.warmup:
+            times.append(s)
+            nbytes = b
+    total = sum(times)
+    value = nbytes * len(times) / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / len(times), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "mode": "oracle (full broadcast then slice)",
+                   "sample_tensors": n, "sample_dst_bytes": nbytes},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"first {n} of {len(wl.tensors)} tensors per step, host buffers, one thread"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------------- our arm
+
+def our_arm(args, rank: int, world: int, local_rank: int) -> None:
+    import torch
+    import torch.distributed as dist
+
+    import dtensor_resharding_gb300 as R
+    import synthetic as S
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = S.workload_by_name(args.workload)
+    lay = S.allocate(wl, dev)
+    S.fill_sources(wl, lay)
+    S.fill_canary(lay)
+    t0 = time.perf_counter()
+    plan = R.plan_workload(wl)
+    plan_s = time.perf_counter() - t0
+    st = R.reshard_plan_stats(plan)
+    sp, dp = R.workload_pointers(wl, lay)
+    quant = wl.quant
+    dst_bytes = wl.dst_bytes()
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def run_steps(mode, k, warm):
+        for _ in range(warm):
+            R.reshard_execute(plan, sp, dp, mode=mode, quant=quant, stream=sh)
+        stream.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
+        barrier()
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for a, b in ev:
+            a.record(stream)
+            R.reshard_execute(plan, sp, dp, mode=mode, quant=quant, stream=sh)
+            b.record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        total_ms = start.elapsed_time(end)
+        per = [a.elapsed_time(b) for a, b in ev]
+        if world > 1:
+            t = torch.tensor([total_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            total_ms = float(t.item())
+        return total_ms, per
+
+    clocks = ClockSampler(local_rank)
+    total_ms, per = run_steps(args.mode, args.steps, args.warmup)
+    clk = clocks.stop()
+    ms_per_step = total_ms / args.steps
+    value = world * dst_bytes * args.steps / (total_ms / 1e3) / 1e9
+
+    # roofline of the dominant kernel (direct: the one copy kernel per execute)
+    peak, peak_kind = peaks()
+    if args.mode == "direct":
+        algo = st["bytes_read"] + (st["bytes_written"] if quant == "none" else dst_bytes)
+        kernel = "reshard_mxfp8_kernel" if quant == "mxfp8" else "reshard_copy_kernel"
+    else:
+        algo = (st["message_bytes"] + (st["bytes_written"] if quant == "none" else dst_bytes))  # unpack
+        kernel = "reshard_mxfp8_kernel" if quant == "mxfp8" else "reshard_copy_kernel"
+    launch_ms = statistics.mean(per)
+    achieved = algo / (launch_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(kernel, wl.name, args.mode),
+                "kernel": kernel, "algorithmic_bytes_per_launch": algo, "peak_source": peak_kind,
+                "launch_ms_median": round(statistics.median(per), 4),
+                "launch_ms_min": round(min(per), 4), "launch_ms_max": round(max(per), 4)}
+    if args.mode == "packed":
+        roofline["note"] = "packed mode: step = pack + unpack launches; achieved counts the unpack bytes only"
+
+    # the other mode on the same inputs, for context
+    other = "packed" if args.mode == "direct" else "direct"
+    o_ms, _ = run_steps(other, max(3, args.steps // 4), 2)
+    modes = {other: {"ms_per_step": round(o_ms / max(3, args.steps // 4), 4),
+                     "value": round(world * dst_bytes * max(3, args.steps // 4) / (o_ms / 1e3) / 1e9, 2)}}
+
+    # end to end through the public call with host buffers: H2D of the step's sources from pinned
+    # memory, the execute, D2H of the step's destinations, all inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        try:
+            hsrc = torch.empty_like(lay.src_slab, device="cpu", pin_memory=True)
+            hdst = torch.empty_like(lay.dst_slab, device="cpu", pin_memory=True)
+            hsrc.copy_(lay.src_slab)
+            ek = args.e2e_steps
+            for i in range(ek + 1):
+                if i == 1:
+                    barrier()
+                    torch.cuda.synchronize()
+                    t_e2e = torch.cuda.Event(enable_timing=True)
+                    t_e2e_end = torch.cuda.Event(enable_timing=True)
+                    t_e2e.record(stream)
+                with torch.cuda.stream(stream):
+                    lay.src_slab.copy_(hsrc, non_blocking=True)
+                    R.reshard_execute(plan, sp, dp, mode=args.mode, quant=quant, stream=sh)
+                    hdst.copy_(lay.dst_slab, non_blocking=True)
+            t_e2e_end.record(stream)
+            torch.cuda.synchronize()
+            e_ms = t_e2e.elapsed_time(t_e2e_end)
+            if world > 1:
+                t = torch.tensor([e_ms], device=dev)
+                dist.all_reduce(t, op=dist.ReduceOp.MAX)
+                e_ms = float(t.item())
+            e2e = {"value": round(world * dst_bytes * ek / (e_ms / 1e3) / 1e9, 3), "unit": "GB/s",
+                   "h2d_bytes_per_step": lay.src_slab.numel(), "d2h_bytes_per_step": lay.dst_slab.numel(),
+                   "steps": ek, "ms_per_step": round(e_ms / ek, 3),
+                   "note": "pinned host slabs, copies and execute on one stream"}
+            del hsrc, hdst
+        except RuntimeError as e:
+            e2e = {"value": None, "unit": "GB/s", "error": str(e)[:200]}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import numpy as np  # noqa: F401
+        from oracle import coracle
+        coracle.build()
+        src_host = lay.src_slab.cpu().numpy()
+        nb, secs, used = time_oracle_sample(wl, src_host, lay.src_off, args.cpu_budget, len(wl.tensors))
+        cpu = {"value": round(nb / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {used} of {len(wl.tensors)} tensors ({nb} destination bytes), host copies, one thread",
+               "seconds": round(secs, 2)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "mode": args.mode, "quant": quant, "tensors": len(wl.tensors),
+                       "src_bytes": st["bytes_read"], "dst_bytes": dst_bytes,
+                       "regions": st["regions"], "items": st["items"],
+                       "l2": "inputs larger than L2 (every step streams all sources and destinations)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                       "plan_build_s": round(plan_s, 3)},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+            "gpu_launches": args.steps * (1 if args.mode == "direct" else 2),
+            "modes": modes,
+        }
+        print(json.dumps(line), flush=True)
+        if args.suite:
+            with open(args.suite, "a") as f:
+                f.write(json.dumps(line) + "\n")
+    R.reshard_plan_destroy(plan)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--mode", default="direct", choices=["direct", "packed"])
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--suite", default=None, help="also append the JSON line to this file")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        reference_arm(args, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        our_arm(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

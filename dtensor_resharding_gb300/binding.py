@@ -1,0 +1,275 @@
+"""Thin ctypes binding of libreshard.so: the C-ABI calls under the same names.
+
+Argument marshalling only: every step of the reshard (planning, copies, quantization) runs in
+the library. There is no fallback: if the library is missing, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Any, Dict, List, Optional, Sequence
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libreshard.so")
+
+RESHARD_OK = 0
+RESHARD_ERR_INVALID_ARG = -1
+RESHARD_ERR_UNSUPPORTED = -2
+RESHARD_ERR_CUDA = -3
+RESHARD_ERR_OOM = -4
+RESHARD_ERR_COVERAGE = -5
+RESHARD_REPLICATE = 0
+RESHARD_SHARD = 1
+RESHARD_DIRECT = 0
+RESHARD_PACKED = 1
+RESHARD_QUANT_NONE = 0
+RESHARD_QUANT_MXFP8 = 1
+RESHARD_MAX_DIMS = 4
+DTYPE_CODES = {"u8": 0, "bf16": 1, "f16": 2, "f32": 3, "i32": 4, "i64": 5}
+MODES = {"direct": RESHARD_DIRECT, "packed": RESHARD_PACKED}
+QUANTS = {"none": RESHARD_QUANT_NONE, "mxfp8": RESHARD_QUANT_MXFP8}
+EXPORTED = ("reshard_plan_create", "reshard_plan_batch", "reshard_execute", "reshard_plan_stats",
+            "reshard_plan_regions", "reshard_plan_group_members", "reshard_plan_items", "reshard_plan_destroy",
+            "reshard_last_error")
+
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+
+
+class MeshT(ctypes.Structure):
+    _fields_ = [("ndim", ctypes.c_int), ("shape", _i64p), ("ranks", _i32p)]
+
+
+class PlacementT(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("dim", ctypes.c_int)]
+
+
+class ViewT(ctypes.Structure):
+    _fields_ = [("offset_elems", ctypes.c_int64), ("strides_elems", _i64p), ("capacity_elems", ctypes.c_int64)]
+
+
+class TensorSpecT(ctypes.Structure):
+    _fields_ = [("ndim", ctypes.c_int), ("global_shape", _i64p), ("dtype", ctypes.c_int),
+                ("src_mesh", MeshT), ("src_pl", ctypes.POINTER(PlacementT)), ("src_views", ctypes.POINTER(ViewT)),
+                ("dst_mesh", MeshT), ("dst_pl", ctypes.POINTER(PlacementT)), ("dst_views", ctypes.POINTER(ViewT))]
+
+
+STATS_FIELDS = ("n_tensors", "regions", "items", "dst_groups", "messages", "bytes_read", "bytes_written",
+                "wire_bytes", "message_bytes", "gather_bcast_bytes", "global_bytes")
+
+
+class StatsT(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_int64) for f in STATS_FIELDS]
+
+
+class ReshardError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"reshard error {code}: {msg}")
+        self.code = code
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libreshard.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp = ctypes.c_void_p
+    lib.reshard_plan_create.argtypes = [ctypes.POINTER(TensorSpecT), ctypes.POINTER(vp)]
+    lib.reshard_plan_batch.argtypes = [ctypes.POINTER(TensorSpecT), ctypes.c_int, ctypes.POINTER(vp)]
+    lib.reshard_execute.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.c_int, ctypes.c_int, vp]
+    lib.reshard_plan_stats.argtypes = [vp, ctypes.POINTER(StatsT)]
+    lib.reshard_plan_regions.argtypes = [vp, ctypes.c_int64, _i32p, _i32p, _i32p, _i64p, _i64p, _i64p]
+    lib.reshard_plan_group_members.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, _i32p, _i64p]
+    lib.reshard_plan_items.argtypes = [vp, ctypes.c_int, ctypes.c_int64, vp, _i64p, _i32p, _i32p, _i64p, _i64p,
+                                       _i64p]
+    lib.reshard_plan_destroy.argtypes = [vp]
+    lib.reshard_last_error.argtypes = []
+    lib.reshard_last_error.restype = ctypes.c_char_p
+    for name in EXPORTED[:-1]:
+        getattr(lib, name).restype = ctypes.c_int
+    return lib
+
+
+LIB = _load()
+
+
+def _check(rc: int) -> None:
+    if rc != RESHARD_OK:
+        raise ReshardError(rc, reshard_last_error())
+
+
+def reshard_last_error() -> str:
+    return LIB.reshard_last_error().decode()
+
+
+# ------------------------------------------------------------------------- spec marshalling
+
+def _arr(ctype, vals):
+    vals = [int(v) for v in vals]
+    return (ctype * max(1, len(vals)))(*vals)
+
+
+def _placements(pls: Sequence[Any]):
+    out = (PlacementT * max(1, len(pls)))()
+    for i, p in enumerate(pls):
+        if isinstance(p, str):
+            out[i].kind, out[i].dim = (RESHARD_REPLICATE, 0) if p == "R" else (RESHARD_SHARD, int(p[1:]))
+        else:
+            out[i].kind, out[i].dim = int(p[0]), int(p[1])
+    return out
+
+
+def _views(views, capacities, keep):
+    if views is None:
+        return None
+    out = (ViewT * max(1, len(views)))()
+    for i, v in enumerate(views):
+        out[i].offset_elems = int(getattr(v, "offset", 0))
+        st = getattr(v, "strides", None)
+        if st is not None:
+            a = _arr(ctypes.c_int64, st)
+            keep.append(a)
+            out[i].strides_elems = a
+        out[i].capacity_elems = int(capacities[i]) if capacities is not None else 0
+    return out
+
+
+def make_spec(desc, src_capacity: Optional[Sequence[int]] = None, dst_capacity: Optional[Sequence[int]] = None,
+              keep: Optional[list] = None) -> TensorSpecT:
+    """Marshal one tensor description into the C struct.
+
+    ``desc`` needs: global_shape, dtype ("bf16", ... or a code), src_mesh, src_placements
+    ("R"/"S<d>" or (kind, dim)), dst_mesh, dst_placements; optionally src_views / dst_views
+    (objects with .offset and .strides, one per pointer index) and src_ranks / dst_ranks.
+    ``keep`` collects the ctypes arrays that must outlive the C call.
+    """
+    keep = keep if keep is not None else []
+    s = TensorSpecT()
+    gs = _arr(ctypes.c_int64, desc.global_shape)
+    s.ndim = len(desc.global_shape)
+    s.global_shape = gs
+    s.dtype = DTYPE_CODES[desc.dtype] if isinstance(desc.dtype, str) else int(desc.dtype)
+    parts = [gs]
+    for side in ("src", "dst"):
+        mesh = getattr(desc, f"{side}_mesh")
+        ms = _arr(ctypes.c_int64, mesh)
+        ranks = getattr(desc, f"{side}_ranks", None)
+        rk = _arr(ctypes.c_int32, ranks) if ranks is not None else None
+        m = MeshT(len(mesh), ms, rk)
+        pl = _placements(getattr(desc, f"{side}_placements"))
+        vw = _views(getattr(desc, f"{side}_views", None), src_capacity if side == "src" else dst_capacity, keep)
+        setattr(s, f"{side}_mesh", m)
+        setattr(s, f"{side}_pl", pl)
+        if vw is not None:
+            setattr(s, f"{side}_views", vw)
+        parts += [ms, rk, pl, vw]
+    keep.extend(p for p in parts if p is not None)
+    return s
+
+
+# ------------------------------------------------------------------------------- the calls
+
+class Plan:
+    """Owns a reshard_plan_t*; destroyed explicitly or on garbage collection."""
+
+    def __init__(self, handle: int, n_src: int, n_dst: int):
+        self.handle = ctypes.c_void_p(handle)
+        self.n_src_ptrs = n_src
+        self.n_dst_ptrs = n_dst
+
+    def __del__(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            LIB.reshard_plan_destroy(self.handle)
+            self.handle = None
+
+
+def _n_ranks(mesh) -> int:
+    n = 1
+    for x in mesh:
+        n *= int(x)
+    return n
+
+
+def reshard_plan_create(desc, src_capacity=None, dst_capacity=None) -> Plan:
+    keep: list = []
+    s = make_spec(desc, src_capacity, dst_capacity, keep)
+    h = ctypes.c_void_p()
+    _check(LIB.reshard_plan_create(ctypes.byref(s), ctypes.byref(h)))
+    return Plan(h.value, _n_ranks(desc.src_mesh), _n_ranks(desc.dst_mesh))
+
+
+def reshard_plan_batch(descs: Sequence[Any], src_capacity=None, dst_capacity=None) -> Plan:
+    """One plan over many tensors. Capacities (optional) are per tensor lists of per-rank counts."""
+    keep: list = []
+    arr = (TensorSpecT * max(1, len(descs)))()
+    for i, d in enumerate(descs):
+        arr[i] = make_spec(d, src_capacity[i] if src_capacity else None,
+                           dst_capacity[i] if dst_capacity else None, keep)
+    h = ctypes.c_void_p()
+    _check(LIB.reshard_plan_batch(arr, len(descs), ctypes.byref(h)))
+    return Plan(h.value, sum(_n_ranks(d.src_mesh) for d in descs), sum(_n_ranks(d.dst_mesh) for d in descs))
+
+
+def reshard_execute(plan: Plan, src_ptrs: Sequence[int], dst_ptrs: Sequence[int], mode="direct", quant="none",
+                    stream: int = 0) -> None:
+    """Enqueue the reshard on ``stream`` (a cudaStream_t as int; 0 = legacy default stream)."""
+    mode = MODES[mode] if isinstance(mode, str) else int(mode)
+    quant = QUANTS[quant] if isinstance(quant, str) else int(quant)
+    sp = (ctypes.c_void_p * max(1, len(src_ptrs)))(*[int(p) if p else None for p in src_ptrs])
+    dp = (ctypes.c_void_p * max(1, len(dst_ptrs)))(*[int(p) if p else None for p in dst_ptrs])
+    _check(LIB.reshard_execute(plan.handle, sp, dp, mode, quant, ctypes.c_void_p(int(stream) or None)))
+
+
+def reshard_plan_stats(plan: Plan) -> Dict[str, int]:
+    st = StatsT()
+    _check(LIB.reshard_plan_stats(plan.handle, ctypes.byref(st)))
+    return {f: int(getattr(st, f)) for f in STATS_FIELDS}
+
+
+def reshard_plan_regions(plan: Plan) -> List[tuple]:
+    """[(tensor, src_rank, dst_group, ((lo, hi), ...)), ...] in plan order (global coordinates)."""
+    n = ctypes.c_int64()
+    _check(LIB.reshard_plan_regions(plan.handle, 0, None, None, None, None, None, ctypes.byref(n)))
+    k = n.value
+    t = (ctypes.c_int32 * max(1, k))()
+    s = (ctypes.c_int32 * max(1, k))()
+    g = (ctypes.c_int32 * max(1, k))()
+    lo = (ctypes.c_int64 * max(1, k * RESHARD_MAX_DIMS))()
+    hi = (ctypes.c_int64 * max(1, k * RESHARD_MAX_DIMS))()
+    _check(LIB.reshard_plan_regions(plan.handle, k, t, s, g, lo, hi, ctypes.byref(n)))
+    D = RESHARD_MAX_DIMS
+    return [(t[i], s[i], g[i], tuple((lo[i * D + d], hi[i * D + d]) for d in range(D))) for i in range(k)]
+
+
+def reshard_plan_group_members(plan: Plan, g: int) -> List[int]:
+    n = ctypes.c_int64()
+    _check(LIB.reshard_plan_group_members(plan.handle, g, 0, None, ctypes.byref(n)))
+    out = (ctypes.c_int32 * max(1, n.value))()
+    _check(LIB.reshard_plan_group_members(plan.handle, g, n.value, out, ctypes.byref(n)))
+    return list(out[: n.value])
+
+
+ITEM_DTYPE = [("src_off", "<i8"), ("dst_off", "<i8"), ("src_pitch", "<i8"), ("dst_pitch", "<i8"),
+              ("rows", "<i4"), ("run", "<i4"), ("src", "<i4"), ("group", "<i4"), ("esize", "<i4"),
+              ("pad", "<i4", (3,))]
+
+
+def reshard_plan_items(plan: Plan, which: int = 0):
+    """(items as a numpy structured array, group_start, member_ptr, member_off) of one pass."""
+    import numpy as np
+    n, ng, nm = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    _check(LIB.reshard_plan_items(plan.handle, which, 0, None, ctypes.byref(n), None, None, None,
+                                  ctypes.byref(ng), ctypes.byref(nm)))
+    items = np.zeros(n.value, dtype=ITEM_DTYPE)
+    gs = np.zeros(ng.value + 1, np.int32)
+    mp = np.zeros(max(1, nm.value), np.int32)
+    mo = np.zeros(max(1, nm.value), np.int64)
+    _check(LIB.reshard_plan_items(plan.handle, which, n.value, items.ctypes.data_as(ctypes.c_void_p), ctypes.byref(n),
+                                  gs.ctypes.data_as(_i32p), mp.ctypes.data_as(_i32p), mo.ctypes.data_as(_i64p),
+                                  ctypes.byref(ng), ctypes.byref(nm)))
+    return items, gs, mp[: nm.value], mo[: nm.value]
+
+
+def reshard_plan_destroy(plan: Plan) -> None:
+    if plan.handle is not None and plan.handle.value:
+        _check(LIB.reshard_plan_destroy(plan.handle))
+    plan.handle = None

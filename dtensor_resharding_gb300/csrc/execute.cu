@@ -1,0 +1,475 @@
+// Device executor of the reshard plan: persistent descriptor-walking kernels for sm_103a.
+//
+// - reshard_copy_kernel: one pass over the work-item table; every item's source rows are read
+//   once and written to every destination replica of its group (the fan-out of "xferdtensor
+//   Transports" in the NeMo-RL design doc "NCCL Reshard Refit (Experimental)"). Used for the
+//   direct mode and for both halves of the packed mode (pack: source -> contiguous message;
+//   unpack: message -> destination replicas), the messages a wire transport would carry
+//   ("NeMo-RL: Optimizing Non-Colocated Refit", "Optimization #2": pack into one contiguous
+//   buffer).
+// - reshard_mxfp8_kernel: the same walk with the receive-side BF16 -> MXFP8 epilogue
+//   (design doc, "Enabling It": generation ranks quantize each received BF16 shard), by the
+//   OCP MX v1.0 rule: per 32 contiguous elements along the destination's last dim, the E8M0
+//   scale X = floor(log2 amax) - 8 and E4M3 elements v / 2^X rounded to nearest even,
+//   saturating at 448. The block amax is combined across the 4 lanes holding a block with
+//   warp shuffles.
+//
+// Nothing here is a contraction; both kernels are bound by HBM bandwidth. Sources and
+// destinations must not overlap in memory.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <string>
+
+#include "plan.h"
+
+namespace reshard {
+namespace {
+
+constexpr int kBlock = 256;   // threads per CTA
+constexpr int kUnroll = 4;    // 16-byte loads in flight per thread (aligned path)
+constexpr int kMaxFan = 8;    // destination replicas held in registers per pass
+
+// ------------------------------------------------------------------------------ helpers --
+
+__device__ __forceinline__ uint4 load_stream(const uint8_t *p) { return __ldcs(reinterpret_cast<const uint4 *>(p)); }
+
+__device__ __forceinline__ void store_stream(uint8_t *p, uint4 v) { __stcs(reinterpret_cast<uint4 *>(p), v); }
+
+// Bytes [sh, sh + 16) of the 32-byte concatenation lo:hi (little endian), sh in [0, 16).
+__device__ __forceinline__ uint4 shift_bytes(uint4 lo, uint4 hi, int sh) {
+  const int r = (sh & 3) * 8;
+  uint32_t x0, x1, x2, x3, x4;
+  switch (sh >> 2) {
+    case 0: x0 = lo.x; x1 = lo.y; x2 = lo.z; x3 = lo.w; x4 = hi.x; break;
+    case 1: x0 = lo.y; x1 = lo.z; x2 = lo.w; x3 = hi.x; x4 = hi.y; break;
+    case 2: x0 = lo.z; x1 = lo.w; x2 = hi.x; x3 = hi.y; x4 = hi.z; break;
+    default: x0 = lo.w; x1 = hi.x; x2 = hi.y; x3 = hi.z; x4 = hi.w; break;
+  }
+  uint4 o;
+  o.x = __funnelshift_r(x0, x1, r);
+  o.y = __funnelshift_r(x1, x2, r);
+  o.z = __funnelshift_r(x2, x3, r);
+  o.w = __funnelshift_r(x3, x4, r);
+  return o;
+}
+
+__device__ __forceinline__ uint32_t byte_of(uint4 v, int k) {
+  const uint32_t w = k < 4 ? v.x : k < 8 ? v.y : k < 12 ? v.z : v.w;
+  return (w >> ((k & 3) * 8)) & 0xFF;
+}
+
+// ------------------------------------------------------------------- copy with fan-out --
+
+// Every source, destination, run and pitch 16-byte aligned: straight 16-byte copies.
+__device__ __forceinline__ void copy_aligned(const uint8_t *__restrict__ src, uint8_t *const *dst, int nf, int rows,
+                                             int64_t run_b, int64_t sp_b, int64_t dp_b) {
+  const int nw = (int)(run_b >> 4);
+  const int total = rows * nw;
+  for (int base = threadIdx.x; base < total; base += kBlock * kUnroll) {
+    uint4 v[kUnroll];
+    int64_t doff[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int j = base + u * kBlock;
+      if (j < total) {
+        const int r = rows == 1 ? 0 : j / nw;
+        const int w = j - r * nw;
+        v[u] = load_stream(src + r * sp_b + 16 * (int64_t)w);
+        doff[u] = r * dp_b + 16 * (int64_t)w;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (base + u * kBlock < total) {
+#pragma unroll
+        for (int f = 0; f < kMaxFan; ++f)
+          if (f < nf) store_stream(dst[f] + doff[u], v[u]);
+      }
+    }
+  }
+}
+
+// General alignment: destination replicas must agree modulo 16. Each thread owns one aligned
+// 16-byte destination word, assembles it from the (at most two) aligned 16-byte source blocks
+// that hold its bytes, and stores it whole, or byte by byte at the two ends of a row. A source
+// block is loaded only when it holds at least one byte of the row, so no access leaves the
+// 16-byte blocks (and hence the pages) the region occupies.
+__device__ __forceinline__ void copy_shifted(const uint8_t *__restrict__ src, uint8_t *const *dst, int nf, int rows,
+                                             int64_t run_b, int64_t sp_b, int64_t dp_b) {
+  const int nwmax = (int)((run_b + 15) >> 4) + 1;
+  const int total = rows * nwmax;
+  for (int j = threadIdx.x; j < total; j += kBlock) {
+    const int r = j / nwmax;
+    const int w = j - r * nwmax;
+    const uintptr_t srow = reinterpret_cast<uintptr_t>(src) + r * sp_b;
+    const int64_t drow = r * dp_b;
+    const int a = (int)((reinterpret_cast<uintptr_t>(dst[0]) + drow) & 15);
+    const int64_t start = 16 * (int64_t)w - a;  // row byte of this word's byte 0
+    if (start >= run_b) continue;
+    const int kmin = start < 0 ? (int)-start : 0;
+    const int kmax = run_b - start < 16 ? (int)(run_b - start) : 16;
+    const uintptr_t p0 = srow + start;
+    const int sh = (int)(p0 & 15);
+    const uint8_t *blk = reinterpret_cast<const uint8_t *>(p0 - sh);
+    uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+    if (kmin < 16 - sh) lo = __ldg(reinterpret_cast<const uint4 *>(blk));
+    if (sh && kmax > 16 - sh) hi = __ldg(reinterpret_cast<const uint4 *>(blk + 16));
+    const uint4 o = sh ? shift_bytes(lo, hi, sh) : lo;
+    if (kmin == 0 && kmax == 16) {
+#pragma unroll
+      for (int f = 0; f < kMaxFan; ++f)
+        if (f < nf) store_stream(dst[f] + drow + start, o);
+    } else {
+#pragma unroll
+      for (int f = 0; f < kMaxFan; ++f) {
+        if (f < nf) {
+          uint8_t *word = dst[f] + drow + start;
+          for (int k = kmin; k < kmax; ++k) word[k] = (uint8_t)byte_of(o, k);
+        }
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kBlock) reshard_copy_kernel(const Item *__restrict__ items, int n_items,
+                                                              const uint64_t *__restrict__ ptrs,
+                                                              const int32_t *__restrict__ gstart,
+                                                              const int32_t *__restrict__ mptr,
+                                                              const int64_t *__restrict__ moff) {
+  for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
+    const Item it = items[i];
+    const int64_t es = it.esize;
+    const uint8_t *src = reinterpret_cast<const uint8_t *>(ptrs[it.src]) + it.src_off * es;
+    const int g0 = gstart[it.group];
+    const int nrep = gstart[it.group + 1] - g0;
+    const int64_t run_b = (int64_t)it.run * es;
+    const int64_t sp_b = it.src_pitch * es, dp_b = it.dst_pitch * es;
+    const uintptr_t geo = reinterpret_cast<uintptr_t>(src) | (uintptr_t)run_b |
+                          (it.rows > 1 ? (uintptr_t)(sp_b | dp_b) : 0);
+    for (int f0 = 0; f0 < nrep; f0 += kMaxFan) {
+      const int nf = min(kMaxFan, nrep - f0);
+      uint8_t *dst[kMaxFan];
+      uintptr_t amask = geo;
+      bool same = true;
+#pragma unroll
+      for (int f = 0; f < kMaxFan; ++f) {
+        dst[f] = nullptr;
+        if (f < nf) {
+          const int m = g0 + f0 + f;
+          dst[f] = reinterpret_cast<uint8_t *>(ptrs[mptr[m]]) + (moff[m] + it.dst_off) * es;
+          amask |= reinterpret_cast<uintptr_t>(dst[f]);
+          same = same && (((reinterpret_cast<uintptr_t>(dst[f]) ^ reinterpret_cast<uintptr_t>(dst[0])) & 15) == 0);
+        }
+      }
+      if ((amask & 15) == 0) {
+        copy_aligned(src, dst, nf, it.rows, run_b, sp_b, dp_b);
+      } else if (same) {
+        copy_shifted(src, dst, nf, it.rows, run_b, sp_b, dp_b);
+      } else {
+        for (int f = 0; f < nf; ++f) copy_shifted(src, dst + f, 1, it.rows, run_b, sp_b, dp_b);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------------ MXFP8 epilogue --
+
+// Shared E8M0 exponent X of a block from its largest BF16 magnitude (15-bit pattern, finite):
+// X = floor(log2 amax) - 8, clamped to [-127, 127]; an all-zero block takes -127.
+__device__ __forceinline__ int block_exponent(uint32_t amax) {
+  if (amax == 0) return -127;
+  const int e = (int)(amax >> 7);
+  const int lg = e ? e - 127 : -133 + (31 - __clz((int)amax));
+  return max(-127, min(127, lg - 8));
+}
+
+// Two floats -> two E4M3 bytes (RNE, saturating to +-448); `lo` lands in the low byte.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return (uint32_t)r;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t mag_max2(uint32_t w) { return max(w & 0x7FFFu, (w >> 16) & 0x7FFFu); }
+
+__global__ void __launch_bounds__(kBlock) reshard_mxfp8_kernel(const Item *__restrict__ items, int n_items,
+                                                               const uint64_t *__restrict__ ptrs,
+                                                               const int32_t *__restrict__ gstart,
+                                                               const int32_t *__restrict__ mptr,
+                                                               const int64_t *__restrict__ moff, int64_t n_dst_ptrs) {
+  const int lane = threadIdx.x & 31;
+  for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
+    const Item it = items[i];
+    const uint8_t *src = reinterpret_cast<const uint8_t *>(ptrs[it.src]) + it.src_off * 2;
+    const int g0 = gstart[it.group];
+    const int nrep = gstart[it.group + 1] - g0;
+    const int oct = it.run >> 3;  // 8-element groups per row; a multiple of 4
+    const int total = it.rows * oct;
+    const int64_t sp_b = it.src_pitch * 2;
+    const bool vec = ((reinterpret_cast<uintptr_t>(src) | (it.rows > 1 ? (uintptr_t)sp_b : 0)) & 15) == 0;
+    for (int f0 = 0; f0 < nrep; f0 += kMaxFan) {
+      const int nf = min(kMaxFan, nrep - f0);
+      uint8_t *dq[kMaxFan];
+      uint8_t *ds[kMaxFan];
+      uintptr_t amask = it.rows > 1 ? (uintptr_t)it.dst_pitch : 0;
+#pragma unroll
+      for (int f = 0; f < kMaxFan; ++f) {
+        dq[f] = nullptr;
+        ds[f] = nullptr;
+        if (f < nf) {
+          const int m = g0 + f0 + f;
+          const int64_t e0 = moff[m] + it.dst_off;  // element offset of the item in the shard buffer
+          dq[f] = reinterpret_cast<uint8_t *>(ptrs[mptr[m]]) + e0;
+          ds[f] = reinterpret_cast<uint8_t *>(ptrs[mptr[m] + n_dst_ptrs]) + e0 / 32;
+          amask |= reinterpret_cast<uintptr_t>(dq[f]);
+        }
+      }
+      const bool st8 = (amask & 7) == 0;
+      for (int j0 = threadIdx.x - lane; j0 < total; j0 += kBlock) {
+        const int j = j0 + lane;
+        const bool valid = j < total;
+        int r = 0, o = 0;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (valid) {
+          r = j / oct;
+          o = j - r * oct;
+          const uint8_t *p = src + r * sp_b + 16 * (int64_t)o;
+          if (vec) {
+            v = load_stream(p);
+          } else {
+            const uint16_t *h = reinterpret_cast<const uint16_t *>(p);
+            v.x = (uint32_t)h[0] | ((uint32_t)h[1] << 16);
+            v.y = (uint32_t)h[2] | ((uint32_t)h[3] << 16);
+            v.z = (uint32_t)h[4] | ((uint32_t)h[5] << 16);
+            v.w = (uint32_t)h[6] | ((uint32_t)h[7] << 16);
+          }
+        }
+        uint32_t amax = max(max(mag_max2(v.x), mag_max2(v.y)), max(mag_max2(v.z), mag_max2(v.w)));
+        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        if (!valid) continue;
+        uint2 q;
+        uint32_t sbyte;
+        if (amax >= 0x7F80u) {  // Inf or NaN in the block: E8M0 NaN scale, E4M3 NaN elements
+          q = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+          sbyte = 0xFF;
+        } else {
+          const int x = block_exponent(amax);
+          const float inv = __uint_as_float((uint32_t)(127 - x) << 23);  // 2^-X, X in [-127, 119]
+          q.x = cvt_e4m3x2(bf16_lo(v.x) * inv, bf16_hi(v.x) * inv) |
+                (cvt_e4m3x2(bf16_lo(v.y) * inv, bf16_hi(v.y) * inv) << 16);
+          q.y = cvt_e4m3x2(bf16_lo(v.z) * inv, bf16_hi(v.z) * inv) |
+                (cvt_e4m3x2(bf16_lo(v.w) * inv, bf16_hi(v.w) * inv) << 16);
+          sbyte = (uint32_t)(x + 127);
+        }
+        const int64_t eoff = r * it.dst_pitch + 8 * (int64_t)o;  // element offset within the item
+#pragma unroll
+        for (int f = 0; f < kMaxFan; ++f) {
+          if (f < nf) {
+            uint8_t *p = dq[f] + eoff;
+            if (st8) {
+              __stcs(reinterpret_cast<uint2 *>(p), q);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) p[k] = (uint8_t)(q.x >> (8 * k));
+#pragma unroll
+              for (int k = 0; k < 4; ++k) p[4 + k] = (uint8_t)(q.y >> (8 * k));
+            }
+            if ((lane & 3) == 0) ds[f][eoff / 32] = (uint8_t)sbyte;
+          }
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------- host side --
+
+int cuda_fail(cudaError_t e, const char *what) {
+  return fail(e == cudaErrorMemoryAllocation ? RESHARD_ERR_OOM : RESHARD_ERR_CUDA,
+              std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+#define RS_CUDA(call)                                   \
+  do {                                                  \
+    cudaError_t e_ = (call);                            \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
+  } while (0)
+
+template <typename T>
+int upload(T **dptr, const std::vector<T> &host) {
+  if (host.empty()) return RESHARD_OK;
+  RS_CUDA(cudaMalloc(reinterpret_cast<void **>(dptr), host.size() * sizeof(T)));
+  RS_CUDA(cudaMemcpy(*dptr, host.data(), host.size() * sizeof(T), cudaMemcpyHostToDevice));
+  return RESHARD_OK;
+}
+
+struct LaunchCaps {
+  int device = -1;
+  int copy_grid = 0;
+  int mxfp8_grid = 0;
+};
+thread_local LaunchCaps g_caps;
+
+int launch_caps(int device, LaunchCaps &c) {
+  if (g_caps.device == device) {
+    c = g_caps;
+    return RESHARD_OK;
+  }
+  int sms = 0, b1 = 0, b2 = 0;
+  RS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device));
+  RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, reshard_copy_kernel, kBlock, 0));
+  RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b2, reshard_mxfp8_kernel, kBlock, 0));
+  g_caps.device = device;
+  g_caps.copy_grid = sms * std::max(1, b1);
+  g_caps.mxfp8_grid = sms * std::max(1, b2);
+  c = g_caps;
+  return RESHARD_OK;
+}
+
+int bind_device(reshard_plan_t *p) {
+  int dev = 0;
+  RS_CUDA(cudaGetDevice(&dev));
+  if (p->device >= 0) {
+    if (dev != p->device)
+      return fail(RESHARD_ERR_INVALID_ARG, "plan was bound to device " + std::to_string(p->device) +
+                                               " by its first execute; current device is " + std::to_string(dev));
+    return RESHARD_OK;
+  }
+  int rc;
+  if ((rc = upload(&p->d_grp_start, p->grp_start))) return rc;
+  if ((rc = upload(&p->d_mem_ptr, p->mem_ptr))) return rc;
+  if ((rc = upload(&p->d_mem_off, p->mem_off))) return rc;
+  RS_CUDA(cudaMalloc(reinterpret_cast<void **>(&p->d_ptrs), pointer_table_size(p) * sizeof(uint64_t)));
+  p->device = dev;
+  return RESHARD_OK;
+}
+
+int ensure_items(reshard_plan_t *p, int set) {
+  if (p->d_items[set] || p->items[set].empty()) return RESHARD_OK;
+  Item *d = nullptr;
+  int rc = upload(&d, p->items[set]);
+  p->d_items[set] = d;
+  return rc;
+}
+
+int launch(reshard_plan_t *p, int set, bool quant, cudaStream_t stream, const LaunchCaps &caps) {
+  const int n = (int)p->items[set].size();
+  if (n == 0) return RESHARD_OK;
+  int rc = ensure_items(p, set);
+  if (rc) return rc;
+  const Item *items = static_cast<const Item *>(p->d_items[set]);
+  if (quant) {
+    const int grid = std::min(n, caps.mxfp8_grid);
+    reshard_mxfp8_kernel<<<grid, kBlock, 0, stream>>>(items, n, p->d_ptrs, p->d_grp_start, p->d_mem_ptr,
+                                                      p->d_mem_off, p->n_dst_ptrs);
+  } else {
+    const int grid = std::min(n, caps.copy_grid);
+    reshard_copy_kernel<<<grid, kBlock, 0, stream>>>(items, n, p->d_ptrs, p->d_grp_start, p->d_mem_ptr,
+                                                     p->d_mem_off);
+  }
+  RS_CUDA(cudaGetLastError());
+  return RESHARD_OK;
+}
+
+void free_device(reshard_plan_t *p) {
+  for (auto &d : p->d_items) {
+    if (d) cudaFree(d);
+    d = nullptr;
+  }
+  if (p->d_grp_start) cudaFree(p->d_grp_start);
+  if (p->d_mem_ptr) cudaFree(p->d_mem_ptr);
+  if (p->d_mem_off) cudaFree(p->d_mem_off);
+  if (p->d_ptrs) cudaFree(p->d_ptrs);
+  if (p->d_workspace) cudaFree(p->d_workspace);
+  p->d_grp_start = nullptr;
+  p->d_mem_ptr = nullptr;
+  p->d_mem_off = nullptr;
+  p->d_ptrs = nullptr;
+  p->d_workspace = nullptr;
+}
+
+}  // namespace
+}  // namespace reshard
+
+using namespace reshard;
+
+extern "C" int reshard_execute(reshard_plan_t *p, void *const *src_ptrs, void *const *dst_ptrs, int mode, int quant,
+                               reshard_stream_t stream_) {
+  if (!p) return fail(RESHARD_ERR_INVALID_ARG, "plan is NULL");
+  if (mode != RESHARD_DIRECT && mode != RESHARD_PACKED) return fail(RESHARD_ERR_INVALID_ARG, "unknown mode");
+  if (quant != RESHARD_QUANT_NONE && quant != RESHARD_QUANT_MXFP8) return fail(RESHARD_ERR_INVALID_ARG, "unknown quant");
+  if (quant == RESHARD_QUANT_MXFP8 && !p->quant_ok) return fail(RESHARD_ERR_UNSUPPORTED, p->quant_why);
+  if (p->regions.empty()) return RESHARD_OK;
+  if ((p->n_src_ptrs && !src_ptrs) || (p->n_dst_ptrs && !dst_ptrs))
+    return fail(RESHARD_ERR_INVALID_ARG, "src_ptrs or dst_ptrs is NULL");
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+
+  // pointer table: [sources | destination data | destination scales | workspace]
+  const int64_t Ns = p->n_src_ptrs, Nd = p->n_dst_ptrs;
+  std::vector<uint64_t> table((size_t)pointer_table_size(p), 0);
+  std::string missing;
+  int n_missing = 0;
+  for (size_t ti = 0; ti < p->tensors.size(); ++ti) {
+    const TensorInfo &t = p->tensors[ti];
+    for (int64_t r = 0; r < t.n_src; ++r) {
+      void *ptr = src_ptrs[t.src_base + r];
+      table[(size_t)(t.src_base + r)] = reinterpret_cast<uint64_t>(ptr);
+      const Box &b = t.src_box[(size_t)r];
+      bool empty = false;
+      for (int d = 0; d < t.ndim; ++d) empty = empty || b.hi[d] <= b.lo[d];
+      if (!ptr && !empty && n_missing++ < 8)
+        missing += "\n  tensor " + std::to_string(ti) + ": source pointer " + std::to_string(r) + " is NULL";
+    }
+    for (int64_t r = 0; r < t.n_dst; ++r) {
+      const int64_t flat = t.dst_base + r;
+      void *data = quant ? dst_ptrs[2 * flat] : dst_ptrs[flat];
+      void *scale = quant ? dst_ptrs[2 * flat + 1] : nullptr;
+      table[(size_t)(Ns + flat)] = reinterpret_cast<uint64_t>(data);
+      table[(size_t)(Ns + Nd + flat)] = reinterpret_cast<uint64_t>(scale);
+      const Box &b = t.dst_box[(size_t)r];
+      bool empty = false;
+      for (int d = 0; d < t.ndim; ++d) empty = empty || b.hi[d] <= b.lo[d];
+      if (!empty && (!data || (quant && !scale)) && n_missing++ < 8)
+        missing += "\n  tensor " + std::to_string(ti) + ": destination pointer " + std::to_string(r) + " is NULL";
+    }
+  }
+  if (n_missing) return fail(RESHARD_ERR_INVALID_ARG, std::to_string(n_missing) + " NULL pointer(s):" + missing);
+
+  int rc = bind_device(p);
+  if (rc) return rc;
+  LaunchCaps caps;
+  if ((rc = launch_caps(p->device, caps))) return rc;
+  if (mode == RESHARD_PACKED && !p->d_workspace && p->stats.message_bytes > 0)
+    RS_CUDA(cudaMalloc(&p->d_workspace, (size_t)p->stats.message_bytes));
+  table[(size_t)p->workspace_ptr] = reinterpret_cast<uint64_t>(p->d_workspace);
+
+  if (!p->ptr_cache_valid || p->ptr_cache != table) {
+    // pageable source: the runtime stages the bytes before returning, so `table` may die
+    RS_CUDA(cudaMemcpyAsync(p->d_ptrs, table.data(), table.size() * sizeof(uint64_t), cudaMemcpyHostToDevice, stream));
+    p->ptr_cache = std::move(table);
+    p->ptr_cache_valid = true;
+  }
+  const bool q = quant == RESHARD_QUANT_MXFP8;
+  if (mode == RESHARD_DIRECT) return launch(p, kDirect, q, stream, caps);
+  if ((rc = launch(p, kPack, false, stream, caps))) return rc;
+  return launch(p, kUnpack, q, stream, caps);
+}
+
+extern "C" int reshard_plan_destroy(reshard_plan_t *p) {
+  if (!p) return RESHARD_OK;
+  if (p->device >= 0) {
+    int cur = 0;
+    cudaGetDevice(&cur);
+    cudaSetDevice(p->device);
+    free_device(p);
+    cudaSetDevice(cur);
+  }
+  delete p;
+  return RESHARD_OK;
+}

@@ -1,0 +1,114 @@
+// Internal plan representation shared by the host planner (plan.cpp) and the device executor
+// (execute.cu). Not part of the public ABI (include/reshard.h).
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/reshard.h"
+
+namespace reshard {
+
+constexpr int kMaxDims = RESHARD_MAX_DIMS;
+
+// Source bytes per device work item. Regions are cut into items of about this size so a
+// persistent grid that walks the item table round-robin stays balanced.
+constexpr int64_t kItemBytes = 256 * 1024;
+// Long runs are cut at multiples of this many elements (keeps MXFP8 blocks whole).
+constexpr int64_t kRunSplitElems = 2048;
+
+// Half-open box [lo, hi) per tensor dim.
+struct Box {
+  int64_t lo[kMaxDims];
+  int64_t hi[kMaxDims];
+};
+
+// A rank's local shard inside its buffer (elements).
+struct RankView {
+  int64_t offset = 0;
+  int64_t strides[kMaxDims] = {0, 0, 0, 0};
+  bool dense = true;  // strides were not given (dense row-major of the local shape)
+};
+
+// Device work item: `rows` rows of `run` contiguous elements. Row i of the source starts at
+// element src_off + i * src_pitch of pointer `src`; row i of destination replica m starts at
+// element member_offset[m] + dst_off + i * dst_pitch of that member's pointer.
+struct alignas(16) Item {
+  int64_t src_off;
+  int64_t dst_off;
+  int64_t src_pitch;
+  int64_t dst_pitch;
+  int32_t rows;
+  int32_t run;
+  int32_t src;    // pointer-table index of the source buffer
+  int32_t group;  // destination group (replica set) index
+  int32_t esize;  // bytes per element of the tensor
+  int32_t pad[3];
+};
+static_assert(sizeof(Item) == 64, "work item is one 64-byte descriptor");
+
+struct TensorInfo {
+  int ndim = 0;
+  int64_t shape[kMaxDims] = {1, 1, 1, 1};
+  int dtype = 0;
+  int esize = 0;
+  int64_t n_src = 0, n_dst = 0;        // ranks on each side
+  int64_t src_base = 0, dst_base = 0;  // first pointer index of this tensor (flat, per side)
+  std::vector<Box> src_box, dst_box;   // per pointer index
+  std::vector<RankView> src_view, dst_view;
+};
+
+struct Region {
+  int32_t tensor;
+  int32_t src;    // pointer index within the tensor's source run (the chosen holder)
+  int32_t group;  // plan-wide destination group id
+  Box box;        // global coordinates
+  int64_t msg_off_bytes = 0;  // packed-mode workspace offset (16-byte aligned)
+};
+
+struct Group {
+  int32_t tensor;
+  std::vector<int32_t> members;  // destination pointer indices within the tensor's run
+  Box box;
+};
+
+enum ItemSet { kDirect = 0, kPack = 1, kUnpack = 2, kNumSets = 3 };
+
+}  // namespace reshard
+
+struct reshard_plan {
+  std::vector<reshard::TensorInfo> tensors;
+  std::vector<reshard::Region> regions;
+  std::vector<reshard::Group> groups;  // plan-wide; one extra group for the workspace is
+                                       // appended in the device tables
+  int64_t n_src_ptrs = 0, n_dst_ptrs = 0;
+  std::vector<reshard::Item> items[reshard::kNumSets];
+  // group table (device layout): members of group g are [grp_start[g], grp_start[g + 1])
+  std::vector<int32_t> grp_start;
+  std::vector<int32_t> mem_ptr;   // pointer-table index of each member's data pointer
+  std::vector<int64_t> mem_off;   // member's view offset (elements)
+  int32_t workspace_group = -1;
+  int64_t workspace_ptr = -1;     // pointer-table index of the workspace
+  int max_fanout = 0;
+  reshard_stats_t stats{};
+  bool quant_ok = false;
+  std::string quant_why;
+
+  // device state (bound at the first execute)
+  int device = -1;
+  void *d_items[reshard::kNumSets] = {nullptr, nullptr, nullptr};
+  int32_t *d_grp_start = nullptr;
+  int32_t *d_mem_ptr = nullptr;
+  int64_t *d_mem_off = nullptr;
+  uint64_t *d_ptrs = nullptr;
+  void *d_workspace = nullptr;
+  std::vector<uint64_t> ptr_cache;
+  bool ptr_cache_valid = false;
+};
+
+namespace reshard {
+void set_error(const std::string &msg);
+int fail(int code, const std::string &msg);
+int64_t pointer_table_size(const reshard_plan *p);  // Ns + 2 Nd + 1
+}  // namespace reshard

@@ -1,0 +1,219 @@
+/*
+ * reshard.h -- C ABI of the single-GPU DTensor -> DTensor reshard executor (libreshard.so).
+ *
+ * The operation is the Reshard collective: move a tensor's values from a source distribution
+ * (M local shards over a device mesh with Shard/Replicate placements) to a destination
+ * distribution (N local shards, possibly replicated), sending only the regions where source
+ * and destination shards overlap and reading each region once even when several destination
+ * replicas need it. Definitions used below:
+ *  - news article on NVIDIA's Reshard collective, sections "Recasting refit as a
+ *    DTensor-to-DTensor transfer" and "The Reshard collective";
+ *  - NeMo-RL design doc "NCCL Reshard Refit (Experimental)": "Execution Flow: Setup Time"
+ *    (global shape, dtype, MeshInfo, Shard/Replicate placements), "xferdtensor Transports"
+ *    (exact overlaps, each destination region moved once, fan-out to replicas, the stream
+ *    argument), "Enabling It" (BF16 -> MXFP8 on the receive side, one ValueError listing every
+ *    violation);
+ *  - "NeMo-RL: Optimizing Non-Colocated Refit for Asynchronous RL", "Optimization #2"
+ *    (coalesce many tensors into one call; pack into contiguous messages).
+ *
+ * In this library all M source and N destination shards are separate buffers on ONE GPU,
+ * so "sending" a region is a device copy. The work is split into a host-side plan (built once,
+ * cached: "descriptor caching" in the ModelExpress reshard PR) and an asynchronous execute.
+ *
+ * Conventions
+ *  - All sizes, offsets and strides are in ELEMENTS of the tensor's dtype unless named _bytes.
+ *  - Ranks are numbered row-major over mesh coordinates. mesh.ranks, when given, maps the
+ *    row-major position to the index of that rank's pointer in the execute pointer arrays
+ *    (a permutation of 0..n-1); NULL means the identity.
+ *  - Uneven splits follow torch.chunk: chunk = ceil(L / n), rank i holds
+ *    [min(i chunk, L), min((i + 1) chunk, L)); trailing ranks may hold nothing.
+ *  - Several mesh dims sharding one tensor dim split in mesh-dim order (nested).
+ *  - Errors: every call returns 0 (RESHARD_OK) or a negative RESHARD_ERR_* code, and
+ *    reshard_last_error() then describes it. Validation lists EVERY violation it finds, one
+ *    per line, and fails closed: no plan is returned.
+ *  - Thread safety: plans are not locked. Calls on different plans may run concurrently; calls
+ *    on one plan must be serialised by the caller. The error text is per thread.
+ */
+#ifndef RESHARD_H
+#define RESHARD_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RESHARD_MAX_DIMS 4      /* tensor dims */
+#define RESHARD_MAX_MESH_DIMS 4 /* device-mesh dims */
+
+/* return codes */
+#define RESHARD_OK 0
+#define RESHARD_ERR_INVALID_ARG (-1) /* malformed spec, pointer or argument */
+#define RESHARD_ERR_UNSUPPORTED (-2) /* well formed but outside what the executor handles */
+#define RESHARD_ERR_CUDA (-3)        /* a CUDA runtime call failed (message has the name) */
+#define RESHARD_ERR_OOM (-4)         /* host or device allocation failed */
+#define RESHARD_ERR_COVERAGE (-5)    /* the plan would leave destination elements unwritten */
+
+/* placement kinds (DTensor Shard(dim) / Replicate()) */
+#define RESHARD_REPLICATE 0
+#define RESHARD_SHARD 1
+
+/* element types. Copies move bytes, so every type is bit-exact; only BF16 can be quantized. */
+#define RESHARD_U8 0
+#define RESHARD_BF16 1
+#define RESHARD_F16 2
+#define RESHARD_F32 3
+#define RESHARD_I32 4
+#define RESHARD_I64 5
+
+/* execute modes */
+#define RESHARD_DIRECT 0 /* one pass: source regions straight into every destination replica */
+#define RESHARD_PACKED 1 /* pack per-(source, destination group) messages, then unpack them */
+
+/* receive-side quantization */
+#define RESHARD_QUANT_NONE 0
+#define RESHARD_QUANT_MXFP8 1 /* BF16 -> E4M3 bytes + one E8M0 scale byte per 32 elements */
+
+/* Opaque CUDA stream; pass a cudaStream_t (NULL = the legacy default stream). */
+struct CUstream_st;
+typedef struct CUstream_st *reshard_stream_t;
+
+/* Device mesh ("MeshInfo"): an ndim-dimensional grid of ranks. */
+typedef struct {
+  int ndim;              /* 1..RESHARD_MAX_MESH_DIMS */
+  const int64_t *shape;  /* ndim extents, each >= 1 */
+  const int32_t *ranks;  /* prod(shape) pointer indices (a permutation), or NULL = identity */
+} reshard_mesh_t;
+
+/* One placement per mesh dim. */
+typedef struct {
+  int kind; /* RESHARD_SHARD or RESHARD_REPLICATE */
+  int dim;  /* sharded tensor dim for RESHARD_SHARD; ignored for RESHARD_REPLICATE */
+} reshard_placement_t;
+
+/* Where a rank's local shard sits in its buffer ("DTensorRef" local tensor, or a slice of a
+ * fused parameter such as gate_up: design doc, "Execution Flow: Setup Time").
+ * The element at local index i is at buffer element offset_elems + sum_d i[d] * strides[d]. */
+typedef struct {
+  int64_t offset_elems;          /* >= 0 */
+  const int64_t *strides_elems;  /* ndim strides, innermost must be 1; NULL = dense row-major */
+  int64_t capacity_elems;        /* elements the buffer holds (bounds check); 0 = not checked */
+} reshard_view_t;
+
+/* One tensor: the DTensor description on both sides. */
+typedef struct {
+  int ndim;                      /* 1..RESHARD_MAX_DIMS */
+  const int64_t *global_shape;   /* ndim extents, each >= 0 */
+  int dtype;                     /* RESHARD_U8 .. RESHARD_I64 */
+  reshard_mesh_t src_mesh;
+  const reshard_placement_t *src_pl;  /* src_mesh.ndim placements */
+  const reshard_view_t *src_views;    /* prod(src_mesh.shape) views (pointer-index order) or NULL */
+  reshard_mesh_t dst_mesh;
+  const reshard_placement_t *dst_pl;
+  const reshard_view_t *dst_views;
+} reshard_tensor_spec_t;
+
+typedef struct reshard_plan reshard_plan_t;
+
+/* Plan statistics (the byte accounting of the ModelExpress reshard PR, "MoE Qwen3-30B-A3B:
+ * expert coverage": planned wire bytes vs engine bytes, exact descriptor count). */
+typedef struct {
+  int64_t n_tensors;
+  int64_t regions;            /* (source, destination group) overlaps, each moved once */
+  int64_t items;              /* device work items of the direct mode */
+  int64_t dst_groups;         /* destination replica groups (distinct destination boxes) */
+  int64_t messages;           /* (source rank, destination group) pairs with data */
+  int64_t bytes_read;         /* source bytes read per direct execute */
+  int64_t bytes_written;      /* destination bytes written per execute (unquantized) */
+  int64_t wire_bytes;         /* bytes a wire transport would carry: each region once */
+  int64_t message_bytes;      /* packed-mode workspace: messages with 16-byte aligned regions */
+  int64_t gather_bcast_bytes; /* all-gather + broadcast payload for comparison: 2 x tensor bytes */
+  int64_t global_bytes;       /* sum of global tensor bytes */
+} reshard_stats_t;
+
+/*
+ * reshard_plan_create -- plan one tensor's reshard (host only; touches no GPU).
+ * spec: the tensor; read during the call only.  out: receives the plan (caller destroys it).
+ * Steps: every rank's box by the chunk rule; replica groups of identical boxes on each side;
+ * per-dim intersection of every source group with every destination group; one source per
+ * region (the lowest pointer index of the source group); work items for the device.
+ * Errors: INVALID_ARG / UNSUPPORTED listing every violation; OOM.
+ */
+int reshard_plan_create(const reshard_tensor_spec_t *spec, reshard_plan_t **out);
+
+/*
+ * reshard_plan_batch -- one plan over n_tensors tensors, executed by one launch per pass.
+ * Pointer arrays of the execute are the per-tensor arrays concatenated in spec order: tensor t
+ * owns prod(src_mesh.shape) consecutive source pointers and prod(dst_mesh.shape) consecutive
+ * destination pointers (two per rank under MXFP8, see reshard_execute).
+ */
+int reshard_plan_batch(const reshard_tensor_spec_t *specs, int n_tensors, reshard_plan_t **out);
+
+/*
+ * reshard_execute -- enqueue the reshard on `stream` and return (asynchronous).
+ * src_ptrs / dst_ptrs: HOST arrays of DEVICE pointers, caller-owned, laid out as above. A rank
+ *   whose shard is empty may pass NULL. Under RESHARD_QUANT_MXFP8 dst_ptrs holds two entries
+ *   per destination rank: the E4M3 data buffer (1 byte per element, dense row-major of the
+ *   local shape, at element offset offset_elems) and the E8M0 scale buffer (1 byte per 32
+ *   elements, row-major [..., K_local / 32], at offset_elems / 32).
+ * mode: RESHARD_DIRECT or RESHARD_PACKED.  quant: RESHARD_QUANT_NONE or RESHARD_QUANT_MXFP8
+ *   (BF16 tensors only; every destination's last local dim and every region boundary along it
+ *   a multiple of 32; dense destination views; otherwise UNSUPPORTED).
+ * The first execute binds the plan to the current device and uploads its descriptor tables
+ * (synchronous device allocations: do it outside stream capture); RESHARD_PACKED also
+ * allocates the message workspace (stats.message_bytes) on first use. The pointer table is
+ * re-uploaded on `stream` only when the pointers differ from the previous call's.
+ * Buffers must stay valid until the stream reaches the end of the work. Executes of one plan
+ * on different streams that overlap in time race on its tables and workspace.
+ * Errors: INVALID_ARG (NULL pointer for a non-empty shard, other device), UNSUPPORTED,
+ *   CUDA (launch or copy failure), OOM. After an error the destinations are undefined.
+ */
+int reshard_execute(reshard_plan_t *plan, void *const *src_ptrs, void *const *dst_ptrs, int mode,
+                    int quant, reshard_stream_t stream);
+
+/* reshard_plan_stats -- fill *out (host only). */
+int reshard_plan_stats(const reshard_plan_t *plan, reshard_stats_t *out);
+
+/*
+ * reshard_plan_regions -- copy up to `cap` planned regions into host arrays (introspection for
+ * tests and tools). Per region i: tensor[i], src_rank[i] (pointer index of the chosen source),
+ * dst_group[i] (plan-wide group id), and box lo/hi in global coordinates at
+ * lo[i * RESHARD_MAX_DIMS + d], hi[...]. Any array may be NULL. *n_out gets the region count.
+ */
+int reshard_plan_regions(const reshard_plan_t *plan, int64_t cap, int32_t *tensor, int32_t *src_rank,
+                         int32_t *dst_group, int64_t *lo, int64_t *hi, int64_t *n_out);
+
+/*
+ * reshard_plan_group_members -- destination pointer indices (within the tensor's run) of group
+ * g. *n_out gets the member count; up to cap are written to members.
+ */
+int reshard_plan_group_members(const reshard_plan_t *plan, int64_t g, int64_t cap, int32_t *members,
+                               int64_t *n_out);
+
+/*
+ * reshard_plan_items -- copy the device work-item table of one pass (0 = direct, 1 = pack,
+ * 2 = unpack) for inspection. Each item is 64 bytes: int64 src_off, dst_off, src_pitch,
+ * dst_pitch (elements); int32 rows, run (elements per row), src (pointer-table index), group,
+ * esize (bytes), 3 x int32 padding. Item i moves `rows` rows of `run` elements from
+ * src_off + r * src_pitch of pointer `src` to member_offset + dst_off + r * dst_pitch of every
+ * member pointer of `group`. Pointer table: [sources | destination data | destination scales |
+ * packed workspace]. Up to cap items go to `items` (may be NULL); *n_out gets the count.
+ * Groups: group_start (n_groups + 2 entries incl. the workspace group), member_ptr and
+ * member_off (elements) are copied when non-NULL; *n_groups_out / *n_members_out get sizes.
+ */
+int reshard_plan_items(const reshard_plan_t *plan, int set, int64_t cap, void *items, int64_t *n_out,
+                       int32_t *group_start, int32_t *member_ptr, int64_t *member_off, int64_t *n_groups_out,
+                       int64_t *n_members_out);
+
+/* reshard_plan_destroy -- free the plan's host tables, device tables and workspace.
+ * Safe on NULL. The caller must make sure no enqueued execute of the plan is still running. */
+int reshard_plan_destroy(reshard_plan_t *plan);
+
+/* reshard_last_error -- text of this thread's last error ("" if none). Valid until the next
+ * call on the same thread. */
+const char *reshard_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RESHARD_H */

@@ -258,7 +258,8 @@ def byte_accounting(desc) -> Dict[str, int]:
     for coord in mesh_coords(desc.dst_mesh):
         box = tuple(shard_box(desc.global_shape, desc.dst_mesh, desc.dst_placements, coord))
         written += box_numel(box) * es
-        boxes.add(box)
+        if box_numel(box):
+            boxes.add(box)   # a replica group is a set of ranks sharing one non-empty box
     read = sum(box_numel(b) * es for b in boxes)
     total = int(np.prod(desc.global_shape)) * es
     return {"bytes_written": written, "bytes_read": read, "gather_bcast_bytes": 2 * total,

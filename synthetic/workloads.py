@@ -81,13 +81,13 @@ class Workload:
     dst_buffer_dtype: List[str] = field(default_factory=list)
 
     def src_bytes(self) -> int:
-        return sum(n * DTYPES[d][1] for n, d in zip(self.src_buffer_numel, self.src_buffer_dtype))
+        return sum(n * DTYPES[d][1] for n, d in zip(self.src_buffer_numel, self.src_buffer_dtype) if n)
 
     def dst_bytes(self) -> int:
         """Bytes of every destination buffer (data, plus scales under mxfp8)."""
         if self.quant == "mxfp8":
             return sum(n + n // 32 for n in self.dst_buffer_numel)
-        return sum(n * DTYPES[d][1] for n, d in zip(self.dst_buffer_numel, self.dst_buffer_dtype))
+        return sum(n * DTYPES[d][1] for n, d in zip(self.dst_buffer_numel, self.dst_buffer_dtype) if n)
 
 
 # ----------------------------------------------------------------------------------------
@@ -370,11 +370,11 @@ def _carve(sizes: List[int], align: int, misalign: int) -> Tuple[List[int], int]
 def allocate(wl: Workload, device, align: int = 256, misalign: int = 0, pin: bool = False) -> Layout:
     """Carve every buffer out of one slab per side. ``misalign`` shifts each buffer's start
     by that many bytes past an ``align`` boundary (to exercise unaligned pointers)."""
-    sb = [n * DTYPES[d][1] for n, d in zip(wl.src_buffer_numel, wl.src_buffer_dtype)]
+    sb = [n * DTYPES[d][1] if n else 0 for n, d in zip(wl.src_buffer_numel, wl.src_buffer_dtype)]
     if wl.quant == "mxfp8":
         db = list(wl.dst_buffer_numel)
     else:
-        db = [n * DTYPES[d][1] for n, d in zip(wl.dst_buffer_numel, wl.dst_buffer_dtype)]
+        db = [n * DTYPES[d][1] if n else 0 for n, d in zip(wl.dst_buffer_numel, wl.dst_buffer_dtype)]
     so, stot = _carve(sb, align, misalign)
     do, dtot = _carve(db, align, misalign)
     kw = dict(dtype=torch.uint8, device=device)

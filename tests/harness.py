@@ -1,0 +1,128 @@
+"""Shared test helpers: run a workload through the C ABI on the GPU and compare with the oracle."""
+from __future__ import annotations
+
+import itertools
+
+import numpy as np
+import torch
+
+import dtensor_resharding_gb300 as R
+import synthetic as S
+from oracle import coracle, golden as G
+
+
+def run_gpu(wl, mode="direct", misalign=0, plan=None, execute=True):
+    """Allocate, fill sources and canary, plan and execute on cuda. Returns (layout, plan)."""
+    lay = S.allocate(wl, "cuda", misalign=misalign)
+    S.fill_sources(wl, lay)
+    S.fill_canary(lay)
+    plan = plan or R.plan_workload(wl)
+    if execute:
+        sp, dp = R.workload_pointers(wl, lay)
+        R.reshard_execute(plan, sp, dp, mode=mode, quant=wl.quant, stream=torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+    return lay, plan
+
+
+def oracle_expected(wl, lay):
+    """Host expectation of the whole destination (and scale) slab: canary outside the views."""
+    src = lay.src_slab.cpu().numpy()
+    want = np.full(lay.dst_slab.numel(), 0xA5, np.uint8)
+    wsc = np.full(lay.scale_slab.numel(), 0xA5, np.uint8) if lay.scale_slab is not None else None
+    coracle.run_workload(wl, src, lay.src_off, want, lay.dst_off, wsc, lay.scale_off)
+    return want, wsc
+
+
+def assert_matches_oracle(wl, lay):
+    want, wsc = oracle_expected(wl, lay)
+    got = lay.dst_slab.cpu().numpy()
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, f"{wl.name}: {bad.size} destination bytes differ, first at {bad[:8]}"
+    if wsc is not None:
+        gs = lay.scale_slab.cpu().numpy()
+        bad = np.nonzero(gs != wsc)[0]
+        assert bad.size == 0, f"{wl.name}: {bad.size} scale bytes differ, first at {bad[:8]}"
+
+
+def _gather(slab: torch.Tensor, offsets: np.ndarray, nbytes: int) -> np.ndarray:
+    idx = torch.from_numpy((offsets[:, None] + np.arange(nbytes)[None, :]).reshape(-1)).to(slab.device)
+    return slab[idx].cpu().numpy().reshape(len(offsets), nbytes)
+
+
+def _dst_shape(t, r):
+    return G.box_shape(G.shard_box(t.global_shape, t.dst_mesh, t.dst_placements, G.mesh_coords(t.dst_mesh)[r]))
+
+
+def _src_shape(t, s):
+    return G.box_shape(G.shard_box(t.global_shape, t.src_mesh, t.src_placements, G.mesh_coords(t.src_mesh)[s]))
+
+
+def sampled_check(wl, lay, per_tensor=8, seed=0, max_tensors=None):
+    """Sampled parity at full size: the oracle maps each sampled destination element to the
+    source element that must supply it; the bytes must be equal (copy workloads)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    tids = range(len(wl.tensors))
+    if max_tensors and len(wl.tensors) > max_tensors:
+        tids = sorted(rng.choice(len(wl.tensors), size=max_tensors, replace=False))
+    src_off, dst_off, es_list = [], [], []
+    for ti in tids:
+        t = wl.tensors[ti]
+        es = G.ESIZE[t.dtype]
+        for _ in range(per_tensor):
+            r = int(rng.integers(0, t.n_dst))
+            shp = _dst_shape(t, r)
+            if int(np.prod(shp)) == 0:
+                continue
+            idx = tuple(int(rng.integers(0, n)) for n in shp)
+            s, sidx = G.dst_element_source(t, r, idx)
+            sv, dv = t.src_views[s], t.dst_views[r]
+            src_off.append(lay.src_off[sv.buffer] + es * G.element_offset(sv, _src_shape(t, s), sidx))
+            dst_off.append(lay.dst_off[dv.buffer] + es * G.element_offset(dv, shp, idx))
+            es_list.append(es)
+    assert len(set(es_list)) == 1
+    es = es_list[0]
+    a = _gather(lay.src_slab, np.array(src_off, np.int64), es)
+    b = _gather(lay.dst_slab, np.array(dst_off, np.int64), es)
+    bad = np.nonzero((a != b).any(axis=1))[0]
+    assert bad.size == 0, f"{wl.name}: {bad.size} of {len(a)} sampled elements differ"
+    return len(a)
+
+
+def sampled_check_mxfp8(wl, lay, per_tensor=8, seed=0):
+    """Sampled parity of MXFP8 blocks: the oracle gathers the block's 32 source elements one by
+    one and quantizes them; the 32 E4M3 bytes and the E8M0 byte must be equal."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    n = 0
+    for t in wl.tensors:
+        for _ in range(per_tensor):
+            r = int(rng.integers(0, t.n_dst))
+            shp = _dst_shape(t, r)
+            outer = tuple(int(rng.integers(0, x)) for x in shp[:-1])
+            b = int(rng.integers(0, shp[-1] // 32))
+            offs = []
+            for i in range(32):
+                idx = outer + (32 * b + i,)
+                s, sidx = G.dst_element_source(t, r, idx)
+                sv = t.src_views[s]
+                offs.append(lay.src_off[sv.buffer] + 2 * G.element_offset(sv, _src_shape(t, s), sidx))
+            vals = _gather(lay.src_slab, np.array(offs, np.int64), 2)
+            bits = [int(v[0]) | (int(v[1]) << 8) for v in vals]
+            codes, scale = coracle.mxfp8_block(bits)
+            dv = t.dst_views[r]
+            e0 = G.element_offset(dv, shp, outer + (32 * b,))
+            got = _gather(lay.dst_slab, np.array([lay.dst_off[dv.buffer] + e0], np.int64), 32)[0]
+            gs = _gather(lay.scale_slab, np.array([lay.scale_off[dv.buffer] + e0 // 32], np.int64), 1)[0, 0]
+            assert list(got) == codes and int(gs) == scale, (t.name, r, outer, b)
+            n += 1
+    return n
+
+
+def round_trip_desc(t):
+    return S.TensorDesc(t.name + ".back", t.global_shape, t.dtype, t.dst_mesh, t.dst_placements,
+                        t.src_mesh, t.src_placements, t.dst_views, t.src_views, t.seed, t.std)
+
+
+def free(*objs):
+    for o in objs:
+        del o
+    torch.cuda.empty_cache()

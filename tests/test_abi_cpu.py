@@ -1,0 +1,175 @@
+"""The C ABI on the host (no GPU): exported symbols, the planner against the oracle, validation."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import dtensor_resharding_gb300 as R
+import synthetic as S
+from oracle import golden as G
+
+from conftest import ROOT, read_fixture
+
+
+def test_library_exports_every_declared_symbol():
+    hdr = open(os.path.join(ROOT, "include", "reshard.h")).read()
+    declared = set(re.findall(r"^(?:int|const char \*)\s*(reshard_\w+)\(", hdr, flags=re.M))
+    assert declared == set(R.EXPORTED)
+    for name in declared:
+        assert hasattr(R.binding.LIB, name)
+        assert callable(getattr(R, name))
+
+
+def _planner_regions(plan):
+    out = []
+    for t, s, g, box in R.reshard_plan_regions(plan):
+        members = tuple(R.reshard_plan_group_members(plan, g))
+        out.append((t, members, s, box))
+    return out
+
+
+def test_planner_8x8_example_regions():
+    rows, _ = read_fixture("example_8x8.txt")
+    want = sorted(((int(d),), int(s), ((int(r0), int(r1)), (int(c0), int(c1)))) for d, s, r0, r1, c0, c1 in rows)
+    plan = R.plan_workload(S.example_8x8())
+    got = sorted((m, s, box[:2]) for _, m, s, box in _planner_regions(plan))
+    assert got == want
+    st = R.reshard_plan_stats(plan)
+    assert st["regions"] == 8 and st["bytes_read"] == 128 and st["bytes_written"] == 128
+
+
+def test_planner_tp4_to_tp2dp2_replicas():
+    rows, meta = read_fixture("tp4_to_tp2dp2.txt")
+    want = sorted((tuple(int(x) for x in g.split(",")), int(s), ((int(r0), int(r1)), (int(c0), int(c1))))
+                  for g, s, r0, r1, c0, c1 in rows)
+    d = S.TensorDesc("w", (8, 4), "i32", (4,), ("S0",), (2, 2), ("R", "S0"),
+                     [S.View(i) for i in range(4)], [S.View(i) for i in range(4)])
+    plan = R.reshard_plan_create(d)
+    got = sorted((m, s, box[:2]) for _, m, s, box in _planner_regions(plan))
+    assert got == want
+    st = R.reshard_plan_stats(plan)
+    assert st["bytes_read"] == int(meta["bytes_read"][0])
+    assert st["bytes_written"] == int(meta["bytes_written"][0])
+
+
+def test_planner_matches_oracle_brute_force():
+    """Regions, chosen sources and replica groups equal the oracle's element-wise enumeration."""
+    for wl in S.brute_force_cases(250, seed=31):
+        t = wl.tensors[0]
+        plan = R.plan_workload(wl)
+        nd = len(t.global_shape)
+        got = sorted((m, s, box[:nd]) for _, m, s, box in _planner_regions(plan))
+        assert got == G.source_regions(t), (t.global_shape, t.src_mesh, t.src_placements, t.dst_mesh, t.dst_placements)
+        st = R.reshard_plan_stats(plan)
+        acc = G.byte_accounting(t)
+        assert st["bytes_read"] == acc["bytes_read"]
+        assert st["bytes_written"] == acc["bytes_written"]
+        assert st["gather_bcast_bytes"] == acc["gather_bcast_bytes"]
+        assert st["dst_groups"] == acc["dst_groups"]
+
+
+@pytest.mark.parametrize("name", ["dense_ffn_32x14336x4096_tp8_to_dp2tp2", "moe_8x128x1536x4096_ep16_to_ep8",
+                                  "moe_8x128x1536x4096_ep16_to_tp4_mxfp8", "uneven_14336x4096_tp6_to_tp5",
+                                  "mesh2x4_to_3_14336x4096", "mesh2x4_to_3x2_14336x4096"])
+def test_full_size_byte_accounting(name):
+    wl = S.workload_by_name(name)
+    plan = R.plan_workload(wl)
+    st = R.reshard_plan_stats(plan)
+    acc = [G.byte_accounting(t) for t in wl.tensors]
+    assert st["bytes_read"] == sum(a["bytes_read"] for a in acc)
+    assert st["bytes_written"] == sum(a["bytes_written"] for a in acc)
+    total = sum(int(np.prod(t.global_shape)) * G.ESIZE[t.dtype] for t in wl.tensors)
+    assert st["global_bytes"] == total and st["gather_bcast_bytes"] == 2 * total
+    assert st["bytes_read"] == total  # each element read once per destination replica group
+
+
+def test_dense_ffn_plan_shape():
+    st = R.reshard_plan_stats(R.plan_workload(S.dense_ffn()))
+    # 32 layers x 3 projections x 8 source ranks; each source shard lies inside one TP2 shard
+    assert st["regions"] == 768 and st["dst_groups"] == 192 and st["messages"] == 8
+    assert st["bytes_read"] == 11_274_289_152 and st["bytes_written"] == 22_548_578_304
+
+
+def test_validation_lists_every_violation():
+    d = S.TensorDesc("w", (8, -1), "bf16", (2,), ("S2",), (0,), ("S1",),
+                     [S.View(0), S.View(1)], [S.View(0)])
+    with pytest.raises(R.ReshardError) as e:
+        R.reshard_plan_create(d)
+    msg = str(e.value)
+    assert e.value.code == R.RESHARD_ERR_INVALID_ARG
+    assert "global_shape[1] < 0" in msg and "dst_mesh.shape[0] < 1" in msg
+
+
+def test_validation_batch_lists_all_tensors():
+    good = S.TensorDesc("a", (8, 8), "bf16", (2,), ("S0",), (4,), ("S1",), [S.View(0)] * 2, [S.View(0)] * 4)
+    bad1 = S.TensorDesc("b", (8, 8), "bf16", (2,), ("S5",), (4,), ("S1",), [S.View(0)] * 2, [S.View(0)] * 4)
+    bad2 = S.TensorDesc("c", (8, 8), "nope", (2,), ("S0",), (4,), ("S1",), [S.View(0)] * 2, [S.View(0)] * 4)
+    bad2.dtype = 99
+    with pytest.raises(R.ReshardError) as e:
+        R.reshard_plan_batch([good, bad1, bad2])
+    msg = str(e.value)
+    assert "tensor 1:" in msg and "tensor 2:" in msg and "tensor 0:" not in msg
+
+
+def test_view_capacity_overflow():
+    d = S.TensorDesc("w", (8, 8), "bf16", (2,), ("S0",), (4,), ("S1",),
+                     [S.View(0, 0), S.View(1, 10)], [S.View(i) for i in range(4)])
+    with pytest.raises(R.ReshardError) as e:
+        R.reshard_plan_create(d, src_capacity=[32, 32], dst_capacity=[16] * 4)
+    assert "overflows its buffer" in str(e.value)
+
+
+def test_non_unit_inner_stride_unsupported():
+    d = S.TensorDesc("w", (8, 8), "bf16", (2,), ("S0",), (4,), ("S1",),
+                     [S.View(0, 0, (16, 2)), S.View(1)], [S.View(i) for i in range(4)])
+    with pytest.raises(R.ReshardError) as e:
+        R.reshard_plan_create(d)
+    assert e.value.code == R.RESHARD_ERR_UNSUPPORTED
+
+
+def test_mesh_rank_permutation():
+    d = S.TensorDesc("w", (8, 8), "i32", (2,), ("S0",), (4,), ("S1",), [S.View(0), S.View(1)],
+                     [S.View(i) for i in range(4)])
+    d.dst_ranks = [3, 2, 1, 0]
+    plan = R.reshard_plan_create(d)
+    regs = _planner_regions(plan)
+    # destination pointer 3 holds mesh position 0: columns 0..1
+    assert sorted(box[1] for _, m, s, box in regs if m == (3,)) == [(0, 2), (0, 2)]
+    d.dst_ranks = [0, 0, 1, 2]
+    with pytest.raises(R.ReshardError):
+        R.reshard_plan_create(d)
+
+
+def test_execute_errors_before_touching_a_gpu():
+    wl = S.dense_ffn(layers=1, hidden=64, ffn=100)   # last dims not multiples of 32 -> no MXFP8
+    plan = R.plan_workload(wl)
+    n_src = plan.n_src_ptrs
+    with pytest.raises(R.ReshardError) as e:
+        R.reshard_execute(plan, [1] * n_src, [1] * plan.n_dst_ptrs, quant="mxfp8")
+    assert e.value.code == R.RESHARD_ERR_UNSUPPORTED
+    with pytest.raises(R.ReshardError) as e:
+        R.reshard_execute(plan, [0] * n_src, [1] * plan.n_dst_ptrs)
+    assert e.value.code == R.RESHARD_ERR_INVALID_ARG and "NULL" in str(e.value)
+    with pytest.raises(R.ReshardError):
+        R.reshard_execute(plan, [1] * n_src, [1] * plan.n_dst_ptrs, mode=7)
+
+
+def test_mxfp8_region_edges_must_hold_whole_blocks():
+    # source splits the last dim at 48 (not a multiple of 32): blocks would straddle sources
+    d = S.TensorDesc("w", (4, 96), "bf16", (2,), ("S1",), (1,), ("R",), [S.View(0), S.View(1)], [S.View(0)])
+    plan = R.reshard_plan_create(d)
+    with pytest.raises(R.ReshardError) as e:
+        R.reshard_execute(plan, [1, 1], [1, 1], quant="mxfp8")
+    assert "straddle" in str(e.value)
+
+
+def test_empty_batch_and_empty_tensor():
+    plan = R.reshard_plan_batch([])
+    assert R.reshard_plan_stats(plan)["regions"] == 0
+    R.reshard_execute(plan, [], [])
+    d = S.TensorDesc("w", (0, 8), "bf16", (2,), ("S0",), (4,), ("S1",), [S.View(0), S.View(1)],
+                     [S.View(i) for i in range(4)])
+    plan = R.reshard_plan_create(d)
+    assert R.reshard_plan_stats(plan)["regions"] == 0
+    R.reshard_execute(plan, [0, 0], [0] * 4)

@@ -1,0 +1,152 @@
+"""Device work-item tables checked on the CPU before any kernel runs them.
+
+A host emulation of the device walk (each item: `rows` rows of `run` elements from the source
+pointer to every member of its group) applied to host copies of the buffers must reproduce the
+oracle byte for byte, and every access of every item (all workloads at full size) must stay
+inside the buffer it targets.
+"""
+import numpy as np
+import pytest
+
+import dtensor_resharding_gb300 as R
+import synthetic as S
+from oracle import coracle
+
+from test_parity_gpu import SMALL
+
+DIRECT, PACK, UNPACK = 0, 1, 2
+
+
+def _ranges(wl, lay, plan):
+    """Byte range [lo, hi) in the host slabs of every pointer-table entry (workspace: own array)."""
+    es = {"u8": 1, "bf16": 2, "f16": 2, "f32": 4, "i32": 4, "i64": 8}
+    src, dst, sc = [], [], []
+    for t in wl.tensors:
+        e = es[t.dtype]
+        for v in t.src_views:
+            src.append(("src", lay.src_off[v.buffer], lay.src_off[v.buffer] + wl.src_buffer_numel[v.buffer] * e))
+        for v in t.dst_views:
+            de = 1 if wl.quant == "mxfp8" else e
+            dst.append(("dst", lay.dst_off[v.buffer], lay.dst_off[v.buffer] + wl.dst_buffer_numel[v.buffer] * de))
+            if wl.quant == "mxfp8":
+                sc.append(("scale", lay.scale_off[v.buffer], lay.scale_off[v.buffer] + wl.dst_buffer_numel[v.buffer] // 32))
+            else:
+                sc.append(("none", 0, 0))
+    ws = R.reshard_plan_stats(plan)["message_bytes"]
+    return src + dst + sc + [("ws", 0, ws)]
+
+
+def check_bounds(wl, lay, plan, which, quant=False):
+    items, gs, mp, mo = R.reshard_plan_items(plan, which)
+    if len(items) == 0:
+        return
+    table = _ranges(wl, lay, plan)
+    n_dst = plan.n_dst_ptrs
+    lo = np.array([r[1] for r in table], np.int64)
+    hi = np.array([r[2] for r in table], np.int64)
+    es = items["esize"].astype(np.int64)
+    src_es = es
+    dst_es = np.ones_like(es) if quant and which != PACK else es
+    last = (items["rows"].astype(np.int64) - 1)
+    s0 = lo[items["src"]] + items["src_off"] * src_es
+    s1 = lo[items["src"]] + (items["src_off"] + last * items["src_pitch"] + items["run"]) * src_es
+    assert (s0 >= lo[items["src"]]).all() and (s1 <= hi[items["src"]]).all(), "source read out of bounds"
+    assert (items["run"] > 0).all() and (items["rows"] > 0).all()
+    counts = gs[items["group"] + 1] - gs[items["group"]]
+    assert (counts >= 1).all()
+    for k in range(int(counts.max())):
+        sel = counts > k
+        m = gs[items["group"][sel]] + k
+        ptr = mp[m]
+        off = mo[m]
+        it = items[sel]
+        d0 = lo[ptr] + (off + it["dst_off"]) * dst_es[sel]
+        d1 = lo[ptr] + (off + it["dst_off"] + last[sel] * it["dst_pitch"] + it["run"]) * dst_es[sel]
+        assert (d0 >= lo[ptr]).all() and (d1 <= hi[ptr]).all(), "destination write out of bounds"
+        if quant and which != PACK:
+            e0 = off + it["dst_off"]
+            assert (e0 % 32 == 0).all() and (it["run"] % 32 == 0).all() and (it["dst_pitch"] % 32 == 0).all()
+            sp = ptr + n_dst
+            c1 = lo[sp] + (e0 + last[sel] * it["dst_pitch"] + it["run"]) // 32
+            assert (lo[sp] + e0 // 32 >= lo[sp]).all() and (c1 <= hi[sp]).all(), "scale write out of bounds"
+
+
+def emulate(wl, lay, plan, mode):
+    """Apply the item tables to host copies of the slabs (plain copies only)."""
+    src = lay.src_slab.numpy()
+    dst = np.full(lay.dst_slab.numel(), 0xA5, np.uint8)
+    ws = np.zeros(max(1, R.reshard_plan_stats(plan)["message_bytes"]), np.uint8)
+    table = _ranges(wl, lay, plan)
+    arrays = {"src": src, "dst": dst, "ws": ws}
+
+    def run(which):
+        items, gs, mp, mo = R.reshard_plan_items(plan, which)
+        for it in items:
+            e = int(it["esize"])
+            kind, base, _ = table[it["src"]]
+            sarr = arrays[kind]
+            for m in range(gs[it["group"]], gs[it["group"] + 1]):
+                dkind, dbase, _ = table[mp[m]]
+                darr = arrays[dkind]
+                for r in range(int(it["rows"])):
+                    s0 = base + (int(it["src_off"]) + r * int(it["src_pitch"])) * e
+                    d0 = dbase + (int(mo[m]) + int(it["dst_off"]) + r * int(it["dst_pitch"])) * e
+                    n = int(it["run"]) * e
+                    darr[d0: d0 + n] = sarr[s0: s0 + n]
+    if mode == "direct":
+        run(DIRECT)
+    else:
+        run(PACK)
+        run(UNPACK)
+    return dst
+
+
+def _oracle(wl, lay):
+    want = np.full(lay.dst_slab.numel(), 0xA5, np.uint8)
+    coracle.run_workload(wl, lay.src_slab.numpy(), lay.src_off, want, lay.dst_off)
+    return want
+
+
+@pytest.mark.parametrize("mode", ["direct", "packed"])
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_item_tables_reproduce_oracle(name, mode):
+    wl = SMALL[name]()
+    lay = S.allocate(wl, "cpu", misalign=2 if wl.tensors[0].dtype in ("bf16", "u8") else 0)
+    S.fill_sources(wl, lay)
+    plan = R.plan_workload(wl)
+    for which in (DIRECT, PACK, UNPACK):
+        check_bounds(wl, lay, plan, which)
+    assert np.array_equal(emulate(wl, lay, plan, mode), _oracle(wl, lay))
+
+
+def test_item_tables_brute_force():
+    for wl in S.brute_force_cases(120, seed=41):
+        lay = S.allocate(wl, "cpu")
+        S.fill_sources(wl, lay)
+        plan = R.plan_workload(wl)
+        for which in (DIRECT, PACK, UNPACK):
+            check_bounds(wl, lay, plan, which)
+        for mode in ("direct", "packed"):
+            assert np.array_equal(emulate(wl, lay, plan, mode), _oracle(wl, lay))
+
+
+def test_mxfp8_item_tables_small():
+    wl = S.moe_experts(layers=1, experts=16, hidden=256, ffn=256, dst="tp4")
+    lay = S.allocate(wl, "meta")
+    plan = R.plan_workload(wl)
+    # the plan accepts MXFP8: with NULL pointers the execute stops at the pointer check
+    with pytest.raises(R.ReshardError) as e:
+        R.reshard_execute(plan, [0] * plan.n_src_ptrs, [0] * (2 * plan.n_dst_ptrs), quant="mxfp8")
+    assert e.value.code == R.RESHARD_ERR_INVALID_ARG
+    for which in (DIRECT, PACK, UNPACK):
+        check_bounds(wl, lay, plan, which, quant=True)
+
+
+@pytest.mark.parametrize("name", sorted(S.WORKLOAD_NAMES))
+def test_full_size_item_bounds(name):
+    """Every item of every pass of every full-size workload stays inside its buffers."""
+    wl = S.workload_by_name(name)
+    lay = S.allocate(wl, "meta")
+    plan = R.plan_workload(wl)
+    for which in (DIRECT, PACK, UNPACK):
+        check_bounds(wl, lay, plan, which, quant=wl.quant == "mxfp8")

@@ -1,0 +1,189 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle, byte for byte (tolerance 0).
+
+Small cases (whole slabs compared with the C oracle, canary bytes included) span several
+work items, ragged tails, uneven and empty chunks, misaligned buffers, both modes and MXFP8.
+Full-size workloads are checked on sampled outputs that the oracle computes one by one, and by
+the A -> B -> A round trip, which must give the sources back unchanged.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synthetic as S
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import dtensor_resharding_gb300 as R
+    from harness import (assert_matches_oracle, run_gpu, sampled_check, sampled_check_mxfp8,
+                         round_trip_desc)
+
+SMALL = {
+    "example_8x8": lambda: S.example_8x8(),
+    "dense_ragged": lambda: S.dense_ffn(layers=2, hidden=256, ffn=1000),
+    "dense_interleaved_fused": lambda: S.dense_ffn(layers=1, hidden=320, ffn=1096, fused="interleave"),
+    "dense_unfused_tp8_to_dp4tp2": lambda: S.dense_ffn(layers=1, hidden=128, ffn=2048, fused="none",
+                                                      dp_dst=4, tp_dst=2),
+    "moe_ep16_to_ep8": lambda: S.moe_experts(layers=1, experts=32, hidden=256, ffn=96, dst="ep8"),
+    "uneven_tp6_to_tp5": lambda: S.uneven_tp(rows=1433, cols=409),
+    "mesh2x4_to_3": lambda: S.mesh2d_to_1d(rows=1434, cols=4096, variant="1d"),
+    "mesh2x4_to_3x2": lambda: S.mesh2d_to_1d(rows=143, cols=409, variant="2d"),
+    "many_small": lambda: S.many_small(n=150),
+    "long_run_f32": lambda: S.uneven_tp(rows=3000, cols=1000, src=3, dst=7, dtype="f32"),
+    "u8_odd": lambda: S.mesh2d_to_1d(rows=77, cols=333, variant="2d", dtype="u8"),
+}
+
+
+def _as_i16(x):
+    """int32 bit patterns in [0, 65536) or [-32768, 32768) -> int16 with the same low 16 bits."""
+    x = x & 0xFFFF
+    return torch.where(x >= 32768, x - 65536, x).to(torch.int16)
+
+
+@pytest.fixture(autouse=True)
+def _cleanup():
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("mode", ["direct", "packed"])
+@pytest.mark.parametrize("misalign", [0, 2, 6])
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_workloads_bit_exact(name, misalign, mode):
+    wl = SMALL[name]()
+    if misalign % max(S.DTYPES[wl.tensors[0].dtype][1], 1):
+        pytest.skip("buffer offset must be a multiple of the element size")
+    lay, plan = run_gpu(wl, mode=mode, misalign=misalign)
+    assert_matches_oracle(wl, lay)
+
+
+@pytest.mark.parametrize("mode", ["direct", "packed"])
+def test_brute_force_small_meshes(mode):
+    """Random meshes (<= 3 dims, <= 4 each), every placement kind, element-id payloads."""
+    for wl in S.brute_force_cases(80, seed=21):
+        lay, plan = run_gpu(wl, mode=mode)
+        assert_matches_oracle(wl, lay)
+
+
+@pytest.mark.parametrize("mode", ["direct", "packed"])
+@pytest.mark.parametrize("misalign", [0, 4])
+def test_mxfp8_small_bit_exact(mode, misalign):
+    wl = S.moe_experts(layers=1, experts=16, hidden=256, ffn=256, dst="tp4")
+    lay, plan = run_gpu(wl, mode=mode, misalign=misalign)
+    assert_matches_oracle(wl, lay)
+
+
+def test_mxfp8_special_values_bit_exact():
+    """Zero blocks, -0, Inf/NaN blocks, subnormals, saturation and midpoints through the kernel."""
+    wl = S.moe_experts(layers=1, experts=8, hidden=64, ffn=128, ep_src=4, dst="tp4")
+    lay, plan = run_gpu(wl, execute=False)
+    src = lay.src_slab.view(torch.int16)
+    n = src.numel()
+    g = torch.Generator(device="cuda").manual_seed(5)
+    special = torch.tensor([0x0000, 0x8000, 0x7F80, 0xFF80, 0x7FC1, 0x0001, 0x8001, 0x007F, 0x43E0, 0x43F0,
+                            0x4400, 0x3F88, 0xBF88, 0x7F7F, 0xFF7F, 0x3A80], dtype=torch.int32, device="cuda")
+    pick = torch.randint(0, special.numel(), (n,), generator=g, device="cuda")
+    rand = torch.randint(-32768, 32767, (n,), generator=g, device="cuda", dtype=torch.int32)
+    mixed = torch.where(torch.rand(n, generator=g, device="cuda") < 0.3, special[pick], rand)
+    # some blocks entirely zero
+    mixed = mixed.view(-1, 32)
+    mixed[::7] = 0
+    src.copy_(_as_i16(mixed.view(-1)))
+    # replicas of a source do not exist here (EP sources are disjoint), so any bits are valid input
+    sp, dp = R.workload_pointers(wl, lay)
+    R.reshard_execute(plan, sp, dp, quant="mxfp8")
+    torch.cuda.synchronize()
+    assert_matches_oracle(wl, lay)
+
+
+def test_mxfp8_every_bf16_pattern_at_many_scales():
+    """All 65,536 BF16 patterns through the kernel's conversion under many block scales: each
+    block holds one scale-setting element and 31 patterns; compared with the C oracle."""
+    wl = S.moe_experts(layers=1, experts=4, hidden=64, ffn=2048, ep_src=4, dst="tp4")
+    lay, plan = run_gpu(wl, execute=False)
+    src = lay.src_slab.view(torch.int16)
+    pats = torch.arange(65536, dtype=torch.int32, device="cuda")
+    finite = pats[(pats & 0x7F80) != 0x7F80]
+    blocks = src.numel() // 32
+    body = finite.repeat((blocks * 31) // finite.numel() + 1)[: blocks * 31].view(blocks, 31)
+    # leading element sets amax: exponents spread over the whole BF16 range
+    lead = ((torch.arange(blocks, device="cuda", dtype=torch.int32) % 254) + 1) << 7
+    x = torch.cat([lead[:, None], body], dim=1)
+    src.copy_(_as_i16(x.view(-1)))
+    sp, dp = R.workload_pointers(wl, lay)
+    R.reshard_execute(plan, sp, dp, quant="mxfp8")
+    torch.cuda.synchronize()
+    assert_matches_oracle(wl, lay)
+
+
+def test_execute_twice_and_pointer_change():
+    """Re-executing a plan with new buffers re-uploads the pointer table."""
+    wl = S.dense_ffn(layers=1, hidden=128, ffn=512)
+    lay1, plan = run_gpu(wl)
+    assert_matches_oracle(wl, lay1)
+    lay2, _ = run_gpu(wl, plan=plan, misalign=2)
+    assert_matches_oracle(wl, lay2)
+    lay3, _ = run_gpu(wl, plan=plan, mode="packed")
+    assert_matches_oracle(wl, lay3)
+
+
+def test_streams_are_honoured():
+    wl = S.dense_ffn(layers=1, hidden=256, ffn=1024)
+    lay, plan = run_gpu(wl, execute=False)
+    s = torch.cuda.Stream()
+    sp, dp = R.workload_pointers(wl, lay)
+    with torch.cuda.stream(s):
+        R.reshard_execute(plan, sp, dp, stream=s.cuda_stream)
+    s.synchronize()
+    assert_matches_oracle(wl, lay)
+
+
+# ------------------------------------------------------------------ full sizes, sampled
+
+def _full(wl_fn, mode, sampler, **kw):
+    wl = wl_fn()
+    lay, plan = run_gpu(wl, mode=mode)
+    n = sampler(wl, lay, **kw)
+    assert n > 0
+    return wl, lay, plan
+
+
+@pytest.mark.parametrize("mode", ["direct", "packed"])
+def test_full_dense_ffn_sampled_and_round_trip(mode):
+    wl, lay, plan = _full(S.dense_ffn, mode, sampled_check, per_tensor=64)
+    # A -> B -> A: the destinations resharded back reproduce the (fused) sources exactly
+    back = S.Workload(wl.name + ".back", [round_trip_desc(t) for t in wl.tensors],
+                      src_buffer_numel=wl.dst_buffer_numel, src_buffer_dtype=wl.dst_buffer_dtype,
+                      dst_buffer_numel=wl.src_buffer_numel, dst_buffer_dtype=wl.src_buffer_dtype)
+    bplan = R.plan_workload(back)
+    out = torch.empty_like(lay.src_slab)
+    out.copy_(lay.src_slab)
+    lay.src_slab.fill_(0x5A)
+    flip = S.Layout(lay.dst_slab, lay.src_slab, None, lay.dst_off, lay.src_off, None)
+    sp, dp = R.workload_pointers(back, flip)
+    R.reshard_execute(bplan, sp, dp, mode=mode)
+    torch.cuda.synchronize()
+    for b, (off, n) in enumerate(zip(lay.src_off, wl.src_buffer_numel)):
+        nb = n * S.DTYPES[wl.src_buffer_dtype[b]][1]
+        assert torch.equal(lay.src_slab[off: off + nb], out[off: off + nb]), f"source buffer {b} changed"
+
+
+def test_full_moe_ep16_to_ep8_sampled():
+    _full(lambda: S.moe_experts(dst="ep8"), "direct", sampled_check, per_tensor=64)
+
+
+@pytest.mark.parametrize("mode", ["direct", "packed"])
+def test_full_moe_tp4_mxfp8_sampled(mode):
+    _full(lambda: S.moe_experts(dst="tp4"), mode, sampled_check_mxfp8, per_tensor=6)
+
+
+def test_full_edge_mix_bit_exact():
+    for wl in (S.uneven_tp(), S.mesh2d_to_1d(variant="1d"), S.mesh2d_to_1d(variant="2d")):
+        for mode in ("direct", "packed"):
+            lay, plan = run_gpu(wl, mode=mode)
+            assert_matches_oracle(wl, lay)
+
+
+def test_full_many_small_sampled():
+    _full(S.many_small, "direct", sampled_check, per_tensor=4)
