@@ -25,7 +25,6 @@
 #include "plan.h"
 
 namespace reshard {
-namespace {
 
 constexpr int kBlock = 256;   // threads per CTA
 constexpr int kUnroll = 4;    // 16-byte loads in flight per thread (aligned path)
@@ -290,6 +289,8 @@ __global__ void __launch_bounds__(kBlock) reshard_mxfp8_kernel(const Item *__res
 
 // ---------------------------------------------------------------------------- host side --
 
+namespace {
+
 int cuda_fail(cudaError_t e, const char *what) {
   return fail(e == cudaErrorMemoryAllocation ? RESHARD_ERR_OOM : RESHARD_ERR_CUDA,
               std::string(what) + ": " + cudaGetErrorString(e));
@@ -473,3 +474,4 @@ extern "C" int reshard_plan_destroy(reshard_plan_t *p) {
   delete p;
   return RESHARD_OK;
 }
+
