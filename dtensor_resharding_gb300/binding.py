@@ -28,7 +28,8 @@ RESHARD_MAX_DIMS = 4
 DTYPE_CODES = {"u8": 0, "bf16": 1, "f16": 2, "f32": 3, "i32": 4, "i64": 5}
 MODES = {"direct": RESHARD_DIRECT, "packed": RESHARD_PACKED}
 QUANTS = {"none": RESHARD_QUANT_NONE, "mxfp8": RESHARD_QUANT_MXFP8}
-EXPORTED = ("reshard_plan_create", "reshard_plan_batch", "reshard_execute", "reshard_plan_stats",
+EXPORTED = ("reshard_plan_create", "reshard_plan_batch", "reshard_execute", "reshard_execute_static",
+            "reshard_plan_stats",
             "reshard_plan_regions", "reshard_plan_group_members", "reshard_plan_items", "reshard_plan_destroy",
             "reshard_last_error")
 
@@ -76,6 +77,7 @@ def _load():
     lib.reshard_plan_create.argtypes = [ctypes.POINTER(TensorSpecT), ctypes.POINTER(vp)]
     lib.reshard_plan_batch.argtypes = [ctypes.POINTER(TensorSpecT), ctypes.c_int, ctypes.POINTER(vp)]
     lib.reshard_execute.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.c_int, ctypes.c_int, vp]
+    lib.reshard_execute_static.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp]
     lib.reshard_plan_stats.argtypes = [vp, ctypes.POINTER(StatsT)]
     lib.reshard_plan_regions.argtypes = [vp, ctypes.c_int64, _i32p, _i32p, _i32p, _i64p, _i64p, _i64p]
     lib.reshard_plan_group_members.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, _i32p, _i64p]
@@ -217,6 +219,15 @@ def reshard_execute(plan: Plan, src_ptrs: Sequence[int], dst_ptrs: Sequence[int]
     sp = (ctypes.c_void_p * max(1, len(src_ptrs)))(*[int(p) if p else None for p in src_ptrs])
     dp = (ctypes.c_void_p * max(1, len(dst_ptrs)))(*[int(p) if p else None for p in dst_ptrs])
     _check(LIB.reshard_execute(plan.handle, sp, dp, mode, quant, ctypes.c_void_p(int(stream) or None)))
+
+
+def reshard_execute_static(plan: Plan, src_ptrs: Sequence[int], dst_ptrs: Sequence[int], stream: int = 0) -> None:
+    """Direct-mode reshard that allocates no device memory (descriptor tables go to a fixed
+    array inside the library; see include/reshard.h). For callers whose device memory is owned
+    elsewhere (an engine's reserved pool, a framework allocator) and must not see cudaMalloc."""
+    sp = (ctypes.c_void_p * max(1, len(src_ptrs)))(*[int(p) if p else None for p in src_ptrs])
+    dp = (ctypes.c_void_p * max(1, len(dst_ptrs)))(*[int(p) if p else None for p in dst_ptrs])
+    _check(LIB.reshard_execute_static(plan.handle, sp, dp, ctypes.c_void_p(int(stream) or None)))
 
 
 def reshard_plan_stats(plan: Plan) -> Dict[str, int]:

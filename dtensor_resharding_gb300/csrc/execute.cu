@@ -20,6 +20,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "plan.h"
@@ -475,3 +476,108 @@ extern "C" int reshard_plan_destroy(reshard_plan_t *p) {
   return RESHARD_OK;
 }
 
+// ------------------------------------------------------------ execute without allocating --
+//
+// Some callers must not have a library allocate device memory on their behalf. A generation
+// engine that has reserved almost all of the GPU for its KV cache, or a framework whose own
+// caching allocator owns the device heap, cannot let a weight refit call cudaMalloc: the call
+// can fail for lack of memory, and cudaMalloc / cudaFree synchronize the device and would stall
+// generation. reshard_execute_static serves them: it runs the direct-mode copy with its
+// descriptor tables held in the file-scope array below, which is part of the library image and
+// is reserved once on every GPU that loads the library, for as long as the process lives.
+
+// Every call uses this one array and it keeps the previous call's contents; nothing in it has to
+// start at zero (the kernel reads only what the current call copied in). Calls that overlap on
+// the GPU (different streams, or other threads) overwrite each other's tables and race.
+static __device__ __align__(256) unsigned char reshard_static_scratch[RESHARD_STATIC_SCRATCH_BYTES];
+
+namespace reshard {
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+uint8_t *g_static_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on device `dev` (which must be current). The host-side
+// name of a __device__ array is not a device address, so it is looked up once per device with
+// cudaGetSymbolAddress on the first call made there.
+int static_scratch(int dev, uint8_t **out) {
+  if (dev < 0 || dev >= kMaxDevices) return fail(RESHARD_ERR_UNSUPPORTED, "device ordinal above 63");
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_addr[dev]) {
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, reshard_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(reshard_static_scratch)");
+    g_static_addr[dev] = static_cast<uint8_t *>(p);
+  }
+  *out = g_static_addr[dev];
+  return RESHARD_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+}  // namespace reshard
+
+extern "C" int reshard_execute_static(const reshard_plan_t *p, void *const *src_ptrs, void *const *dst_ptrs,
+                                      reshard_stream_t stream_) {
+  using namespace reshard;
+  if (!p) return fail(RESHARD_ERR_INVALID_ARG, "plan is NULL");
+  if (p->regions.empty()) return RESHARD_OK;
+  if ((p->n_src_ptrs && !src_ptrs) || (p->n_dst_ptrs && !dst_ptrs))
+    return fail(RESHARD_ERR_INVALID_ARG, "src_ptrs or dst_ptrs is NULL");
+  for (const TensorInfo &t : p->tensors) {
+    for (int side = 0; side < 2; ++side) {
+      const int64_t n = side ? t.n_dst : t.n_src;
+      for (int64_t r = 0; r < n; ++r) {
+        const Box &b = side ? t.dst_box[(size_t)r] : t.src_box[(size_t)r];
+        bool empty = false;
+        for (int d = 0; d < t.ndim; ++d) empty = empty || b.hi[d] <= b.lo[d];
+        void *ptr = side ? dst_ptrs[t.dst_base + r] : src_ptrs[t.src_base + r];
+        if (!empty && !ptr) return fail(RESHARD_ERR_INVALID_ARG, "a pointer of a non-empty shard is NULL");
+      }
+    }
+  }
+  // scratch layout: items | group starts | member pointers | member offsets | pointer table
+  const std::vector<Item> &items = p->items[kDirect];
+  const size_t b_items = items.size() * sizeof(Item);
+  const size_t b_gs = p->grp_start.size() * sizeof(int32_t);
+  const size_t b_mp = p->mem_ptr.size() * sizeof(int32_t);
+  const size_t b_mo = p->mem_off.size() * sizeof(int64_t);
+  const size_t b_pt = (size_t)pointer_table_size(p) * sizeof(uint64_t);
+  const size_t o_gs = align256(b_items), o_mp = o_gs + align256(b_gs), o_mo = o_mp + align256(b_mp);
+  const size_t o_pt = o_mo + align256(b_mo), need = o_pt + align256(b_pt);
+  if (need > (size_t)RESHARD_STATIC_SCRATCH_BYTES)
+    return fail(RESHARD_ERR_UNSUPPORTED, "plan needs " + std::to_string(need) +
+                                             " bytes of descriptor scratch; reshard_execute_static holds at most " +
+                                             std::to_string((size_t)RESHARD_STATIC_SCRATCH_BYTES) +
+                                             " (split the batch or use reshard_execute)");
+  int dev = 0;
+  RS_CUDA(cudaGetDevice(&dev));
+  uint8_t *base = nullptr;
+  int rc = static_scratch(dev, &base);
+  if (rc) return rc;
+  LaunchCaps caps;
+  if ((rc = launch_caps(dev, caps))) return rc;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  // pageable sources: the runtime stages them before each call returns
+  RS_CUDA(cudaMemcpyAsync(base, items.data(), b_items, cudaMemcpyHostToDevice, stream));
+  RS_CUDA(cudaMemcpyAsync(base + o_gs, p->grp_start.data(), b_gs, cudaMemcpyHostToDevice, stream));
+  RS_CUDA(cudaMemcpyAsync(base + o_mp, p->mem_ptr.data(), b_mp, cudaMemcpyHostToDevice, stream));
+  RS_CUDA(cudaMemcpyAsync(base + o_mo, p->mem_off.data(), b_mo, cudaMemcpyHostToDevice, stream));
+  // pointer table [sources | destinations | ...]: the direct copy reads only these two runs
+  if (p->n_src_ptrs)
+    RS_CUDA(cudaMemcpyAsync(base + o_pt, src_ptrs, (size_t)p->n_src_ptrs * sizeof(void *), cudaMemcpyHostToDevice,
+                            stream));
+  if (p->n_dst_ptrs)
+    RS_CUDA(cudaMemcpyAsync(base + o_pt + (size_t)p->n_src_ptrs * sizeof(uint64_t), dst_ptrs,
+                            (size_t)p->n_dst_ptrs * sizeof(void *), cudaMemcpyHostToDevice, stream));
+  const int n = (int)items.size();
+  const int grid = std::min(n, caps.copy_grid);
+  reshard_copy_kernel<<<grid, kBlock, 0, stream>>>(
+      reinterpret_cast<const Item *>(base), n, reinterpret_cast<const uint64_t *>(base + o_pt),
+      reinterpret_cast<const int32_t *>(base + o_gs), reinterpret_cast<const int32_t *>(base + o_mp),
+      reinterpret_cast<const int64_t *>(base + o_mo));
+  RS_CUDA(cudaGetLastError());
+  return RESHARD_OK;
+}

@@ -171,6 +171,30 @@ int reshard_plan_batch(const reshard_tensor_spec_t *specs, int n_tensors, reshar
 int reshard_execute(reshard_plan_t *plan, void *const *src_ptrs, void *const *dst_ptrs, int mode,
                     int quant, reshard_stream_t stream);
 
+/*
+ * reshard_execute_static -- the direct-mode reshard (quant none) without any device allocation.
+ * The pages have no counterpart to this call; it exists for callers that cannot let a library
+ * allocate device memory during a refit: an inference engine that has reserved nearly all of
+ * the GPU for its KV cache, or a framework whose own caching allocator owns the device heap,
+ * where cudaMalloc could fail for lack of memory and cudaMalloc/cudaFree would synchronize the
+ * device and stall work already running.
+ * The plan's descriptor tables and the pointer arrays are copied (cudaMemcpyAsync on `stream`,
+ * from pageable memory, staged before the call returns) into one file-scope device array of
+ * RESHARD_STATIC_SCRATCH_BYTES bytes that the library image reserves on every GPU that loads it,
+ * until the process exits; then the same copy kernel as reshard_execute runs from there. The
+ * first call on a device looks the array's device address up (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture. Calls on one device share the
+ * array and it keeps the last call's contents (nothing in it needs to start at zero): calls that
+ * overlap on the GPU race, so serialise them (for example, all on one stream).
+ * Arguments as in reshard_execute (one destination pointer per rank). The plan is only read and
+ * is not bound to a device. Errors: INVALID_ARG (NULL plan or pointer of a non-empty shard);
+ * UNSUPPORTED when the tables need more than RESHARD_STATIC_SCRATCH_BYTES (the message gives the
+ * size; split the batch or use reshard_execute); CUDA. Calls no cudaMalloc or cudaFree.
+ */
+#define RESHARD_STATIC_SCRATCH_BYTES (16u << 20)
+int reshard_execute_static(const reshard_plan_t *plan, void *const *src_ptrs, void *const *dst_ptrs,
+                           reshard_stream_t stream);
+
 /* reshard_plan_stats -- fill *out (host only). */
 int reshard_plan_stats(const reshard_plan_t *plan, reshard_stats_t *out);
 
