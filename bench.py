@@ -105,6 +105,24 @@ class ClockSampler:
                 "power_w_max": max((num(r[2]) or 0) for r in rows), "reasons": reasons, "samples": len(busy)}
 
 
+# ----------------------------------------------------------------------------- ranks
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of every rank's `value` (the slowest replica sets the job's time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_step_per_rank: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job GB/s: every rank's bytes over the slowest rank's time (weak scaling)."""
+    return world * bytes_per_step_per_rank * steps / (max_ms / 1e3) / 1e9
+
+
 # ----------------------------------------------------------------------------- oracle timing
 
 def time_oracle_sample(wl, src_host, src_off, budget_s: float, max_tensors: int):
@@ -242,19 +260,15 @@ def our_arm(args, rank: int, world: int, local_rank: int) -> None:
         end.record(stream)
         torch.cuda.synchronize()
         barrier()
-        total_ms = start.elapsed_time(end)
+        total_ms = max_over_ranks(start.elapsed_time(end), world, dev)
         per = [a.elapsed_time(b) for a, b in ev]
-        if world > 1:
-            t = torch.tensor([total_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            total_ms = float(t.item())
         return total_ms, per
 
     clocks = ClockSampler(local_rank)
     total_ms, per = run_steps(args.mode, args.steps, args.warmup)
     clk = clocks.stop()
     ms_per_step = total_ms / args.steps
-    value = world * dst_bytes * args.steps / (total_ms / 1e3) / 1e9
+    value = job_throughput(dst_bytes, args.steps, world, total_ms)
 
     # roofline of the dominant kernel (direct: the one copy kernel per execute)
     peak, peak_kind = peaks()
@@ -278,7 +292,7 @@ def our_arm(args, rank: int, world: int, local_rank: int) -> None:
     other = "packed" if args.mode == "direct" else "direct"
     o_ms, _ = run_steps(other, max(3, args.steps // 4), 2)
     modes = {other: {"ms_per_step": round(o_ms / max(3, args.steps // 4), 4),
-                     "value": round(world * dst_bytes * max(3, args.steps // 4) / (o_ms / 1e3) / 1e9, 2)}}
+                     "value": round(job_throughput(dst_bytes, max(3, args.steps // 4), world, o_ms), 2)}}
 
     # end to end through the public call with host buffers: H2D of the step's sources from pinned
     # memory, the execute, D2H of the step's destinations, all inside the timed region
@@ -302,12 +316,8 @@ def our_arm(args, rank: int, world: int, local_rank: int) -> None:
                     hdst.copy_(lay.dst_slab, non_blocking=True)
             t_e2e_end.record(stream)
             torch.cuda.synchronize()
-            e_ms = t_e2e.elapsed_time(t_e2e_end)
-            if world > 1:
-                t = torch.tensor([e_ms], device=dev)
-                dist.all_reduce(t, op=dist.ReduceOp.MAX)
-                e_ms = float(t.item())
-            e2e = {"value": round(world * dst_bytes * ek / (e_ms / 1e3) / 1e9, 3), "unit": "GB/s",
+            e_ms = max_over_ranks(t_e2e.elapsed_time(t_e2e_end), world, dev)
+            e2e = {"value": round(job_throughput(dst_bytes, ek, world, e_ms), 3), "unit": "GB/s",
                    "h2d_bytes_per_step": lay.src_slab.numel(), "d2h_bytes_per_step": lay.dst_slab.numel(),
                    "steps": ek, "ms_per_step": round(e_ms / ek, 3),
                    "note": "pinned host slabs, copies and execute on one stream"}

@@ -69,10 +69,10 @@ class ReshardError(RuntimeError):
         self.code = code
 
 
-def _load():
-    if not os.path.exists(LIB_PATH):
-        raise ImportError(f"libreshard.so is not built ({LIB_PATH}); run __graft_entry__.build()")
-    lib = ctypes.CDLL(LIB_PATH)
+def _load(path: str = LIB_PATH):
+    if not os.path.exists(path):
+        raise ImportError(f"libreshard.so is not built ({path}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
     vp = ctypes.c_void_p
     lib.reshard_plan_create.argtypes = [ctypes.POINTER(TensorSpecT), ctypes.POINTER(vp)]
     lib.reshard_plan_batch.argtypes = [ctypes.POINTER(TensorSpecT), ctypes.c_int, ctypes.POINTER(vp)]
@@ -211,13 +211,34 @@ def reshard_plan_batch(descs: Sequence[Any], src_capacity=None, dst_capacity=Non
     return Plan(h.value, sum(_n_ranks(d.src_mesh) for d in descs), sum(_n_ranks(d.dst_mesh) for d in descs))
 
 
-def reshard_execute(plan: Plan, src_ptrs: Sequence[int], dst_ptrs: Sequence[int], mode="direct", quant="none",
-                    stream: int = 0) -> None:
-    """Enqueue the reshard on ``stream`` (a cudaStream_t as int; 0 = legacy default stream)."""
+def pointer_array(ptrs: Sequence[int]):
+    """Device pointers as a contiguous uint64 numpy array, passed to the C calls without copying.
+
+    Build it once per set of buffers: re-marshalling tens of thousands of pointers per call
+    costs milliseconds of host time."""
+    import numpy as np
+    return np.ascontiguousarray(np.asarray([int(p) if p else 0 for p in ptrs], dtype=np.uint64))
+
+
+def _ptrs_arg(ptrs):
+    import numpy as np
+    if isinstance(ptrs, np.ndarray):
+        if ptrs.dtype not in (np.uint64, np.int64) or not ptrs.flags["C_CONTIGUOUS"]:
+            raise TypeError("pointer arrays must be contiguous uint64/int64")
+        return ptrs.ctypes.data_as(ctypes.POINTER(ctypes.c_void_p)), ptrs
+    arr = (ctypes.c_void_p * max(1, len(ptrs)))(*[int(p) if p else None for p in ptrs])
+    return arr, arr
+
+
+def reshard_execute(plan: Plan, src_ptrs, dst_ptrs, mode="direct", quant="none", stream: int = 0) -> None:
+    """Enqueue the reshard on ``stream`` (a cudaStream_t as int; 0 = legacy default stream).
+
+    ``src_ptrs`` / ``dst_ptrs``: sequences of device pointers, or uint64 arrays from
+    ``pointer_array`` (no per-call marshalling)."""
     mode = MODES[mode] if isinstance(mode, str) else int(mode)
     quant = QUANTS[quant] if isinstance(quant, str) else int(quant)
-    sp = (ctypes.c_void_p * max(1, len(src_ptrs)))(*[int(p) if p else None for p in src_ptrs])
-    dp = (ctypes.c_void_p * max(1, len(dst_ptrs)))(*[int(p) if p else None for p in dst_ptrs])
+    sp, _ks = _ptrs_arg(src_ptrs)
+    dp, _kd = _ptrs_arg(dst_ptrs)
     _check(LIB.reshard_execute(plan.handle, sp, dp, mode, quant, ctypes.c_void_p(int(stream) or None)))
 
 
@@ -225,8 +246,8 @@ def reshard_execute_static(plan: Plan, src_ptrs: Sequence[int], dst_ptrs: Sequen
     """Direct-mode reshard that allocates no device memory (descriptor tables go to a fixed
     array inside the library; see include/reshard.h). For callers whose device memory is owned
     elsewhere (an engine's reserved pool, a framework allocator) and must not see cudaMalloc."""
-    sp = (ctypes.c_void_p * max(1, len(src_ptrs)))(*[int(p) if p else None for p in src_ptrs])
-    dp = (ctypes.c_void_p * max(1, len(dst_ptrs)))(*[int(p) if p else None for p in dst_ptrs])
+    sp, _ks = _ptrs_arg(src_ptrs)
+    dp, _kd = _ptrs_arg(dst_ptrs)
     _check(LIB.reshard_execute_static(plan.handle, sp, dp, ctypes.c_void_p(int(stream) or None)))
 
 

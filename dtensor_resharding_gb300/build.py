@@ -26,37 +26,43 @@ def _sources() -> List[str]:
     return out
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile (if stale) and return the path of libreshard.so."""
+def build(force: bool = False, verbose: bool = False, extra_flags: List[str] = (), out: str = LIB_PATH) -> str:
+    """Compile (if stale) and return the path of libreshard.so.
+
+    ``extra_flags`` (or RESHARD_EXTRA_NVCC_FLAGS, space separated) are appended to the CUDA
+    compile, e.g. -DRESHARD_UNROLL=8 for launch-shape sweeps; they force a rebuild."""
+    extra = list(extra_flags) + os.environ.get("RESHARD_EXTRA_NVCC_FLAGS", "").split()
+    force = force or bool(extra)
     srcs = _sources()
-    if (not force and os.path.exists(LIB_PATH)
-            and os.path.getmtime(LIB_PATH) >= max(os.path.getmtime(s) for s in srcs)):
-        return LIB_PATH
-    bdir = os.path.join(HERE, "_build")
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= max(os.path.getmtime(s) for s in srcs)):
+        return out
+    tag = "" if out == LIB_PATH else os.path.basename(out).replace(".so", "")
+    bdir = os.path.join(HERE, "_build", tag)
     os.makedirs(bdir, exist_ok=True)
     nvcc = _nvcc()
     common = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
     jobs = [
         [nvcc, *common, "-x", "c++", "-c", os.path.join(CSRC, "plan.cpp"), "-o", os.path.join(bdir, "plan.o")],
-        [nvcc, *common, *ARCH, "-lineinfo", "-Xptxas", "-v" if verbose else "-O3",
+        [nvcc, *common, *ARCH, "-lineinfo", "-Xptxas", "-v" if verbose else "-O3", *extra,
          "-c", os.path.join(CSRC, "execute.cu"), "-o", os.path.join(bdir, "execute.o")],
     ]
     procs = [subprocess.Popen(j, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True) for j in jobs]
     logs = []
     for j, p in zip(jobs, procs):
-        out, _ = p.communicate()
-        logs.append(out)
+        log, _ = p.communicate()
+        logs.append(log)
         if p.returncode:
-            raise RuntimeError(f"build failed: {' '.join(j)}\n{out}")
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+            raise RuntimeError(f"build failed: {' '.join(j)}\n{log}")
+    tmp = out + f".tmp{os.getpid()}"
     link = [nvcc, "-shared", *ARCH, os.path.join(bdir, "plan.o"), os.path.join(bdir, "execute.o"), "-o", tmp]
     r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
     if r.returncode:
         raise RuntimeError(f"link failed: {' '.join(link)}\n{r.stdout}")
-    os.replace(tmp, LIB_PATH)
+    os.replace(tmp, out)
     if verbose:
         print("".join(logs))
-    return LIB_PATH
+    return out
 
 
 if __name__ == "__main__":

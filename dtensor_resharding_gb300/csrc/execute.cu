@@ -27,15 +27,69 @@
 
 namespace reshard {
 
-constexpr int kBlock = 256;   // threads per CTA
-constexpr int kUnroll = 4;    // 16-byte loads in flight per thread (aligned path)
-constexpr int kMaxFan = 8;    // destination replicas held in registers per pass
+// Launch shape; the defaults are the measured best on GB300 (build-time overridable for sweeps).
+#ifndef RESHARD_BLOCK
+#define RESHARD_BLOCK 256
+#endif
+#ifndef RESHARD_UNROLL
+#define RESHARD_UNROLL 8
+#endif
+#ifndef RESHARD_MIN_BLOCKS
+#define RESHARD_MIN_BLOCKS 2
+#endif
+constexpr int kBlock = RESHARD_BLOCK;    // threads per CTA
+constexpr int kUnroll = RESHARD_UNROLL;  // 16-byte loads in flight per thread (aligned path)
+constexpr int kMaxFan = 8;               // destination replicas held in registers per pass
 
 // ------------------------------------------------------------------------------ helpers --
 
-__device__ __forceinline__ uint4 load_stream(const uint8_t *p) { return __ldcs(reinterpret_cast<const uint4 *>(p)); }
+#ifndef RESHARD_LOAD_HINT
+#define RESHARD_LOAD_HINT 0
+#endif
+#ifndef RESHARD_STORE_HINT
+#define RESHARD_STORE_HINT 0
+#endif
 
-__device__ __forceinline__ void store_stream(uint8_t *p, uint4 v) { __stcs(reinterpret_cast<uint4 *>(p), v); }
+// Streaming 16-byte load: each source byte is read once per launch.
+__device__ __forceinline__ uint4 load_stream(const uint8_t *p) {
+#if RESHARD_LOAD_HINT == 0
+  return __ldcs(reinterpret_cast<const uint4 *>(p));
+#elif RESHARD_LOAD_HINT == 1
+  return __ldg(reinterpret_cast<const uint4 *>(p));
+#else
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+#endif
+}
+
+#ifndef RESHARD_WIDE
+#define RESHARD_WIDE 0
+#endif
+
+// 32-byte global load / store (sm_100 and later accept 256-bit vectors on global memory).
+__device__ __forceinline__ void load_stream32(const uint8_t *p, uint4 &a, uint4 &b) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+               : "l"(p));
+}
+
+__device__ __forceinline__ void store_stream32(uint8_t *p, uint4 a, uint4 b) {
+  asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+               :
+               : "l"(p), "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+
+// Streaming 16-byte store: destinations are not read back by this launch.
+__device__ __forceinline__ void store_stream(uint8_t *p, uint4 v) {
+#if RESHARD_STORE_HINT == 0
+  __stcs(reinterpret_cast<uint4 *>(p), v);
+#else
+  *reinterpret_cast<uint4 *>(p) = v;
+#endif
+}
 
 // Bytes [sh, sh + 16) of the 32-byte concatenation lo:hi (little endian), sh in [0, 16).
 __device__ __forceinline__ uint4 shift_bytes(uint4 lo, uint4 hi, int sh) {
@@ -91,49 +145,101 @@ __device__ __forceinline__ void copy_aligned(const uint8_t *__restrict__ src, ui
   }
 }
 
-// General alignment: destination replicas must agree modulo 16. Each thread owns one aligned
-// 16-byte destination word, assembles it from the (at most two) aligned 16-byte source blocks
-// that hold its bytes, and stores it whole, or byte by byte at the two ends of a row. A source
-// block is loaded only when it holds at least one byte of the row, so no access leaves the
-// 16-byte blocks (and hence the pages) the region occupies.
+// Every source, destination, run and pitch 32-byte aligned: 32-byte copies.
+__device__ __forceinline__ void copy_aligned32(const uint8_t *__restrict__ src, uint8_t *const *dst, int nf, int rows,
+                                               int64_t run_b, int64_t sp_b, int64_t dp_b) {
+  const int nw = (int)(run_b >> 5);
+  const int total = rows * nw;
+  for (int base = threadIdx.x; base < total; base += kBlock * kUnroll) {
+    uint4 va[kUnroll], vb[kUnroll];
+    int64_t doff[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int j = base + u * kBlock;
+      if (j < total) {
+        const int r = rows == 1 ? 0 : j / nw;
+        const int w = j - r * nw;
+        load_stream32(src + r * sp_b + 32 * (int64_t)w, va[u], vb[u]);
+        doff[u] = r * dp_b + 32 * (int64_t)w;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (base + u * kBlock < total) {
+#pragma unroll
+        for (int f = 0; f < kMaxFan; ++f)
+          if (f < nf) store_stream32(dst[f] + doff[u], va[u], vb[u]);
+      }
+    }
+  }
+}
+
+// General alignment: destination replicas must agree modulo 16. Each thread owns aligned
+// 16-byte destination words (kShiftUnroll of them per pass, loads first), assembles each from
+// the (at most two) aligned 16-byte source blocks that hold its bytes, and stores it whole, or
+// byte by byte at the two ends of a row. A source block is loaded only when it holds at least
+// one byte of the row, so no access leaves the 16-byte blocks (and hence the pages) the region
+// occupies.
+constexpr int kShiftUnroll = 4;
+
 __device__ __forceinline__ void copy_shifted(const uint8_t *__restrict__ src, uint8_t *const *dst, int nf, int rows,
                                              int64_t run_b, int64_t sp_b, int64_t dp_b) {
-  const int nwmax = (int)((run_b + 15) >> 4) + 1;
+  const int nwmax = (int)((run_b + 15) >> 4) + 1;  // destination words a row can touch
   const int total = rows * nwmax;
-  for (int j = threadIdx.x; j < total; j += kBlock) {
-    const int r = j / nwmax;
-    const int w = j - r * nwmax;
-    const uintptr_t srow = reinterpret_cast<uintptr_t>(src) + r * sp_b;
-    const int64_t drow = r * dp_b;
-    const int a = (int)((reinterpret_cast<uintptr_t>(dst[0]) + drow) & 15);
-    const int64_t start = 16 * (int64_t)w - a;  // row byte of this word's byte 0
-    if (start >= run_b) continue;
-    const int kmin = start < 0 ? (int)-start : 0;
-    const int kmax = run_b - start < 16 ? (int)(run_b - start) : 16;
-    const uintptr_t p0 = srow + start;
-    const int sh = (int)(p0 & 15);
-    const uint8_t *blk = reinterpret_cast<const uint8_t *>(p0 - sh);
-    uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-    if (kmin < 16 - sh) lo = __ldg(reinterpret_cast<const uint4 *>(blk));
-    if (sh && kmax > 16 - sh) hi = __ldg(reinterpret_cast<const uint4 *>(blk + 16));
-    const uint4 o = sh ? shift_bytes(lo, hi, sh) : lo;
-    if (kmin == 0 && kmax == 16) {
+  const uintptr_t d0 = reinterpret_cast<uintptr_t>(dst[0]);
+  for (int base = threadIdx.x; base < total; base += kBlock * kShiftUnroll) {
+    uint4 lo[kShiftUnroll], hi[kShiftUnroll];
+    int64_t dpos[kShiftUnroll];  // destination byte offset of the word's byte 0, from dst[f]
+    int kmin[kShiftUnroll], kmax[kShiftUnroll], sh[kShiftUnroll];
 #pragma unroll
-      for (int f = 0; f < kMaxFan; ++f)
-        if (f < nf) store_stream(dst[f] + drow + start, o);
-    } else {
+    for (int u = 0; u < kShiftUnroll; ++u) {
+      const int j = base + u * kBlock;
+      kmin[u] = 16;
+      kmax[u] = 0;
+      sh[u] = 0;
+      dpos[u] = 0;
+      lo[u] = make_uint4(0, 0, 0, 0);
+      hi[u] = make_uint4(0, 0, 0, 0);
+      if (j < total) {
+        const int r = rows == 1 ? 0 : j / nwmax;
+        const int w = j - r * nwmax;
+        const int64_t drow = r * dp_b;
+        const int a = (int)((d0 + drow) & 15);
+        const int64_t start = 16 * (int64_t)w - a;  // row byte of this word's byte 0
+        if (start < run_b) {
+          kmin[u] = start < 0 ? (int)-start : 0;
+          kmax[u] = run_b - start < 16 ? (int)(run_b - start) : 16;
+          dpos[u] = drow + start;
+          const uintptr_t p0 = reinterpret_cast<uintptr_t>(src) + r * sp_b + start;
+          sh[u] = (int)(p0 & 15);
+          const uint8_t *blk = reinterpret_cast<const uint8_t *>(p0 - sh[u]);
+          if (kmin[u] < 16 - sh[u]) lo[u] = __ldg(reinterpret_cast<const uint4 *>(blk));
+          if (sh[u] && kmax[u] > 16 - sh[u]) hi[u] = __ldg(reinterpret_cast<const uint4 *>(blk + 16));
+        }
+      }
+    }
 #pragma unroll
-      for (int f = 0; f < kMaxFan; ++f) {
-        if (f < nf) {
-          uint8_t *word = dst[f] + drow + start;
-          for (int k = kmin; k < kmax; ++k) word[k] = (uint8_t)byte_of(o, k);
+    for (int u = 0; u < kShiftUnroll; ++u) {
+      if (kmin[u] >= kmax[u]) continue;
+      const uint4 o = sh[u] ? shift_bytes(lo[u], hi[u], sh[u]) : lo[u];
+      if (kmin[u] == 0 && kmax[u] == 16) {
+#pragma unroll
+        for (int f = 0; f < kMaxFan; ++f)
+          if (f < nf) store_stream(dst[f] + dpos[u], o);
+      } else {
+#pragma unroll
+        for (int f = 0; f < kMaxFan; ++f) {
+          if (f < nf) {
+            uint8_t *word = dst[f] + dpos[u];
+            for (int k = kmin[u]; k < kmax[u]; ++k) word[k] = (uint8_t)byte_of(o, k);
+          }
         }
       }
     }
   }
 }
 
-__global__ void __launch_bounds__(kBlock) reshard_copy_kernel(const Item *__restrict__ items, int n_items,
+__global__ void __launch_bounds__(kBlock, RESHARD_MIN_BLOCKS) reshard_copy_kernel(const Item *__restrict__ items, int n_items,
                                                               const uint64_t *__restrict__ ptrs,
                                                               const int32_t *__restrict__ gstart,
                                                               const int32_t *__restrict__ mptr,
@@ -163,7 +269,9 @@ __global__ void __launch_bounds__(kBlock) reshard_copy_kernel(const Item *__rest
           same = same && (((reinterpret_cast<uintptr_t>(dst[f]) ^ reinterpret_cast<uintptr_t>(dst[0])) & 15) == 0);
         }
       }
-      if ((amask & 15) == 0) {
+      if (RESHARD_WIDE && (amask & 31) == 0) {
+        copy_aligned32(src, dst, nf, it.rows, run_b, sp_b, dp_b);
+      } else if ((amask & 15) == 0) {
         copy_aligned(src, dst, nf, it.rows, run_b, sp_b, dp_b);
       } else if (same) {
         copy_shifted(src, dst, nf, it.rows, run_b, sp_b, dp_b);
@@ -197,28 +305,74 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 
 __device__ __forceinline__ uint32_t mag_max2(uint32_t w) { return max(w & 0x7FFFu, (w >> 16) & 0x7FFFu); }
 
-__global__ void __launch_bounds__(kBlock) reshard_mxfp8_kernel(const Item *__restrict__ items, int n_items,
-                                                               const uint64_t *__restrict__ ptrs,
-                                                               const int32_t *__restrict__ gstart,
-                                                               const int32_t *__restrict__ mptr,
-                                                               const int64_t *__restrict__ moff, int64_t n_dst_ptrs) {
+#ifndef RESHARD_MXFP8_UNROLL
+#define RESHARD_MXFP8_UNROLL 4
+#endif
+#ifndef RESHARD_MXFP8_MIN_BLOCKS
+#define RESHARD_MXFP8_MIN_BLOCKS 4
+#endif
+#ifndef RESHARD_MXFP8_BLOCK
+#define RESHARD_MXFP8_BLOCK 256
+#endif
+#ifndef RESHARD_MXFP8_ELEMS
+#define RESHARD_MXFP8_ELEMS 8
+#endif
+constexpr int kQBlock = RESHARD_MXFP8_BLOCK;    // threads per CTA
+constexpr int kQUnroll = RESHARD_MXFP8_UNROLL;  // lane slots in flight per thread
+constexpr int kQE = RESHARD_MXFP8_ELEMS;        // BF16 elements per lane slot (8 or 16)
+constexpr int kQV = kQE / 8;                    // 16-byte loads per slot
+constexpr int kQLanes = 32 / kQE;               // lanes sharing one 32-element block
+constexpr int kQMaxFan = 4;                     // replicas per pass (pointer pairs in registers)
+static_assert(kQE == 8 || kQE == 16, "a lane holds 8 or 16 elements of a 32-element block");
+
+// Quantize 8 BF16 values (one 16-byte load) under the block amax shared by its lanes.
+__device__ __forceinline__ uint2 quantize8(uint4 v, uint32_t amax) {
+  if (amax >= 0x7F80u) return make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);  // Inf/NaN block: E4M3 NaN
+  const int x = block_exponent(amax);
+  const float inv = __uint_as_float((uint32_t)(127 - x) << 23);  // 2^-X, X in [-127, 119]
+  uint2 q;
+  q.x = cvt_e4m3x2(bf16_lo(v.x) * inv, bf16_hi(v.x) * inv) | (cvt_e4m3x2(bf16_lo(v.y) * inv, bf16_hi(v.y) * inv) << 16);
+  q.y = cvt_e4m3x2(bf16_lo(v.z) * inv, bf16_hi(v.z) * inv) | (cvt_e4m3x2(bf16_lo(v.w) * inv, bf16_hi(v.w) * inv) << 16);
+  return q;
+}
+
+// E8M0 byte of a block: 0xFF (NaN) when the block holds Inf/NaN, else X + 127.
+__device__ __forceinline__ uint32_t scale_byte(uint32_t amax) {
+  return amax >= 0x7F80u ? 0xFFu : (uint32_t)(block_exponent(amax) + 127);
+}
+
+__device__ __forceinline__ uint4 load_bf16x8(const uint8_t *p, bool vec) {
+  if (vec) return load_stream(p);
+  const uint16_t *h = reinterpret_cast<const uint16_t *>(p);
+  return make_uint4((uint32_t)h[0] | ((uint32_t)h[1] << 16), (uint32_t)h[2] | ((uint32_t)h[3] << 16),
+                    (uint32_t)h[4] | ((uint32_t)h[5] << 16), (uint32_t)h[6] | ((uint32_t)h[7] << 16));
+}
+
+__device__ __forceinline__ void store_bytes(uint8_t *p, uint32_t w) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) p[k] = (uint8_t)(w >> (8 * k));
+}
+
+__global__ void __launch_bounds__(kQBlock, RESHARD_MXFP8_MIN_BLOCKS) reshard_mxfp8_kernel(
+    const Item *__restrict__ items, int n_items, const uint64_t *__restrict__ ptrs, const int32_t *__restrict__ gstart,
+    const int32_t *__restrict__ mptr, const int64_t *__restrict__ moff, int64_t n_dst_ptrs) {
   const int lane = threadIdx.x & 31;
   for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
     const Item it = items[i];
     const uint8_t *src = reinterpret_cast<const uint8_t *>(ptrs[it.src]) + it.src_off * 2;
     const int g0 = gstart[it.group];
     const int nrep = gstart[it.group + 1] - g0;
-    const int oct = it.run >> 3;  // 8-element groups per row; a multiple of 4
-    const int total = it.rows * oct;
+    const int per_row = it.run / kQE;  // lane slots per row; a multiple of kQLanes
+    const int total = it.rows * per_row;
     const int64_t sp_b = it.src_pitch * 2;
     const bool vec = ((reinterpret_cast<uintptr_t>(src) | (it.rows > 1 ? (uintptr_t)sp_b : 0)) & 15) == 0;
-    for (int f0 = 0; f0 < nrep; f0 += kMaxFan) {
-      const int nf = min(kMaxFan, nrep - f0);
-      uint8_t *dq[kMaxFan];
-      uint8_t *ds[kMaxFan];
+    for (int f0 = 0; f0 < nrep; f0 += kQMaxFan) {
+      const int nf = min(kQMaxFan, nrep - f0);
+      uint8_t *dq[kQMaxFan];
+      uint8_t *ds[kQMaxFan];
       uintptr_t amask = it.rows > 1 ? (uintptr_t)it.dst_pitch : 0;
 #pragma unroll
-      for (int f = 0; f < kMaxFan; ++f) {
+      for (int f = 0; f < kQMaxFan; ++f) {
         dq[f] = nullptr;
         ds[f] = nullptr;
         if (f < nf) {
@@ -229,58 +383,58 @@ __global__ void __launch_bounds__(kBlock) reshard_mxfp8_kernel(const Item *__res
           amask |= reinterpret_cast<uintptr_t>(dq[f]);
         }
       }
-      const bool st8 = (amask & 7) == 0;
-      for (int j0 = threadIdx.x - lane; j0 < total; j0 += kBlock) {
-        const int j = j0 + lane;
-        const bool valid = j < total;
-        int r = 0, o = 0;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (valid) {
-          r = j / oct;
-          o = j - r * oct;
-          const uint8_t *p = src + r * sp_b + 16 * (int64_t)o;
-          if (vec) {
-            v = load_stream(p);
-          } else {
-            const uint16_t *h = reinterpret_cast<const uint16_t *>(p);
-            v.x = (uint32_t)h[0] | ((uint32_t)h[1] << 16);
-            v.y = (uint32_t)h[2] | ((uint32_t)h[3] << 16);
-            v.z = (uint32_t)h[4] | ((uint32_t)h[5] << 16);
-            v.w = (uint32_t)h[6] | ((uint32_t)h[7] << 16);
+      const bool stv = (amask & (kQE - 1)) == 0;  // one kQE-byte store per slot
+      // j0 is warp-uniform, so every lane takes part in every shuffle
+      for (int j0 = threadIdx.x - lane; j0 < total; j0 += kQBlock * kQUnroll) {
+        uint4 v[kQUnroll][kQV];
+        int64_t eoff[kQUnroll];  // element offset of this slot's first value within the item
+#pragma unroll
+        for (int u = 0; u < kQUnroll; ++u) {
+          const int j = j0 + u * kQBlock + lane;
+#pragma unroll
+          for (int k = 0; k < kQV; ++k) v[u][k] = make_uint4(0, 0, 0, 0);
+          eoff[u] = -1;
+          if (j < total) {
+            const int r = it.rows == 1 ? 0 : j / per_row;
+            const int o = j - r * per_row;
+            const uint8_t *p = src + r * sp_b + 2 * kQE * (int64_t)o;
+            eoff[u] = r * it.dst_pitch + kQE * (int64_t)o;
+#pragma unroll
+            for (int k = 0; k < kQV; ++k) v[u][k] = load_bf16x8(p + 16 * k, vec);
           }
         }
-        uint32_t amax = max(max(mag_max2(v.x), mag_max2(v.y)), max(mag_max2(v.z), mag_max2(v.w)));
-        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        if (!valid) continue;
-        uint2 q;
-        uint32_t sbyte;
-        if (amax >= 0x7F80u) {  // Inf or NaN in the block: E8M0 NaN scale, E4M3 NaN elements
-          q = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
-          sbyte = 0xFF;
-        } else {
-          const int x = block_exponent(amax);
-          const float inv = __uint_as_float((uint32_t)(127 - x) << 23);  // 2^-X, X in [-127, 119]
-          q.x = cvt_e4m3x2(bf16_lo(v.x) * inv, bf16_hi(v.x) * inv) |
-                (cvt_e4m3x2(bf16_lo(v.y) * inv, bf16_hi(v.y) * inv) << 16);
-          q.y = cvt_e4m3x2(bf16_lo(v.z) * inv, bf16_hi(v.z) * inv) |
-                (cvt_e4m3x2(bf16_lo(v.w) * inv, bf16_hi(v.w) * inv) << 16);
-          sbyte = (uint32_t)(x + 127);
-        }
-        const int64_t eoff = r * it.dst_pitch + 8 * (int64_t)o;  // element offset within the item
 #pragma unroll
-        for (int f = 0; f < kMaxFan; ++f) {
-          if (f < nf) {
-            uint8_t *p = dq[f] + eoff;
-            if (st8) {
-              __stcs(reinterpret_cast<uint2 *>(p), q);
-            } else {
+        for (int u = 0; u < kQUnroll; ++u) {
+          uint32_t amax = 0;
 #pragma unroll
-              for (int k = 0; k < 4; ++k) p[k] = (uint8_t)(q.x >> (8 * k));
+          for (int k = 0; k < kQV; ++k)
+            amax = max(amax, max(max(mag_max2(v[u][k].x), mag_max2(v[u][k].y)),
+                                 max(mag_max2(v[u][k].z), mag_max2(v[u][k].w))));
 #pragma unroll
-              for (int k = 0; k < 4; ++k) p[4 + k] = (uint8_t)(q.y >> (8 * k));
+          for (int s = 1; s < kQLanes; s <<= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, s));
+          if (eoff[u] < 0) continue;
+          uint2 q[kQV];
+#pragma unroll
+          for (int k = 0; k < kQV; ++k) q[k] = quantize8(v[u][k], amax);
+          const uint32_t sbyte = scale_byte(amax);
+#pragma unroll
+          for (int f = 0; f < kQMaxFan; ++f) {
+            if (f < nf) {
+              uint8_t *p = dq[f] + eoff[u];
+              if (stv) {
+                if constexpr (kQV == 2)
+                  __stcs(reinterpret_cast<uint4 *>(p), make_uint4(q[0].x, q[0].y, q[kQV - 1].x, q[kQV - 1].y));
+                else
+                  __stcs(reinterpret_cast<uint2 *>(p), q[0]);
+              } else {
+#pragma unroll
+                for (int k = 0; k < kQV; ++k) {
+                  store_bytes(p + 8 * k, q[k].x);
+                  store_bytes(p + 8 * k + 4, q[k].y);
+                }
+              }
+              if ((lane & (kQLanes - 1)) == 0) ds[f][eoff[u] / 32] = (uint8_t)sbyte;
             }
-            if ((lane & 3) == 0) ds[f][eoff / 32] = (uint8_t)sbyte;
           }
         }
       }
@@ -326,7 +480,7 @@ int launch_caps(int device, LaunchCaps &c) {
   int sms = 0, b1 = 0, b2 = 0;
   RS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device));
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, reshard_copy_kernel, kBlock, 0));
-  RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b2, reshard_mxfp8_kernel, kBlock, 0));
+  RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b2, reshard_mxfp8_kernel, kQBlock, 0));
   g_caps.device = device;
   g_caps.copy_grid = sms * std::max(1, b1);
   g_caps.mxfp8_grid = sms * std::max(1, b2);
@@ -368,7 +522,7 @@ int launch(reshard_plan_t *p, int set, bool quant, cudaStream_t stream, const La
   const Item *items = static_cast<const Item *>(p->d_items[set]);
   if (quant) {
     const int grid = std::min(n, caps.mxfp8_grid);
-    reshard_mxfp8_kernel<<<grid, kBlock, 0, stream>>>(items, n, p->d_ptrs, p->d_grp_start, p->d_mem_ptr,
+    reshard_mxfp8_kernel<<<grid, kQBlock, 0, stream>>>(items, n, p->d_ptrs, p->d_grp_start, p->d_mem_ptr,
                                                       p->d_mem_off, p->n_dst_ptrs);
   } else {
     const int grid = std::min(n, caps.copy_grid);

@@ -7,9 +7,7 @@ pointers through ``src_ptrs(wl, t)`` / ``dst_ptrs(wl, t)``.
 """
 from __future__ import annotations
 
-from typing import List, Tuple
-
-from .binding import Plan, reshard_plan_batch
+from .binding import Plan, pointer_array, reshard_plan_batch
 
 
 def plan_workload(wl) -> Plan:
@@ -19,10 +17,10 @@ def plan_workload(wl) -> Plan:
     return reshard_plan_batch(wl.tensors, src_cap, dst_cap)
 
 
-def workload_pointers(wl, layout) -> Tuple[List[int], List[int]]:
-    """Flat source / destination pointer arrays in plan order."""
+def workload_pointers(wl, layout):
+    """Flat source / destination pointer arrays in plan order (uint64 numpy arrays)."""
     src, dst = [], []
     for t in range(len(wl.tensors)):
         src += layout.src_ptrs(wl, t)
         dst += layout.dst_ptrs(wl, t)
-    return src, dst
+    return pointer_array(src), pointer_array(dst)
