@@ -306,7 +306,7 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ uint32_t mag_max2(uint32_t w) { return max(w & 0x7FFFu, (w >> 16) & 0x7FFFu); }
 
 #ifndef RESHARD_MXFP8_UNROLL
-#define RESHARD_MXFP8_UNROLL 4
+#define RESHARD_MXFP8_UNROLL 2
 #endif
 #ifndef RESHARD_MXFP8_MIN_BLOCKS
 #define RESHARD_MXFP8_MIN_BLOCKS 4
@@ -315,7 +315,7 @@ __device__ __forceinline__ uint32_t mag_max2(uint32_t w) { return max(w & 0x7FFF
 #define RESHARD_MXFP8_BLOCK 256
 #endif
 #ifndef RESHARD_MXFP8_ELEMS
-#define RESHARD_MXFP8_ELEMS 8
+#define RESHARD_MXFP8_ELEMS 16
 #endif
 constexpr int kQBlock = RESHARD_MXFP8_BLOCK;    // threads per CTA
 constexpr int kQUnroll = RESHARD_MXFP8_UNROLL;  // lane slots in flight per thread

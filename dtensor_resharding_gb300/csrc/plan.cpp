@@ -224,7 +224,7 @@ BoxKey key_of(const Box &b) {
 // Cut one strided region into 2-D work items (rows x run). `ext` are the region extents,
 // `so`/`ss` and `dof`/`ds` the element offset and strides on the source and destination side.
 void emit_items(int nd, const int64_t *ext, int64_t so, const int64_t *ss, int64_t dof, const int64_t *ds,
-                int32_t src, int32_t group, int esize, std::vector<Item> &out) {
+                int32_t src, int32_t group, int esize, int64_t item_bytes, std::vector<Item> &out) {
   for (int d = 0; d < nd; ++d)
     if (ext[d] <= 0) return;
   // innermost run, merged outward while both sides stay contiguous
@@ -260,8 +260,8 @@ void emit_items(int nd, const int64_t *ext, int64_t so, const int64_t *ss, int64
     it.src = src;
     it.group = group;
     it.esize = esize;
-    if (run_bytes > kItemBytes) {
-      int64_t seg = (kItemBytes / esize) / kRunSplitElems * kRunSplitElems;
+    if (run_bytes > item_bytes) {
+      int64_t seg = (item_bytes / esize) / kRunSplitElems * kRunSplitElems;
       if (seg < kRunSplitElems) seg = kRunSplitElems;
       for (int64_t r = 0; r < rows; ++r)
         for (int64_t c = 0; c < run; c += seg) {
@@ -274,7 +274,7 @@ void emit_items(int nd, const int64_t *ext, int64_t so, const int64_t *ss, int64
           out.push_back(it);
         }
     } else {
-      const int64_t per = std::max<int64_t>(1, kItemBytes / std::max<int64_t>(1, run_bytes));
+      const int64_t per = std::max<int64_t>(1, item_bytes / std::max<int64_t>(1, run_bytes));
       for (int64_t r = 0; r < rows; r += per) {
         it.rows = (int32_t)std::min(per, rows - r);
         it.run = (int32_t)run;
@@ -460,6 +460,11 @@ int build(const reshard_tensor_spec_t *specs, int n, reshard_plan_t **out) {
   // 5. work items: direct (source -> destination replicas), pack (source -> message),
   //    unpack (message -> destination replicas)
   int64_t bytes_read = 0, bytes_written = 0, global_bytes = 0;
+  int64_t plan_bytes = 0;
+  for (const Region &r : plan->regions)
+    plan_bytes += volume(r.box, plan->tensors[(size_t)r.tensor].ndim) * plan->tensors[(size_t)r.tensor].esize;
+  int64_t item_bytes = kMaxItemBytes;
+  while (item_bytes > kMinItemBytes && plan_bytes / item_bytes < kItemsPerPlan) item_bytes /= 2;
   for (const Region &r : plan->regions) {
     const TensorInfo &t = plan->tensors[(size_t)r.tensor];
     const int nd = t.ndim;
@@ -481,9 +486,9 @@ int build(const reshard_tensor_spec_t *specs, int n, reshard_plan_t **out) {
     }
     const int32_t sp = (int32_t)(t.src_base + r.src);
     const int64_t mo = r.msg_off_bytes / t.esize;
-    emit_items(nd, ext, so, sv.strides, dof, dv.strides, sp, r.group, t.esize, plan->items[kDirect]);
-    emit_items(nd, ext, so, sv.strides, mo, ms, sp, plan->workspace_group, t.esize, plan->items[kPack]);
-    emit_items(nd, ext, mo, ms, dof, dv.strides, (int32_t)plan->workspace_ptr, r.group, t.esize,
+    emit_items(nd, ext, so, sv.strides, dof, dv.strides, sp, r.group, t.esize, item_bytes, plan->items[kDirect]);
+    emit_items(nd, ext, so, sv.strides, mo, ms, sp, plan->workspace_group, t.esize, item_bytes, plan->items[kPack]);
+    emit_items(nd, ext, mo, ms, dof, dv.strides, (int32_t)plan->workspace_ptr, r.group, t.esize, item_bytes,
                plan->items[kUnpack]);
     const int64_t b = volume(r.box, nd) * t.esize;
     bytes_read += b;

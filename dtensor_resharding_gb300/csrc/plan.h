@@ -13,8 +13,12 @@ namespace reshard {
 constexpr int kMaxDims = RESHARD_MAX_DIMS;
 
 // Source bytes per device work item. Regions are cut into items of about this size so a
-// persistent grid that walks the item table round-robin stays balanced.
-constexpr int64_t kItemBytes = 256 * 1024;
+// persistent grid that walks the item table round-robin stays balanced: the largest power of
+// two in [kMinItemBytes, kMaxItemBytes] that still gives about kItemsPerPlan items per plan
+// (small plans get small items, so every SM has work).
+constexpr int64_t kMaxItemBytes = 256 * 1024;
+constexpr int64_t kMinItemBytes = 16 * 1024;
+constexpr int64_t kItemsPerPlan = 4096;
 // Long runs are cut at multiples of this many elements (keeps MXFP8 blocks whole).
 constexpr int64_t kRunSplitElems = 2048;
 

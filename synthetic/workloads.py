@@ -318,6 +318,8 @@ WORKLOAD_NAMES = {
     "many_small_10000_tp4_to_dp2tp2": lambda: many_small(),
     # reduced layer counts of the same shapes, for profiler captures (a few GB on the device)
     "dense_ffn_4x14336x4096_tp8_to_dp2tp2": lambda: dense_ffn(layers=4),
+    "dense_ffn_2x14336x4096_tp8_to_dp2tp2": lambda: dense_ffn(layers=2),
+    "moe_1x32x1536x4096_ep16_to_tp4_mxfp8": lambda: moe_experts(layers=1, experts=32, dst="tp4"),
     "moe_1x128x1536x4096_ep16_to_ep8": lambda: moe_experts(layers=1, dst="ep8"),
     "moe_1x128x1536x4096_ep16_to_tp4_mxfp8": lambda: moe_experts(layers=1, dst="tp4"),
 }
