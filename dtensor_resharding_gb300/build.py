@@ -43,7 +43,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags: List[str] = (
     nvcc = _nvcc()
     common = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
     jobs = [
-        [nvcc, *common, "-x", "c++", "-c", os.path.join(CSRC, "plan.cpp"), "-o", os.path.join(bdir, "plan.o")],
+        [nvcc, *common, *extra, "-x", "c++", "-c", os.path.join(CSRC, "plan.cpp"), "-o", os.path.join(bdir, "plan.o")],
         [nvcc, *common, *ARCH, "-lineinfo", "-Xptxas", "-v" if verbose else "-O3", *extra,
          "-c", os.path.join(CSRC, "execute.cu"), "-o", os.path.join(bdir, "execute.o")],
     ]

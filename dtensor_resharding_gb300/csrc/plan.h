@@ -16,9 +16,15 @@ constexpr int kMaxDims = RESHARD_MAX_DIMS;
 // persistent grid that walks the item table round-robin stays balanced: the largest power of
 // two in [kMinItemBytes, kMaxItemBytes] that still gives about kItemsPerPlan items per plan
 // (small plans get small items, so every SM has work).
+#ifndef RESHARD_ITEMS_PER_PLAN
+#define RESHARD_ITEMS_PER_PLAN 1024
+#endif
+#ifndef RESHARD_MIN_ITEM_KIB
+#define RESHARD_MIN_ITEM_KIB 32
+#endif
 constexpr int64_t kMaxItemBytes = 256 * 1024;
-constexpr int64_t kMinItemBytes = 16 * 1024;
-constexpr int64_t kItemsPerPlan = 4096;
+constexpr int64_t kMinItemBytes = RESHARD_MIN_ITEM_KIB * 1024;
+constexpr int64_t kItemsPerPlan = RESHARD_ITEMS_PER_PLAN;
 // Long runs are cut at multiples of this many elements (keeps MXFP8 blocks whole).
 constexpr int64_t kRunSplitElems = 2048;
 
