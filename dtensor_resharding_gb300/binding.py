@@ -30,8 +30,8 @@ MODES = {"direct": RESHARD_DIRECT, "packed": RESHARD_PACKED}
 QUANTS = {"none": RESHARD_QUANT_NONE, "mxfp8": RESHARD_QUANT_MXFP8}
 EXPORTED = ("reshard_plan_create", "reshard_plan_batch", "reshard_execute", "reshard_execute_static",
             "reshard_plan_stats",
-            "reshard_plan_regions", "reshard_plan_group_members", "reshard_plan_items", "reshard_plan_destroy",
-            "reshard_last_error")
+            "reshard_plan_regions", "reshard_plan_group_members", "reshard_plan_items", "reshard_plan_slabs",
+            "reshard_plan_status", "reshard_plan_destroy", "reshard_last_error")
 
 _i64p = ctypes.POINTER(ctypes.c_int64)
 _i32p = ctypes.POINTER(ctypes.c_int32)
@@ -83,6 +83,8 @@ def _load(path: str = LIB_PATH):
     lib.reshard_plan_group_members.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, _i32p, _i64p]
     lib.reshard_plan_items.argtypes = [vp, ctypes.c_int, ctypes.c_int64, vp, _i64p, _i32p, _i32p, _i64p, _i64p,
                                        _i64p]
+    lib.reshard_plan_slabs.argtypes = [vp, ctypes.c_int64, _i64p, _i64p]
+    lib.reshard_plan_status.argtypes = [vp, _i32p, ctypes.c_int]
     lib.reshard_plan_destroy.argtypes = [vp]
     lib.reshard_last_error.argtypes = []
     lib.reshard_last_error.restype = ctypes.c_char_p
@@ -285,13 +287,19 @@ ITEM_DTYPE = [("src_off", "<i8"), ("dst_off", "<i8"), ("src_pitch", "<i8"), ("ds
               ("pad", "<i4", (3,))]
 
 
+TITEM_DTYPE = [("src_off", "<i8"), ("dst_off", "<i8"), ("src_pitch", "<i8"), ("dst_pitch", "<i8"),
+               ("rows", "<i4"), ("cols", "<i4"), ("src", "<i4"), ("group", "<i4"), ("esize", "<i4"),
+               ("slab", "<i4"), ("x", "<i4"), ("y", "<i4")]
+
+
 def reshard_plan_items(plan: Plan, which: int = 0):
-    """(items as a numpy structured array, group_start, member_ptr, member_off) of one pass."""
+    """(items as a numpy structured array, group_start, member_ptr, member_off) of one table:
+    0/1/2 strided-copy items of the direct/pack/unpack pass, 3/4/5 their transposing items."""
     import numpy as np
     n, ng, nm = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
     _check(LIB.reshard_plan_items(plan.handle, which, 0, None, ctypes.byref(n), None, None, None,
                                   ctypes.byref(ng), ctypes.byref(nm)))
-    items = np.zeros(n.value, dtype=ITEM_DTYPE)
+    items = np.zeros(n.value, dtype=ITEM_DTYPE if which < 3 else TITEM_DTYPE)
     gs = np.zeros(ng.value + 1, np.int32)
     mp = np.zeros(max(1, nm.value), np.int32)
     mo = np.zeros(max(1, nm.value), np.int64)
@@ -299,6 +307,22 @@ def reshard_plan_items(plan: Plan, which: int = 0):
                                   gs.ctypes.data_as(_i32p), mp.ctypes.data_as(_i32p), mo.ctypes.data_as(_i64p),
                                   ctypes.byref(ng), ctypes.byref(nm)))
     return items, gs, mp[: nm.value], mo[: nm.value]
+
+
+def reshard_plan_slabs(plan: Plan):
+    """[(pointer index, esize, base offset, cols, rows, pitch), ...] read by the TMA kernel."""
+    n = ctypes.c_int64()
+    _check(LIB.reshard_plan_slabs(plan.handle, 0, None, ctypes.byref(n)))
+    out = (ctypes.c_int64 * max(1, 6 * n.value))()
+    _check(LIB.reshard_plan_slabs(plan.handle, n.value, out, ctypes.byref(n)))
+    return [tuple(out[6 * i: 6 * i + 6]) for i in range(n.value)]
+
+
+def reshard_plan_status(plan: Plan, reset: bool = False) -> int:
+    """Device status word of the plan (0 = fine); synchronizes the device."""
+    st = ctypes.c_int32()
+    _check(LIB.reshard_plan_status(plan.handle, ctypes.byref(st), 1 if reset else 0))
+    return int(st.value)
 
 
 def reshard_plan_destroy(plan: Plan) -> None:

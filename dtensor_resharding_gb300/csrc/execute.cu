@@ -16,6 +16,8 @@
 //
 // Nothing here is a contraction; both kernels are bound by HBM bandwidth. Sources and
 // destinations must not overlap in memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -442,6 +444,201 @@ __global__ void __launch_bounds__(kQBlock, RESHARD_MXFP8_MIN_BLOCKS) reshard_mxf
   }
 }
 
+// ----------------------------------------------------------- transposing copy (TMA) --
+//
+// reshard_transpose_kernel moves regions whose source is contiguous along one dim (C) and whose
+// destination is contiguous along another (R): a transposed layout on one side. Tiles of
+// 64 rows (R) x 128 bytes (C) are staged in shared memory by TMA 2-D box loads
+// (cp.async.bulk.tensor, 128-byte swizzle, mbarrier completion, two stages in flight); each
+// thread then reads 32 bytes' worth of one column down the tile (conflict-free thanks to the
+// swizzle) and stores them as one contiguous 32-byte run of the destination. Where a slab's
+// tensor map could not be encoded (base or pitch not 16-byte aligned), the tile is filled by
+// plain loads instead. Every wait on an mbarrier is bounded; on timeout the kernel sets bit 0
+// of the plan's status word and returns.
+
+constexpr int kTBlock = 256;                          // threads per CTA (one unit per tile per thread)
+constexpr int kTStages = 2;
+constexpr int kTileBytes = kTileRows * kTileRowBytes;  // 8 KiB
+constexpr unsigned long long kWaitLimitNs = 200ull * 1000 * 1000;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, unsigned long long deadline) {
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (global_ns() > deadline) return false;
+  }
+}
+
+// Byte offset in a 128-byte-swizzled tile of (row, byte within the row).
+__device__ __forceinline__ int swz(int row, int byte) { return row * kTileRowBytes + ((((byte >> 4) ^ (row & 7))) << 4) + (byte & 15); }
+
+template <int ES>
+__device__ __forceinline__ void elem_store(uint8_t *p, const uint8_t *from) {
+  if constexpr (ES == 1) *p = *from;
+  if constexpr (ES == 2) *reinterpret_cast<uint16_t *>(p) = *reinterpret_cast<const uint16_t *>(from);
+  if constexpr (ES == 4) *reinterpret_cast<uint32_t *>(p) = *reinterpret_cast<const uint32_t *>(from);
+  if constexpr (ES == 8) *reinterpret_cast<uint64_t *>(p) = *reinterpret_cast<const uint64_t *>(from);
+}
+
+// Fill one tile with plain loads (same swizzled layout as TMA). Column x of the tile is slab
+// column x0 + x; only elements inside the item are read, the rest become zero.
+template <int ES>
+__device__ __forceinline__ void tile_fill_plain(uint8_t *tile, const TItem &it, const uint8_t *src, int x0, int y0) {
+  constexpr int TC = kTileRowBytes / ES;
+  for (int e = threadIdx.x; e < kTileRows * TC; e += kTBlock) {
+    const int row = e / TC, col = e - row * TC;
+    const int xs = x0 + col - it.x, ys = y0 + row - it.y;  // item-relative
+    uint8_t v[ES];
+#pragma unroll
+    for (int b = 0; b < ES; ++b) v[b] = 0;
+    if (xs >= 0 && xs < it.cols && ys >= 0 && ys < it.rows) {
+      const uint8_t *g = src + ((int64_t)ys * it.src_pitch + xs) * ES;
+#pragma unroll
+      for (int b = 0; b < ES; ++b) v[b] = g[b];
+    }
+    uint8_t *d = tile + swz(row, col * ES);
+#pragma unroll
+    for (int b = 0; b < ES; ++b) d[b] = v[b];
+  }
+}
+
+// One tile to the destinations: thread = (column, 32-byte chunk of rows).
+template <int ES>
+__device__ __forceinline__ void tile_store(const uint8_t *tile, const TItem &it, uint8_t *const *dst, int nf, int x0,
+                                           int y0) {
+  constexpr int TC = kTileRowBytes / ES;
+  constexpr int RPC = 32 / ES;  // rows per 32-byte chunk
+  const int col = threadIdx.x % TC, chunk = threadIdx.x / TC;
+  const int c = x0 + col - it.x;            // item column
+  const int r0 = y0 + chunk * RPC - it.y;   // item row of the chunk's first element
+  if (c < 0 || c >= it.cols || r0 >= it.rows) return;
+  alignas(16) uint8_t buf[32];
+#pragma unroll
+  for (int k = 0; k < RPC; ++k) elem_store<ES>(buf + k * ES, tile + swz(chunk * RPC + k, col * ES));
+  const int nvalid = min(RPC, it.rows - r0);
+  const int64_t eoff = it.dst_off + (int64_t)c * it.dst_pitch + r0;
+#pragma unroll
+  for (int f = 0; f < kMaxFan; ++f) {
+    if (f >= nf) break;
+    uint8_t *p = dst[f] + eoff * ES;
+    if (nvalid == RPC && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+      store_stream(p, *reinterpret_cast<const uint4 *>(buf));
+      store_stream(p + 16, *reinterpret_cast<const uint4 *>(buf + 16));
+    } else {
+      for (int k = 0; k < nvalid; ++k) elem_store<ES>(p + k * ES, buf + k * ES);
+    }
+  }
+}
+
+template <int ES>
+__device__ void transpose_item(const TItem &it, const uint8_t *src, uint8_t *const *dst, int nf, const CUtensorMap *map,
+                               bool tma, uint8_t (*tile)[kTileBytes], uint64_t *bar, uint32_t &phases,
+                               int32_t *status, bool &abort) {
+  constexpr int TC = kTileRowBytes / ES;
+  constexpr int XAL = 16 / ES;                 // TMA box x must start on a 16-byte boundary
+  const int xa = it.x / XAL * XAL;             // first tile's slab column
+  const int ntc = (it.x + it.cols - xa + TC - 1) / TC;
+  const int ntr = (it.rows + kTileRows - 1) / kTileRows;
+  const int nt = ntc * ntr;
+  if (!tma) {
+    for (int t = 0; t < nt; ++t) {
+      const int x0 = xa + (t % ntc) * TC, y0 = it.y + (t / ntc) * kTileRows;
+      __syncthreads();
+      tile_fill_plain<ES>(tile[0], it, src, x0, y0);
+      __syncthreads();
+      tile_store<ES>(tile[0], it, dst, nf, x0, y0);
+    }
+    __syncthreads();
+    return;
+  }
+  auto issue = [&](int t, int stage) {
+    if (threadIdx.x == 0) {
+      const int x0 = xa + (t % ntc) * TC, y0 = it.y + (t / ntc) * kTileRows;
+      const uint32_t b = smem_u32(&bar[stage]);
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(kTileBytes) : "memory");
+      asm volatile(
+          "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+              smem_u32(tile[stage])),
+          "l"(reinterpret_cast<uint64_t>(map)), "r"(x0), "r"(y0), "r"(b)
+          : "memory");
+    }
+  };
+  if (threadIdx.x == 0)
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+  issue(0, 0);
+  for (int t = 0; t < nt; ++t) {
+    const int stage = t & 1;
+    if (t + 1 < nt) issue(t + 1, stage ^ 1);
+    const uint32_t parity = (phases >> stage) & 1;
+    const bool ok = bar_wait(smem_u32(&bar[stage]), parity, global_ns() + kWaitLimitNs);
+    if (__syncthreads_or(!ok)) {
+      // a TMA load never completed: report, give the copies in flight one more bounded wait, stop
+      if (threadIdx.x == 0) atomicOr(status, 1);
+      bar_wait(smem_u32(&bar[stage]), parity, global_ns() + kWaitLimitNs);
+      if (t + 1 < nt) bar_wait(smem_u32(&bar[stage ^ 1]), (phases >> (stage ^ 1)) & 1, global_ns() + kWaitLimitNs);
+      abort = true;
+      return;
+    }
+    phases ^= 1u << stage;
+    const int x0 = xa + (t % ntc) * TC, y0 = it.y + (t / ntc) * kTileRows;
+    tile_store<ES>(tile[stage], it, dst, nf, x0, y0);
+    __syncthreads();  // the stage is free for the load two tiles ahead
+  }
+}
+
+__global__ void __launch_bounds__(kTBlock) reshard_transpose_kernel(
+    const TItem *__restrict__ items, int n_items, const uint64_t *__restrict__ ptrs, const int32_t *__restrict__ gstart,
+    const int32_t *__restrict__ mptr, const int64_t *__restrict__ moff, const CUtensorMap *__restrict__ maps,
+    const int32_t *__restrict__ map_ok, int32_t *status) {
+  __shared__ __align__(1024) uint8_t tile[kTStages][kTileBytes];
+  __shared__ __align__(8) uint64_t bar[kTStages];
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTStages; ++s) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar[s])));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  uint32_t phases = 0;  // expected parity bit per stage
+  bool abort = false;
+  for (int i = blockIdx.x; i < n_items && !abort; i += gridDim.x) {
+    const TItem it = items[i];
+    const uint8_t *src = reinterpret_cast<const uint8_t *>(ptrs[it.src]) + it.src_off * it.esize;
+    const bool tma = it.map >= 0 && map_ok[it.map];
+    const CUtensorMap *map = tma ? maps + it.map : nullptr;
+    const int g0 = gstart[it.group];
+    const int nrep = gstart[it.group + 1] - g0;
+    for (int f0 = 0; f0 < nrep && !abort; f0 += kMaxFan) {
+      const int nf = min(kMaxFan, nrep - f0);
+      uint8_t *dst[kMaxFan];
+#pragma unroll
+      for (int f = 0; f < kMaxFan; ++f) {
+        dst[f] = nullptr;
+        if (f < nf) dst[f] = reinterpret_cast<uint8_t *>(ptrs[mptr[g0 + f0 + f]]) + moff[g0 + f0 + f] * it.esize;
+      }
+      switch (it.esize) {
+        case 1: transpose_item<1>(it, src, dst, nf, map, tma, tile, bar, phases, status, abort); break;
+        case 2: transpose_item<2>(it, src, dst, nf, map, tma, tile, bar, phases, status, abort); break;
+        case 4: transpose_item<4>(it, src, dst, nf, map, tma, tile, bar, phases, status, abort); break;
+        default: transpose_item<8>(it, src, dst, nf, map, tma, tile, bar, phases, status, abort); break;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------- host side --
 
 namespace {
@@ -469,6 +666,7 @@ struct LaunchCaps {
   int device = -1;
   int copy_grid = 0;
   int mxfp8_grid = 0;
+  int transpose_grid = 0;
 };
 thread_local LaunchCaps g_caps;
 
@@ -477,13 +675,15 @@ int launch_caps(int device, LaunchCaps &c) {
     c = g_caps;
     return RESHARD_OK;
   }
-  int sms = 0, b1 = 0, b2 = 0;
+  int sms = 0, b1 = 0, b2 = 0, b3 = 0;
   RS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device));
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, reshard_copy_kernel, kBlock, 0));
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b2, reshard_mxfp8_kernel, kQBlock, 0));
+  RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b3, reshard_transpose_kernel, kTBlock, 0));
   g_caps.device = device;
   g_caps.copy_grid = sms * std::max(1, b1);
   g_caps.mxfp8_grid = sms * std::max(1, b2);
+  g_caps.transpose_grid = sms * std::max(1, b3);
   c = g_caps;
   return RESHARD_OK;
 }
@@ -502,7 +702,62 @@ int bind_device(reshard_plan_t *p) {
   if ((rc = upload(&p->d_mem_ptr, p->mem_ptr))) return rc;
   if ((rc = upload(&p->d_mem_off, p->mem_off))) return rc;
   RS_CUDA(cudaMalloc(reinterpret_cast<void **>(&p->d_ptrs), pointer_table_size(p) * sizeof(uint64_t)));
+  RS_CUDA(cudaMalloc(reinterpret_cast<void **>(&p->d_status), sizeof(int32_t)));
+  RS_CUDA(cudaMemset(p->d_status, 0, sizeof(int32_t)));
+  if (!p->slabs.empty()) {
+    RS_CUDA(cudaMalloc(&p->d_maps, p->slabs.size() * sizeof(CUtensorMap)));
+    RS_CUDA(cudaMalloc(reinterpret_cast<void **>(&p->d_map_ok), p->slabs.size() * sizeof(int32_t)));
+  }
   p->device = dev;
+  return RESHARD_OK;
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+std::once_flag g_encode_once;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  std::call_once(g_encode_once, [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+// One 2-D tensor map per source slab of the transposing items, for the current pointers. A slab
+// whose base or row pitch is not 16-byte aligned (or that the driver rejects) gets map_ok = 0:
+// its tiles are then loaded with plain loads.
+int encode_maps(reshard_plan_t *p, const std::vector<uint64_t> &table, cudaStream_t stream) {
+  const size_t n = p->slabs.size();
+  if (!n) return RESHARD_OK;
+  std::vector<CUtensorMap> maps(n);
+  std::vector<int32_t> ok(n, 0);
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  for (size_t i = 0; i < n && enc; ++i) {
+    const SlabSpec &sl = p->slabs[i];
+    const uint64_t base = table[(size_t)sl.ptr] + (uint64_t)sl.base_off * (uint64_t)sl.esize;
+    const uint64_t stride = (uint64_t)sl.pitch * (uint64_t)sl.esize;
+    if (!table[(size_t)sl.ptr] || base % 16 || stride % 16 || stride == 0 || stride >= (1ull << 40) || sl.cols < 1 ||
+        sl.rows < 1 || sl.cols > (1ll << 32) || sl.rows > (1ll << 32))
+      continue;
+    const CUtensorMapDataType dt = sl.esize == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : sl.esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
+                                   : sl.esize == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32
+                                                   : CU_TENSOR_MAP_DATA_TYPE_UINT64;
+    const cuuint64_t dims[2] = {(cuuint64_t)sl.cols, (cuuint64_t)sl.rows};
+    const cuuint64_t strides[1] = {stride};
+    const cuuint32_t box[2] = {(cuuint32_t)(kTileRowBytes / sl.esize), (cuuint32_t)kTileRows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(&maps[i], dt, 2, reinterpret_cast<void *>(base), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    ok[i] = r == CUDA_SUCCESS ? 1 : 0;
+  }
+  RS_CUDA(cudaMemcpyAsync(p->d_maps, maps.data(), n * sizeof(CUtensorMap), cudaMemcpyHostToDevice, stream));
+  RS_CUDA(cudaMemcpyAsync(p->d_map_ok, ok.data(), n * sizeof(int32_t), cudaMemcpyHostToDevice, stream));
   return RESHARD_OK;
 }
 
@@ -514,10 +769,29 @@ int ensure_items(reshard_plan_t *p, int set) {
   return rc;
 }
 
+int launch_transpose(reshard_plan_t *p, int set, cudaStream_t stream, const LaunchCaps &caps) {
+  const int n = (int)p->titems[set].size();
+  if (n == 0) return RESHARD_OK;
+  if (!p->d_titems[set]) {
+    TItem *d = nullptr;
+    int rc = upload(&d, p->titems[set]);
+    p->d_titems[set] = d;
+    if (rc) return rc;
+  }
+  const int grid = std::min(n, caps.transpose_grid);
+  reshard_transpose_kernel<<<grid, kTBlock, 0, stream>>>(
+      static_cast<const TItem *>(p->d_titems[set]), n, p->d_ptrs, p->d_grp_start, p->d_mem_ptr, p->d_mem_off,
+      static_cast<const CUtensorMap *>(p->d_maps), p->d_map_ok, p->d_status);
+  RS_CUDA(cudaGetLastError());
+  return RESHARD_OK;
+}
+
 int launch(reshard_plan_t *p, int set, bool quant, cudaStream_t stream, const LaunchCaps &caps) {
+  int rc = launch_transpose(p, set, stream, caps);
+  if (rc) return rc;
   const int n = (int)p->items[set].size();
   if (n == 0) return RESHARD_OK;
-  int rc = ensure_items(p, set);
+  rc = ensure_items(p, set);
   if (rc) return rc;
   const Item *items = static_cast<const Item *>(p->d_items[set]);
   if (quant) {
@@ -538,6 +812,16 @@ void free_device(reshard_plan_t *p) {
     if (d) cudaFree(d);
     d = nullptr;
   }
+  for (auto &d : p->d_titems) {
+    if (d) cudaFree(d);
+    d = nullptr;
+  }
+  if (p->d_maps) cudaFree(p->d_maps);
+  if (p->d_map_ok) cudaFree(p->d_map_ok);
+  if (p->d_status) cudaFree(p->d_status);
+  p->d_maps = nullptr;
+  p->d_map_ok = nullptr;
+  p->d_status = nullptr;
   if (p->d_grp_start) cudaFree(p->d_grp_start);
   if (p->d_mem_ptr) cudaFree(p->d_mem_ptr);
   if (p->d_mem_off) cudaFree(p->d_mem_off);
@@ -608,6 +892,7 @@ extern "C" int reshard_execute(reshard_plan_t *p, void *const *src_ptrs, void *c
   if (!p->ptr_cache_valid || p->ptr_cache != table) {
     // pageable source: the runtime stages the bytes before returning, so `table` may die
     RS_CUDA(cudaMemcpyAsync(p->d_ptrs, table.data(), table.size() * sizeof(uint64_t), cudaMemcpyHostToDevice, stream));
+    if ((rc = encode_maps(p, table, stream))) return rc;
     p->ptr_cache = std::move(table);
     p->ptr_cache_valid = true;
   }
@@ -615,6 +900,21 @@ extern "C" int reshard_execute(reshard_plan_t *p, void *const *src_ptrs, void *c
   if (mode == RESHARD_DIRECT) return launch(p, kDirect, q, stream, caps);
   if ((rc = launch(p, kPack, false, stream, caps))) return rc;
   return launch(p, kUnpack, q, stream, caps);
+}
+
+extern "C" int reshard_plan_status(reshard_plan_t *p, int32_t *status, int reset) {
+  if (!p || !status) return fail(RESHARD_ERR_INVALID_ARG, "plan or status is NULL");
+  *status = 0;
+  if (p->device < 0 || !p->d_status) return RESHARD_OK;
+  int cur = 0;
+  RS_CUDA(cudaGetDevice(&cur));
+  RS_CUDA(cudaSetDevice(p->device));
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(status, p->d_status, sizeof(int32_t), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && reset) e = cudaMemset(p->d_status, 0, sizeof(int32_t));
+  cudaSetDevice(cur);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the plan status");
+  return RESHARD_OK;
 }
 
 extern "C" int reshard_plan_destroy(reshard_plan_t *p) {
@@ -680,6 +980,8 @@ extern "C" int reshard_execute_static(const reshard_plan_t *p, void *const *src_
   if (p->regions.empty()) return RESHARD_OK;
   if ((p->n_src_ptrs && !src_ptrs) || (p->n_dst_ptrs && !dst_ptrs))
     return fail(RESHARD_ERR_INVALID_ARG, "src_ptrs or dst_ptrs is NULL");
+  if (!p->titems[kDirect].empty())
+    return fail(RESHARD_ERR_UNSUPPORTED, "plans with transposing regions need reshard_execute (TMA tensor maps)");
   for (const TensorInfo &t : p->tensors) {
     for (int side = 0; side < 2; ++side) {
       const int64_t n = side ? t.n_dst : t.n_src;

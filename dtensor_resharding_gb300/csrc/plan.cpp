@@ -177,8 +177,6 @@ void side_layout(const reshard_tensor_spec_t &s, bool src, TensorInfo &t, const 
           if (w.strides[d] < 0)
             v.add(RESHARD_ERR_INVALID_ARG, pre + side + " view " + std::to_string(p) + " has a negative stride");
         }
-        if (w.strides[s.ndim - 1] != 1)
-          v.add(RESHARD_ERR_UNSUPPORTED, pre + side + " view " + std::to_string(p) + ": innermost stride must be 1");
         // a stride equal to the dense one everywhere is still dense
         int64_t dd = 1;
         bool same = true;
@@ -248,7 +246,7 @@ void emit_items(int nd, const int64_t *ext, int64_t so, const int64_t *ss, int64
     }
   }
   // remaining outer dims [0, k] are walked explicitly
-  int64_t idx[kMaxDims] = {0, 0, 0, 0};
+  int64_t idx[kMaxDims + 1] = {0, 0, 0, 0, 0};
   const int64_t run_bytes = run * esize;
   for (;;) {
     int64_t s0 = so, d0 = dof;
@@ -292,6 +290,108 @@ void emit_items(int nd, const int64_t *ext, int64_t so, const int64_t *ss, int64
     }
     if (d < 0) break;
   }
+}
+
+// Side A (the reader) of a region, for the TMA slab of transposing items: the region origin
+// sits at coordinates a_lo[d] of a slab of extents a_ext[d] whose element (0, ..., 0) is at
+// element offset a_base of pointer a_ptr.
+struct ReadSide {
+  int32_t ptr;
+  int64_t base;
+  const int64_t *lo;
+  const int64_t *ext;
+};
+
+// Emit the work of one region between side A (offset so, strides sa) and side B (offset dof,
+// strides sb). When both sides are contiguous along the same dim (or neither has a contiguous
+// dim), the region is a strided copy: that dim becomes the run. When A is contiguous along one
+// dim and B along another, the region is a transpose and becomes transposing items.
+void emit_region(int nd, const int64_t *ext, int64_t so, const int64_t *sa, const ReadSide &ra, int64_t dof,
+                 const int64_t *sb, int32_t group, int esize, int64_t item_bytes, std::vector<Item> &out,
+                 std::vector<TItem> &tout, std::map<SlabSpec, int32_t> &slab_ids, std::vector<SlabSpec> &slabs) {
+  int ua = -1, ub = -1;
+  for (int d = 0; d < nd; ++d) {
+    if (ext[d] > 1 && sa[d] == 1) ua = d;
+    if (ext[d] > 1 && sb[d] == 1) ub = d;
+  }
+  if (ua >= 0 && ub >= 0 && ua != ub) {
+    const int R = ub, C = ua;
+    const int64_t tc = kTileRowBytes / esize;
+    const int64_t rows_per = (int64_t)kItemTiles * kTileRows, cols_per = kItemTiles * tc;
+    int outer[kMaxDims], no = 0;
+    for (int d = 0; d < nd; ++d)
+      if (d != R && d != C && ext[d] > 1) outer[no++] = d;
+    int64_t idx[kMaxDims] = {0, 0, 0, 0};
+    for (;;) {
+      int64_t sbase = so, dbase = dof, slab_base = ra.base;
+      for (int d = 0; d < nd; ++d) {
+        if (d == R || d == C) continue;
+        const int64_t o = ext[d] > 1 ? idx[d] : 0;
+        sbase += o * sa[d];
+        dbase += o * sb[d];
+        slab_base += (ra.lo[d] + o) * sa[d];
+      }
+      SlabSpec sl{ra.ptr, esize, slab_base, ra.ext[C], ra.ext[R], sa[R]};
+      auto f = slab_ids.find(sl);
+      int32_t sid;
+      if (f == slab_ids.end()) {
+        sid = (int32_t)slabs.size();
+        slab_ids[sl] = sid;
+        slabs.push_back(sl);
+      } else {
+        sid = f->second;
+      }
+      for (int64_t r0 = 0; r0 < ext[R]; r0 += rows_per)
+        for (int64_t c0 = 0; c0 < ext[C]; c0 += cols_per) {
+          TItem t{};
+          t.src_off = sbase + r0 * sa[R] + c0;
+          t.dst_off = dbase + c0 * sb[C] + r0;
+          t.src_pitch = sa[R];
+          t.dst_pitch = sb[C];
+          t.rows = (int32_t)std::min(rows_per, ext[R] - r0);
+          t.cols = (int32_t)std::min(cols_per, ext[C] - c0);
+          t.src = ra.ptr;
+          t.group = group;
+          t.esize = esize;
+          const int64_t x = ra.lo[C] + c0, y = ra.lo[R] + r0;
+          const bool fits = x < INT32_MAX && y < INT32_MAX && sl.cols < ((int64_t)1 << 32) && sl.rows < ((int64_t)1 << 32);
+          t.map = fits ? sid : -1;
+          t.x = fits ? (int32_t)x : 0;
+          t.y = fits ? (int32_t)y : 0;
+          tout.push_back(t);
+        }
+      int k = no - 1;
+      for (; k >= 0; --k) {
+        const int d = outer[k];
+        if (++idx[d] < ext[d]) break;
+        idx[d] = 0;
+      }
+      if (k < 0) break;
+    }
+    return;
+  }
+  // strided copy: the shared contiguous dim (or a virtual unit dim) goes last as the run
+  const int run_dim = (ua >= 0 && ua == ub) ? ua : -1;
+  int64_t pe[kMaxDims + 1], pa[kMaxDims + 1], pb[kMaxDims + 1];
+  int m = 0;
+  for (int d = 0; d < nd; ++d) {
+    if (d == run_dim) continue;
+    pe[m] = ext[d];
+    pa[m] = sa[d];
+    pb[m] = sb[d];
+    ++m;
+  }
+  if (run_dim >= 0) {
+    pe[m] = ext[run_dim];
+    pa[m] = 1;
+    pb[m] = 1;
+  } else {
+    pe[m] = 1;
+    pa[m] = 1;
+    pb[m] = 1;
+  }
+  ++m;
+  emit_items(m, pe, so, pa, dof, pb, ra.ptr, group, esize, item_bytes, out);
 }
 
 int build(const reshard_tensor_spec_t *specs, int n, reshard_plan_t **out) {
@@ -358,6 +458,11 @@ int build(const reshard_tensor_spec_t *specs, int n, reshard_plan_t **out) {
     const int nd = t.ndim;
     const std::string pre = "tensor " + std::to_string(ti) + ": ";
     if (t.dtype != RESHARD_BF16) quant_no(pre + "MXFP8 needs a BF16 tensor");
+    for (int64_t p = 0; p < t.n_src; ++p) {
+      const Box &b = t.src_box[(size_t)p];
+      if (volume(b, nd) > 0 && b.hi[nd - 1] - b.lo[nd - 1] > 1 && t.src_view[(size_t)p].strides[nd - 1] != 1)
+        quant_no(pre + "MXFP8 needs sources contiguous along the last dim");
+    }
     // source groups: identical boxes hold identical data; the lowest pointer index supplies
     std::map<BoxKey, int32_t> src_rep;
     for (int64_t p = 0; p < t.n_src; ++p) {
@@ -465,6 +570,7 @@ int build(const reshard_tensor_spec_t *specs, int n, reshard_plan_t **out) {
     plan_bytes += volume(r.box, plan->tensors[(size_t)r.tensor].ndim) * plan->tensors[(size_t)r.tensor].esize;
   int64_t item_bytes = kMaxItemBytes;
   while (item_bytes > kMinItemBytes && plan_bytes / item_bytes < kItemsPerPlan) item_bytes /= 2;
+  std::map<SlabSpec, int32_t> slab_ids;
   for (const Region &r : plan->regions) {
     const TensorInfo &t = plan->tensors[(size_t)r.tensor];
     const int nd = t.ndim;
@@ -486,10 +592,19 @@ int build(const reshard_tensor_spec_t *specs, int n, reshard_plan_t **out) {
     }
     const int32_t sp = (int32_t)(t.src_base + r.src);
     const int64_t mo = r.msg_off_bytes / t.esize;
-    emit_items(nd, ext, so, sv.strides, dof, dv.strides, sp, r.group, t.esize, item_bytes, plan->items[kDirect]);
-    emit_items(nd, ext, so, sv.strides, mo, ms, sp, plan->workspace_group, t.esize, item_bytes, plan->items[kPack]);
-    emit_items(nd, ext, mo, ms, dof, dv.strides, (int32_t)plan->workspace_ptr, r.group, t.esize, item_bytes,
-               plan->items[kUnpack]);
+    int64_t slo[kMaxDims], sext[kMaxDims], zero[kMaxDims] = {0, 0, 0, 0};
+    for (int d = 0; d < nd; ++d) {
+      slo[d] = r.box.lo[d] - sb.lo[d];
+      sext[d] = sb.hi[d] - sb.lo[d];
+    }
+    const ReadSide from_src{sp, sv.offset, slo, sext};
+    const ReadSide from_msg{(int32_t)plan->workspace_ptr, mo, zero, ext};
+    emit_region(nd, ext, so, sv.strides, from_src, dof, dv.strides, r.group, t.esize, item_bytes,
+                plan->items[kDirect], plan->titems[kDirect], slab_ids, plan->slabs);
+    emit_region(nd, ext, so, sv.strides, from_src, mo, ms, plan->workspace_group, t.esize, item_bytes,
+                plan->items[kPack], plan->titems[kPack], slab_ids, plan->slabs);
+    emit_region(nd, ext, mo, ms, from_msg, dof, dv.strides, r.group, t.esize, item_bytes, plan->items[kUnpack],
+                plan->titems[kUnpack], slab_ids, plan->slabs);
     const int64_t b = volume(r.box, nd) * t.esize;
     bytes_read += b;
     bytes_written += b * (int64_t)g.members.size();
@@ -503,7 +618,7 @@ int build(const reshard_tensor_spec_t *specs, int n, reshard_plan_t **out) {
   reshard_stats_t &st = plan->stats;
   st.n_tensors = n;
   st.regions = (int64_t)plan->regions.size();
-  st.items = (int64_t)plan->items[kDirect].size();
+  st.items = (int64_t)(plan->items[kDirect].size() + plan->titems[kDirect].size());
   st.dst_groups = (int64_t)plan->groups.size();
   st.messages = (int64_t)messages.size();
   st.bytes_read = bytes_read;
@@ -512,7 +627,7 @@ int build(const reshard_tensor_spec_t *specs, int n, reshard_plan_t **out) {
   st.message_bytes = msg_bytes;
   st.gather_bcast_bytes = 2 * global_bytes;
   st.global_bytes = global_bytes;
-  if (st.items > INT32_MAX || (int64_t)plan->mem_ptr.size() > INT32_MAX ||
+  if (st.items > INT32_MAX || (int64_t)plan->mem_ptr.size() > INT32_MAX || (int64_t)plan->slabs.size() > INT32_MAX ||
       pointer_table_size(plan) > INT32_MAX) {
     delete plan;
     return fail(RESHARD_ERR_UNSUPPORTED, "plan too large (more than 2^31 items, members or pointers)");
@@ -583,15 +698,33 @@ extern "C" int reshard_plan_items(const reshard_plan_t *plan, int set, int64_t c
                                   int32_t *group_start, int32_t *member_ptr, int64_t *member_off,
                                   int64_t *n_groups_out, int64_t *n_members_out) {
   if (!plan) return fail(RESHARD_ERR_INVALID_ARG, "plan is NULL");
-  if (set < 0 || set >= kNumSets) return fail(RESHARD_ERR_INVALID_ARG, "set must be 0, 1 or 2");
-  const auto &v = plan->items[set];
-  if (n_out) *n_out = (int64_t)v.size();
-  if (items && cap > 0) std::memcpy(items, v.data(), (size_t)std::min<int64_t>(cap, (int64_t)v.size()) * sizeof(Item));
+  if (set < 0 || set >= 2 * kNumSets) return fail(RESHARD_ERR_INVALID_ARG, "set must be in 0..5");
+  static_assert(sizeof(Item) == sizeof(TItem), "both item kinds are 64 bytes");
+  const size_t count = set < kNumSets ? plan->items[set].size() : plan->titems[set - kNumSets].size();
+  const void *data = set < kNumSets ? (const void *)plan->items[set].data() : (const void *)plan->titems[set - kNumSets].data();
+  if (n_out) *n_out = (int64_t)count;
+  if (items && cap > 0) std::memcpy(items, data, (size_t)std::min<int64_t>(cap, (int64_t)count) * sizeof(Item));
   if (n_groups_out) *n_groups_out = (int64_t)plan->grp_start.size() - 1;
   if (n_members_out) *n_members_out = (int64_t)plan->mem_ptr.size();
   if (group_start) std::memcpy(group_start, plan->grp_start.data(), plan->grp_start.size() * sizeof(int32_t));
   if (member_ptr) std::memcpy(member_ptr, plan->mem_ptr.data(), plan->mem_ptr.size() * sizeof(int32_t));
   if (member_off) std::memcpy(member_off, plan->mem_off.data(), plan->mem_off.size() * sizeof(int64_t));
+  return RESHARD_OK;
+}
+
+extern "C" int reshard_plan_slabs(const reshard_plan_t *plan, int64_t cap, int64_t *out, int64_t *n_out) {
+  if (!plan) return fail(RESHARD_ERR_INVALID_ARG, "plan is NULL");
+  if (n_out) *n_out = (int64_t)plan->slabs.size();
+  for (int64_t i = 0; i < std::min<int64_t>(cap, (int64_t)plan->slabs.size()); ++i) {
+    const SlabSpec &s = plan->slabs[(size_t)i];
+    int64_t *o = out + 6 * i;
+    o[0] = s.ptr;
+    o[1] = s.esize;
+    o[2] = s.base_off;
+    o[3] = s.cols;
+    o[4] = s.rows;
+    o[5] = s.pitch;
+  }
   return RESHARD_OK;
 }
 

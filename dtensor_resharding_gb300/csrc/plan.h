@@ -17,10 +17,10 @@ constexpr int kMaxDims = RESHARD_MAX_DIMS;
 // two in [kMinItemBytes, kMaxItemBytes] that still gives about kItemsPerPlan items per plan
 // (small plans get small items, so every SM has work).
 #ifndef RESHARD_ITEMS_PER_PLAN
-#define RESHARD_ITEMS_PER_PLAN 1024
+#define RESHARD_ITEMS_PER_PLAN 512
 #endif
 #ifndef RESHARD_MIN_ITEM_KIB
-#define RESHARD_MIN_ITEM_KIB 32
+#define RESHARD_MIN_ITEM_KIB 64
 #endif
 constexpr int64_t kMaxItemBytes = 256 * 1024;
 constexpr int64_t kMinItemBytes = RESHARD_MIN_ITEM_KIB * 1024;
@@ -58,6 +58,52 @@ struct alignas(16) Item {
 };
 static_assert(sizeof(Item) == 64, "work item is one 64-byte descriptor");
 
+// Transposing work item: the source is contiguous along the item's columns (C), the
+// destination along its rows (R). Element (r, c) is read at src_off + r * src_pitch + c of
+// pointer `src` and written at member_offset + dst_off + c * dst_pitch + r of every member of
+// `group`. `map` names the source slab (a 2-D tensor map encoded at execute time); (x, y) are
+// the item's (c0, r0) coordinates in that slab.
+struct alignas(16) TItem {
+  int64_t src_off;
+  int64_t dst_off;
+  int64_t src_pitch;
+  int64_t dst_pitch;
+  int32_t rows;
+  int32_t cols;
+  int32_t src;
+  int32_t group;
+  int32_t esize;
+  int32_t map;
+  int32_t x;
+  int32_t y;
+};
+static_assert(sizeof(TItem) == 64, "transposing item is one 64-byte descriptor");
+
+// A 2-D source slab read by TMA: element (y, x) at base_off + y * pitch + x (elements) of
+// pointer `ptr`, extents x < cols, y < rows.
+struct SlabSpec {
+  int32_t ptr;
+  int32_t esize;
+  int64_t base_off;
+  int64_t cols;
+  int64_t rows;
+  int64_t pitch;
+  bool operator<(const SlabSpec &o) const {
+    if (ptr != o.ptr) return ptr < o.ptr;
+    if (esize != o.esize) return esize < o.esize;
+    if (base_off != o.base_off) return base_off < o.base_off;
+    if (cols != o.cols) return cols < o.cols;
+    if (rows != o.rows) return rows < o.rows;
+    return pitch < o.pitch;
+  }
+};
+
+// Rows and bytes of one transpose tile (one 128-byte swizzle span per tile row).
+constexpr int kTileRows = 64;
+constexpr int kTileRowBytes = 128;
+// Tiles per transposing item along each dim.
+constexpr int kItemTiles = 4;
+
 struct TensorInfo {
   int ndim = 0;
   int64_t shape[kMaxDims] = {1, 1, 1, 1};
@@ -94,6 +140,8 @@ struct reshard_plan {
                                        // appended in the device tables
   int64_t n_src_ptrs = 0, n_dst_ptrs = 0;
   std::vector<reshard::Item> items[reshard::kNumSets];
+  std::vector<reshard::TItem> titems[reshard::kNumSets];  // transposing items of each pass
+  std::vector<reshard::SlabSpec> slabs;                    // TMA source slabs (all passes)
   // group table (device layout): members of group g are [grp_start[g], grp_start[g + 1])
   std::vector<int32_t> grp_start;
   std::vector<int32_t> mem_ptr;   // pointer-table index of each member's data pointer
@@ -108,6 +156,11 @@ struct reshard_plan {
   // device state (bound at the first execute)
   int device = -1;
   void *d_items[reshard::kNumSets] = {nullptr, nullptr, nullptr};
+  void *d_titems[reshard::kNumSets] = {nullptr, nullptr, nullptr};
+  void *d_maps = nullptr;      // one 128-byte CUtensorMap per slab (64-byte aligned)
+  int32_t *d_map_ok = nullptr; // 1 where the slab's map could be encoded
+  int32_t *d_status = nullptr; // device-side status word (bit 0: a TMA wait timed out)
+  std::vector<uint64_t> map_ptr_cache;  // pointers the maps were encoded for
   int32_t *d_grp_start = nullptr;
   int32_t *d_mem_ptr = nullptr;
   int64_t *d_mem_off = nullptr;

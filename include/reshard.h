@@ -93,10 +93,15 @@ typedef struct {
 
 /* Where a rank's local shard sits in its buffer ("DTensorRef" local tensor, or a slice of a
  * fused parameter such as gate_up: design doc, "Execution Flow: Setup Time").
- * The element at local index i is at buffer element offset_elems + sum_d i[d] * strides[d]. */
+ * The element at local index i is at buffer element offset_elems + sum_d i[d] * strides[d].
+ * Strides are any non-negative values that do not make elements alias. When the source and the
+ * destination of a region are contiguous along the same dim, the region is a strided copy;
+ * when they are contiguous along different dims (a transposed layout on one side, e.g. a
+ * destination that keeps W^T), the region goes through the TMA transposing kernel; with no
+ * contiguous dim at all it is copied element by element. */
 typedef struct {
   int64_t offset_elems;          /* >= 0 */
-  const int64_t *strides_elems;  /* ndim strides, innermost must be 1; NULL = dense row-major */
+  const int64_t *strides_elems;  /* ndim strides (>= 0); NULL = dense row-major */
   int64_t capacity_elems;        /* elements the buffer holds (bounds check); 0 = not checked */
 } reshard_view_t;
 
@@ -187,7 +192,8 @@ int reshard_execute(reshard_plan_t *plan, void *const *src_ptrs, void *const *ds
  * array and it keeps the last call's contents (nothing in it needs to start at zero): calls that
  * overlap on the GPU race, so serialise them (for example, all on one stream).
  * Arguments as in reshard_execute (one destination pointer per rank). The plan is only read and
- * is not bound to a device. Errors: INVALID_ARG (NULL plan or pointer of a non-empty shard);
+ * is not bound to a device; plans with transposing regions are UNSUPPORTED here (their tensor
+ * maps live with the plan). Errors: INVALID_ARG (NULL plan or pointer of a non-empty shard);
  * UNSUPPORTED when the tables need more than RESHARD_STATIC_SCRATCH_BYTES (the message gives the
  * size; split the batch or use reshard_execute); CUDA. Calls no cudaMalloc or cudaFree.
  */
@@ -215,19 +221,39 @@ int reshard_plan_group_members(const reshard_plan_t *plan, int64_t g, int64_t ca
                                int64_t *n_out);
 
 /*
- * reshard_plan_items -- copy the device work-item table of one pass (0 = direct, 1 = pack,
- * 2 = unpack) for inspection. Each item is 64 bytes: int64 src_off, dst_off, src_pitch,
- * dst_pitch (elements); int32 rows, run (elements per row), src (pointer-table index), group,
- * esize (bytes), 3 x int32 padding. Item i moves `rows` rows of `run` elements from
- * src_off + r * src_pitch of pointer `src` to member_offset + dst_off + r * dst_pitch of every
- * member pointer of `group`. Pointer table: [sources | destination data | destination scales |
- * packed workspace]. Up to cap items go to `items` (may be NULL); *n_out gets the count.
+ * reshard_plan_items -- copy a device work-item table for inspection. set 0/1/2: the strided
+ * copy items of the direct / pack / unpack pass; set 3/4/5: the transposing items of the same
+ * passes. Each item is 64 bytes.
+ * Copy item: int64 src_off, dst_off, src_pitch, dst_pitch (elements); int32 rows, run (elements
+ * per row), src (pointer-table index), group, esize (bytes), 3 x int32 padding. It moves `rows`
+ * rows of `run` elements from src_off + r * src_pitch of pointer `src` to
+ * member_offset + dst_off + r * dst_pitch of every member pointer of `group`.
+ * Transposing item: int64 src_off, dst_off, src_pitch, dst_pitch; int32 rows, cols, src, group,
+ * esize, slab, x, y. Element (r, c) moves from src_off + r * src_pitch + c to
+ * member_offset + dst_off + c * dst_pitch + r; (x, y) are (c = 0, r = 0) in slab coordinates.
+ * Pointer table: [sources | destination data | destination scales | packed workspace]. Up to
+ * cap items go to `items` (may be NULL); *n_out gets the count.
  * Groups: group_start (n_groups + 2 entries incl. the workspace group), member_ptr and
  * member_off (elements) are copied when non-NULL; *n_groups_out / *n_members_out get sizes.
  */
 int reshard_plan_items(const reshard_plan_t *plan, int set, int64_t cap, void *items, int64_t *n_out,
                        int32_t *group_start, int32_t *member_ptr, int64_t *member_off, int64_t *n_groups_out,
                        int64_t *n_members_out);
+
+/*
+ * reshard_plan_slabs -- the 2-D source slabs the transposing items read through TMA tensor maps
+ * (encoded at execute time for the current pointers). Per slab, 6 int64 at out[6 i]: pointer-
+ * table index, element size, element offset of (0, 0), columns (contiguous extent), rows, row
+ * pitch (elements). Up to cap slabs are written; *n_out gets the count.
+ */
+int reshard_plan_slabs(const reshard_plan_t *plan, int64_t cap, int64_t *out, int64_t *n_out);
+
+/*
+ * reshard_plan_status -- the plan's device status word (0 = fine; bit 0: a TMA wait in the
+ * transposing kernel gave up after its time limit and that launch's output is incomplete).
+ * Synchronizes the device, then reads the word; reset != 0 clears it. 0 before any execute.
+ */
+int reshard_plan_status(reshard_plan_t *plan, int32_t *status, int reset);
 
 /* reshard_plan_destroy -- free the plan's host tables, device tables and workspace.
  * Safe on NULL. The caller must make sure no enqueued execute of the plan is still running. */

@@ -276,6 +276,42 @@ def many_small(n: int = 10000, size_seed: int = 55, value_seed: int = 56, rows=(
     return _size_buffers(Workload(f"many_small_{n}_tp{tp_src}_to_dp{dp_dst}tp{tp_dst}", tensors), nsb, ndb)
 
 
+def _colmajor_views(global_shape, mesh, placements, start: int) -> List[View]:
+    """Views that store each local shard with its last two dims transposed (dim -2 contiguous)."""
+    out = []
+    for i, coord in enumerate(mesh_coords(mesh)):
+        shp = local_shape(global_shape, mesh, placements, coord)
+        nd = len(shp)
+        st = [0] * nd
+        st[-2] = 1
+        st[-1] = max(1, shp[-2])
+        acc = max(1, shp[-2]) * max(1, shp[-1])
+        for d in range(nd - 3, -1, -1):
+            st[d] = acc
+            acc *= max(1, shp[d])
+        out.append(View(start + i, 0, tuple(st)))
+    return out
+
+
+def transposed(shape=(14336, 4096), src_mesh=(8,), src_pl=("S0",), dst_mesh=(2, 2), dst_pl=("R", "S0"),
+               side: str = "dst", dtype: str = "bf16", seed: int = 6, std: float = 0.02, tensors: int = 1) -> Workload:
+    """Tensors whose local shards are stored with the last two dims transposed on one side
+    (``side="dst"``: the generation side keeps W^T; ``"src"``: the training side does; ``"both"``)."""
+    ts = []
+    nsb = ndb = 0
+    ns, nd = int(np.prod(src_mesh)), int(np.prod(dst_mesh))
+    for k in range(tensors):
+        sv = _colmajor_views(shape, src_mesh, src_pl, nsb) if side in ("src", "both") else _dense_views(ns, nsb)
+        dv = _colmajor_views(shape, dst_mesh, dst_pl, ndb) if side in ("dst", "both") else _dense_views(nd, ndb)
+        nsb += ns
+        ndb += nd
+        ts.append(TensorDesc(f"w{k}", tuple(shape), dtype, tuple(src_mesh), tuple(src_pl), tuple(dst_mesh),
+                             tuple(dst_pl), sv, dv, seed=seed * 1_000_003 + k, std=std))
+    name = (f"transpose_{'x'.join(map(str, shape))}_{'x'.join(map(str, src_mesh))}{''.join(src_pl)}_to_"
+            f"{'x'.join(map(str, dst_mesh))}{''.join(dst_pl)}_{side}_colmajor")
+    return _size_buffers(Workload(name, ts), nsb, ndb)
+
+
 def brute_force_cases(n_cases: int, seed: int = 7, max_mesh_dims: int = 3, max_mesh: int = 4,
                       max_tensor_dims: int = 3, max_len: int = 9, dtype: str = "i32") -> List[Workload]:
     """Random small problems: every placement kind, nested mesh dims, uneven and empty chunks.
@@ -320,6 +356,9 @@ WORKLOAD_NAMES = {
     "dense_ffn_4x14336x4096_tp8_to_dp2tp2": lambda: dense_ffn(layers=4),
     "dense_ffn_2x14336x4096_tp8_to_dp2tp2": lambda: dense_ffn(layers=2),
     "moe_1x32x1536x4096_ep16_to_tp4_mxfp8": lambda: moe_experts(layers=1, experts=32, dst="tp4"),
+    # a generation side that keeps every FFN weight transposed (local shards column-major)
+    "transpose_32x14336x4096_tp8_to_dp2tp2_dst_colmajor": lambda: transposed(tensors=32),
+    "transpose_2x14336x4096_tp8_to_dp2tp2_dst_colmajor": lambda: transposed(tensors=2),
     "moe_1x128x1536x4096_ep16_to_ep8": lambda: moe_experts(layers=1, dst="ep8"),
     "moe_1x128x1536x4096_ep16_to_tp4_mxfp8": lambda: moe_experts(layers=1, dst="tp4"),
 }

@@ -120,12 +120,19 @@ def test_view_capacity_overflow():
     assert "overflows its buffer" in str(e.value)
 
 
-def test_non_unit_inner_stride_unsupported():
-    d = S.TensorDesc("w", (8, 8), "bf16", (2,), ("S0",), (4,), ("S1",),
-                     [S.View(0, 0, (16, 2)), S.View(1)], [S.View(i) for i in range(4)])
+def test_negative_stride_rejected_and_transposed_view_planned():
+    bad = S.TensorDesc("w", (8, 8), "bf16", (2,), ("S0",), (4,), ("S1",),
+                       [S.View(0, 0, (8, -1)), S.View(1)], [S.View(i) for i in range(4)])
     with pytest.raises(R.ReshardError) as e:
-        R.reshard_plan_create(d)
-    assert e.value.code == R.RESHARD_ERR_UNSUPPORTED
+        R.reshard_plan_create(bad)
+    assert e.value.code == R.RESHARD_ERR_INVALID_ARG
+    wl = S.transposed(shape=(300, 200), src_mesh=(2,), src_pl=("S0",), dst_mesh=(2,), dst_pl=("S1",))
+    plan = R.plan_workload(wl)
+    t, *_ = R.reshard_plan_items(plan, 3)
+    assert len(t) > 0 and len(R.reshard_plan_items(plan, 0)[0]) == 0
+    slabs = R.reshard_plan_slabs(plan)
+    # direct: one slab per source shard; unpack: one per message region (2 x 2 regions)
+    assert len(set(t["slab"])) == 2 and len(slabs) == 6 and all(sl[1] == 2 for sl in slabs)
 
 
 def test_mesh_rank_permutation():

@@ -71,6 +71,40 @@ def check_bounds(wl, lay, plan, which, quant=False):
             assert (lo[sp] + e0 // 32 >= lo[sp]).all() and (c1 <= hi[sp]).all(), "scale write out of bounds"
 
 
+def check_transpose_bounds(wl, lay, plan, which):
+    """Transposing items: every element read and written stays in its buffer, and every item's
+    TMA slab coordinates name exactly the element its plain-load offset names, inside a slab that
+    lies inside the source buffer."""
+    items, gs, mp, mo = R.reshard_plan_items(plan, which + 3)
+    if len(items) == 0:
+        return
+    table = _ranges(wl, lay, plan)
+    lo = np.array([r[1] for r in table], np.int64)
+    hi = np.array([r[2] for r in table], np.int64)
+    es = items["esize"].astype(np.int64)
+    rows1 = items["rows"].astype(np.int64) - 1
+    cols1 = items["cols"].astype(np.int64) - 1
+    s0 = lo[items["src"]] + items["src_off"] * es
+    s1 = lo[items["src"]] + (items["src_off"] + rows1 * items["src_pitch"] + cols1 + 1) * es
+    assert (s0 >= lo[items["src"]]).all() and (s1 <= hi[items["src"]]).all(), "transpose read out of bounds"
+    counts = gs[items["group"] + 1] - gs[items["group"]]
+    for k in range(int(counts.max())):
+        sel = counts > k
+        m = gs[items["group"][sel]] + k
+        ptr, off, it = mp[m], mo[m], items[sel]
+        d0 = lo[ptr] + (off + it["dst_off"]) * es[sel]
+        d1 = lo[ptr] + (off + it["dst_off"] + cols1[sel] * it["dst_pitch"] + rows1[sel] + 1) * es[sel]
+        assert (d0 >= lo[ptr]).all() and (d1 <= hi[ptr]).all(), "transpose write out of bounds"
+    slabs = np.array(R.reshard_plan_slabs(plan), np.int64).reshape(-1, 6)
+    withmap = items[items["slab"] >= 0]
+    sl = slabs[withmap["slab"]]
+    assert (sl[:, 0] == withmap["src"]).all() and (sl[:, 1] == withmap["esize"]).all()
+    assert (sl[:, 2] + withmap["y"] * sl[:, 5] + withmap["x"] == withmap["src_off"]).all()
+    assert (withmap["x"] + withmap["cols"] <= sl[:, 3]).all() and (withmap["y"] + withmap["rows"] <= sl[:, 4]).all()
+    end = lo[sl[:, 0]] + (sl[:, 2] + (sl[:, 4] - 1) * sl[:, 5] + sl[:, 3]) * sl[:, 1]
+    assert (end <= hi[sl[:, 0]]).all(), "a TMA slab reaches past its buffer"
+
+
 def emulate(wl, lay, plan, mode):
     """Apply the item tables to host copies of the slabs (plain copies only)."""
     src = lay.src_slab.numpy()
@@ -79,7 +113,21 @@ def emulate(wl, lay, plan, mode):
     table = _ranges(wl, lay, plan)
     arrays = {"src": src, "dst": dst, "ws": ws}
 
+    def run_t(which):
+        items, gs, mp, mo = R.reshard_plan_items(plan, which + 3)
+        for it in items:
+            e = int(it["esize"])
+            kind, base, _ = table[it["src"]]
+            rr, cc = np.meshgrid(np.arange(int(it["rows"])), np.arange(int(it["cols"])), indexing="ij")
+            soff = base + (int(it["src_off"]) + rr * int(it["src_pitch"]) + cc) * e
+            vals = arrays[kind][(soff[..., None] + np.arange(e)).reshape(-1)]
+            for m in range(gs[it["group"]], gs[it["group"] + 1]):
+                dkind, dbase, _ = table[mp[m]]
+                doff = dbase + (int(mo[m]) + int(it["dst_off"]) + cc * int(it["dst_pitch"]) + rr) * e
+                arrays[dkind][(doff[..., None] + np.arange(e)).reshape(-1)] = vals
+
     def run(which):
+        run_t(which)
         items, gs, mp, mo = R.reshard_plan_items(plan, which)
         for it in items:
             e = int(it["esize"])
@@ -116,6 +164,7 @@ def test_item_tables_reproduce_oracle(name, mode):
     plan = R.plan_workload(wl)
     for which in (DIRECT, PACK, UNPACK):
         check_bounds(wl, lay, plan, which)
+        check_transpose_bounds(wl, lay, plan, which)
     assert np.array_equal(emulate(wl, lay, plan, mode), _oracle(wl, lay))
 
 
@@ -150,3 +199,4 @@ def test_full_size_item_bounds(name):
     plan = R.plan_workload(wl)
     for which in (DIRECT, PACK, UNPACK):
         check_bounds(wl, lay, plan, which, quant=wl.quant == "mxfp8")
+        check_transpose_bounds(wl, lay, plan, which)

@@ -31,6 +31,15 @@ SMALL = {
     "many_small": lambda: S.many_small(n=150),
     "long_run_f32": lambda: S.uneven_tp(rows=3000, cols=1000, src=3, dst=7, dtype="f32"),
     "u8_odd": lambda: S.mesh2d_to_1d(rows=77, cols=333, variant="2d", dtype="u8"),
+    "transpose_dst_bf16": lambda: S.transposed(shape=(300, 200), src_mesh=(4,), src_pl=("S0",)),
+    "transpose_dst_bf16_big_tiles": lambda: S.transposed(shape=(1100, 640), src_mesh=(2,), src_pl=("S1",),
+                                                         dst_mesh=(3,), dst_pl=("S0",)),
+    "transpose_src_f32": lambda: S.transposed(shape=(130, 257), src_mesh=(3,), src_pl=("S1",), dst_mesh=(2,),
+                                              dst_pl=("S0",), side="src", dtype="f32"),
+    "transpose_both_u8": lambda: S.transposed(shape=(77, 300), src_mesh=(2,), src_pl=("S0",), dst_mesh=(2, 2),
+                                              dst_pl=("S1", "R"), side="both", dtype="u8"),
+    "transpose_3d_i64": lambda: S.transposed(shape=(3, 70, 90), src_mesh=(3,), src_pl=("S0",), dst_mesh=(2,),
+                                             dst_pl=("S2",), dtype="i64"),
 }
 
 
@@ -56,6 +65,18 @@ def test_small_workloads_bit_exact(name, misalign, mode):
         pytest.skip("buffer offset must be a multiple of the element size")
     lay, plan = run_gpu(wl, mode=mode, misalign=misalign)
     assert_matches_oracle(wl, lay)
+
+
+@pytest.mark.parametrize("mode", ["direct", "packed"])
+def test_transposed_layouts_use_tma_and_report_no_timeouts(mode):
+    """Transposed shards go through the TMA kernel (aligned slabs) or its plain-load fallback
+    (unaligned buffers); both must match the oracle and leave the status word clear."""
+    for misalign in (0, 2):
+        wl = S.transposed(shape=(1100, 640), src_mesh=(2,), src_pl=("S1",), dst_mesh=(3,), dst_pl=("S0",))
+        lay, plan = run_gpu(wl, mode=mode, misalign=misalign)
+        assert_matches_oracle(wl, lay)
+        assert R.reshard_plan_status(plan) == 0
+        assert len(R.reshard_plan_items(plan, 3)[0]) > 0
 
 
 @pytest.mark.parametrize("mode", ["direct", "packed"])
@@ -187,3 +208,10 @@ def test_full_edge_mix_bit_exact():
 
 def test_full_many_small_sampled():
     _full(S.many_small, "direct", sampled_check, per_tensor=4)
+
+
+@pytest.mark.parametrize("mode", ["direct", "packed"])
+def test_full_transposed_destination_sampled(mode):
+    wl, lay, plan = _full(lambda: S.workload_by_name("transpose_32x14336x4096_tp8_to_dp2tp2_dst_colmajor"), mode,
+                          sampled_check, per_tensor=64)
+    assert R.reshard_plan_status(plan) == 0
