@@ -216,6 +216,26 @@ def reference_arm(args, rank: int) -> None:
 
 # --------------------------------------------------------------------------------- our arm
 
+def launches_per_execute(R, plan, mode: str) -> int:
+    """Kernel launches one execute enqueues: per pass, one copy launch and one transposing
+    launch when the pass has items of that kind."""
+    passes = (0,) if mode == "direct" else (1, 2)
+    return sum((len(R.reshard_plan_items(plan, p)[0]) > 0) + (len(R.reshard_plan_items(plan, p + 3)[0]) > 0)
+               for p in passes)
+
+
+def dominant_kernel(R, plan, mode: str, quant: str) -> str:
+    """The kernel that moves most of the bytes of the (last) pass."""
+    p = 0 if mode == "direct" else 2
+    copy_items = R.reshard_plan_items(plan, p)[0]
+    t_items = R.reshard_plan_items(plan, p + 3)[0]
+    copy_elems = int((copy_items["rows"].astype("int64") * copy_items["run"]).sum()) if len(copy_items) else 0
+    t_elems = int((t_items["rows"].astype("int64") * t_items["cols"]).sum()) if len(t_items) else 0
+    if t_elems > copy_elems:
+        return "reshard_transpose_kernel"
+    return "reshard_mxfp8_kernel" if quant == "mxfp8" else "reshard_copy_kernel"
+
+
 def e2e_run(R, plan, sp, dp, lay, args, quant, world, dev, dst_bytes, barrier):
     """End to end through the public call with host buffers: every step copies its sources in
     from pinned host memory, reshards, and copies its destinations back out. Three streams:
@@ -323,12 +343,12 @@ def our_arm(args, rank: int, world: int, local_rank: int) -> None:
 
     # roofline of the dominant kernel (direct: the one copy kernel per execute)
     peak, peak_kind = peaks()
+    launches = launches_per_execute(R, plan, args.mode)
     if args.mode == "direct":
         algo = st["bytes_read"] + (st["bytes_written"] if quant == "none" else dst_bytes)
-        kernel = "reshard_mxfp8_kernel" if quant == "mxfp8" else "reshard_copy_kernel"
     else:
         algo = (st["message_bytes"] + (st["bytes_written"] if quant == "none" else dst_bytes))  # unpack
-        kernel = "reshard_mxfp8_kernel" if quant == "mxfp8" else "reshard_copy_kernel"
+    kernel = dominant_kernel(R, plan, args.mode, quant)
     launch_ms = statistics.mean(per)
     achieved = algo / (launch_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
@@ -377,7 +397,7 @@ def our_arm(args, rank: int, world: int, local_rank: int) -> None:
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                        "plan_build_s": round(plan_s, 3)},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-            "gpu_launches": args.steps * (1 if args.mode == "direct" else 2),
+            "gpu_launches": args.steps * launches,
             "modes": modes,
         }
         print(json.dumps(line), flush=True)

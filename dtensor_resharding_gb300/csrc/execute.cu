@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(kQBlock, RESHARD_MXFP8_MIN_BLOCKS) reshard_mxf
 //
 // reshard_transpose_kernel moves regions whose source is contiguous along one dim (C) and whose
 // destination is contiguous along another (R): a transposed layout on one side. Tiles of
-// 64 rows (R) x 128 bytes (C) are staged in shared memory by TMA 2-D box loads
+// 128 rows (R) x 128 bytes (C) are staged in shared memory by TMA 2-D box loads
 // (cp.async.bulk.tensor, 128-byte swizzle, mbarrier completion, two stages in flight); each
 // thread then reads 32 bytes' worth of one column down the tile (conflict-free thanks to the
 // swizzle) and stores them as one contiguous 32-byte run of the destination. Where a slab's
@@ -458,7 +458,7 @@ __global__ void __launch_bounds__(kQBlock, RESHARD_MXFP8_MIN_BLOCKS) reshard_mxf
 
 constexpr int kTBlock = 256;                          // threads per CTA (one unit per tile per thread)
 constexpr int kTStages = 2;
-constexpr int kTileBytes = kTileRows * kTileRowBytes;  // 8 KiB
+constexpr int kTileBytes = kTileRows * kTileRowBytes;  // 16 KiB per stage
 constexpr unsigned long long kWaitLimitNs = 200ull * 1000 * 1000;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -487,14 +487,6 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, unsigned
 // Byte offset in a 128-byte-swizzled tile of (row, byte within the row).
 __device__ __forceinline__ int swz(int row, int byte) { return row * kTileRowBytes + ((((byte >> 4) ^ (row & 7))) << 4) + (byte & 15); }
 
-template <int ES>
-__device__ __forceinline__ void elem_store(uint8_t *p, const uint8_t *from) {
-  if constexpr (ES == 1) *p = *from;
-  if constexpr (ES == 2) *reinterpret_cast<uint16_t *>(p) = *reinterpret_cast<const uint16_t *>(from);
-  if constexpr (ES == 4) *reinterpret_cast<uint32_t *>(p) = *reinterpret_cast<const uint32_t *>(from);
-  if constexpr (ES == 8) *reinterpret_cast<uint64_t *>(p) = *reinterpret_cast<const uint64_t *>(from);
-}
-
 // Fill one tile with plain loads (same swizzled layout as TMA). Column x of the tile is slab
 // column x0 + x; only elements inside the item are read, the rest become zero.
 template <int ES>
@@ -517,30 +509,79 @@ __device__ __forceinline__ void tile_fill_plain(uint8_t *tile, const TItem &it, 
   }
 }
 
-// One tile to the destinations: thread = (column, 32-byte chunk of rows).
+__device__ __forceinline__ void store32(uint8_t *p, const uint32_t *w) {
+  asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
+// One tile to the destinations. A thread owns CPT adjacent columns (one 4-byte shared word per
+// row; 8 bytes for 8-byte elements) and RPC rows: 32 bytes of each column, which it writes as
+// one contiguous 32-byte run of the destination (one 256-bit store when aligned). Lanes of a warp
+// take consecutive column groups of one row chunk: with the 128-byte swizzle their shared reads
+// hit 32 different banks.
 template <int ES>
 __device__ __forceinline__ void tile_store(const uint8_t *tile, const TItem &it, uint8_t *const *dst, int nf, int x0,
                                            int y0) {
-  constexpr int TC = kTileRowBytes / ES;
-  constexpr int RPC = 32 / ES;  // rows per 32-byte chunk
-  const int col = threadIdx.x % TC, chunk = threadIdx.x / TC;
-  const int c = x0 + col - it.x;            // item column
-  const int r0 = y0 + chunk * RPC - it.y;   // item row of the chunk's first element
-  if (c < 0 || c >= it.cols || r0 >= it.rows) return;
-  alignas(16) uint8_t buf[32];
+  constexpr int TC = kTileRowBytes / ES;          // columns per tile
+  constexpr int CPT = ES >= 4 ? 1 : 4 / ES;       // columns per thread
+  constexpr int RPC = 32 / ES;                    // rows per thread (32 bytes per column)
+  constexpr int NG = TC / CPT;                    // column groups per tile
+  constexpr int UNITS = NG * (kTileRows / RPC);
+  for (int u = threadIdx.x; u < UNITS; u += kTBlock) {
+    const int g = u % NG, chunk = u / NG;
+    const int r0 = y0 + chunk * RPC - it.y;       // item row of the first element
+    const int c0 = x0 + g * CPT - it.x;           // item column of the first column
+    if (r0 >= it.rows || c0 + CPT <= 0 || c0 >= it.cols) continue;
+    uint32_t w[CPT][8];
 #pragma unroll
-  for (int k = 0; k < RPC; ++k) elem_store<ES>(buf + k * ES, tile + swz(chunk * RPC + k, col * ES));
-  const int nvalid = min(RPC, it.rows - r0);
-  const int64_t eoff = it.dst_off + (int64_t)c * it.dst_pitch + r0;
+    for (int k = 0; k < RPC; ++k) {
+      const int row = chunk * RPC + k;
+      if constexpr (ES == 8) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(tile + swz(row, g * 8));
+        w[0][2 * k] = v.x;
+        w[0][2 * k + 1] = v.y;
+      } else {
+        const uint32_t v = *reinterpret_cast<const uint32_t *>(tile + swz(row, g * 4));
 #pragma unroll
-  for (int f = 0; f < kMaxFan; ++f) {
-    if (f >= nf) break;
-    uint8_t *p = dst[f] + eoff * ES;
-    if (nvalid == RPC && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
-      store_stream(p, *reinterpret_cast<const uint4 *>(buf));
-      store_stream(p + 16, *reinterpret_cast<const uint4 *>(buf + 16));
-    } else {
-      for (int k = 0; k < nvalid; ++k) elem_store<ES>(p + k * ES, buf + k * ES);
+        for (int j = 0; j < CPT; ++j) {
+          if constexpr (ES == 4) {
+            w[j][k] = v;
+          } else if constexpr (ES == 2) {
+            const uint32_t h = (v >> (16 * j)) & 0xFFFFu;
+            w[j][k / 2] = (k & 1) ? (w[j][k / 2] | (h << 16)) : h;
+          } else {
+            const uint32_t b = (v >> (8 * j)) & 0xFFu;
+            w[j][k / 4] = (k & 3) ? (w[j][k / 4] | (b << (8 * (k & 3)))) : b;
+          }
+        }
+      }
+    }
+    const int nvalid = min(RPC, it.rows - r0);
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+      const int c = c0 + j;
+      if (c < 0 || c >= it.cols) continue;
+      const int64_t eoff = it.dst_off + (int64_t)c * it.dst_pitch + r0;
+#pragma unroll
+      for (int f = 0; f < kMaxFan; ++f) {
+        if (f >= nf) break;
+        uint8_t *p = dst[f] + eoff * ES;
+        const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+        if (nvalid == RPC && (a & 31) == 0) {
+          store32(p, w[j]);
+        } else if (nvalid == RPC && (a & 15) == 0) {
+          store_stream(p, make_uint4(w[j][0], w[j][1], w[j][2], w[j][3]));
+          store_stream(p + 16, make_uint4(w[j][4], w[j][5], w[j][6], w[j][7]));
+        } else {
+          const int nb = nvalid * ES;
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+#pragma unroll
+            for (int bb = 0; bb < 4; ++bb)
+              if (4 * q + bb < nb) p[4 * q + bb] = (uint8_t)(w[j][q] >> (8 * bb));
+        }
+      }
     }
   }
 }
@@ -601,7 +642,7 @@ __device__ void transpose_item(const TItem &it, const uint8_t *src, uint8_t *con
   }
 }
 
-__global__ void __launch_bounds__(kTBlock) reshard_transpose_kernel(
+__global__ void __launch_bounds__(kTBlock, 2) reshard_transpose_kernel(
     const TItem *__restrict__ items, int n_items, const uint64_t *__restrict__ ptrs, const int32_t *__restrict__ gstart,
     const int32_t *__restrict__ mptr, const int64_t *__restrict__ moff, const CUtensorMap *__restrict__ maps,
     const int32_t *__restrict__ map_ok, int32_t *status) {

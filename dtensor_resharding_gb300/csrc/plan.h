@@ -99,7 +99,7 @@ struct SlabSpec {
 };
 
 // Rows and bytes of one transpose tile (one 128-byte swizzle span per tile row).
-constexpr int kTileRows = 64;
+constexpr int kTileRows = 128;
 constexpr int kTileRowBytes = 128;
 // Tiles per transposing item along each dim.
 constexpr int kItemTiles = 4;
