@@ -182,7 +182,10 @@ __device__ __forceinline__ void copy_aligned32(const uint8_t *__restrict__ src, 
 // byte by byte at the two ends of a row. A source block is loaded only when it holds at least
 // one byte of the row, so no access leaves the 16-byte blocks (and hence the pages) the region
 // occupies.
-constexpr int kShiftUnroll = 4;
+#ifndef RESHARD_SHIFT_UNROLL
+#define RESHARD_SHIFT_UNROLL 4
+#endif
+constexpr int kShiftUnroll = RESHARD_SHIFT_UNROLL;
 
 __device__ __forceinline__ void copy_shifted(const uint8_t *__restrict__ src, uint8_t *const *dst, int nf, int rows,
                                              int64_t run_b, int64_t sp_b, int64_t dp_b) {

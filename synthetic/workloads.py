@@ -307,7 +307,7 @@ def transposed(shape=(14336, 4096), src_mesh=(8,), src_pl=("S0",), dst_mesh=(2, 
         ndb += nd
         ts.append(TensorDesc(f"w{k}", tuple(shape), dtype, tuple(src_mesh), tuple(src_pl), tuple(dst_mesh),
                              tuple(dst_pl), sv, dv, seed=seed * 1_000_003 + k, std=std))
-    name = (f"transpose_{'x'.join(map(str, shape))}_{'x'.join(map(str, src_mesh))}{''.join(src_pl)}_to_"
+    name = (f"transpose_{tensors}x{'x'.join(map(str, shape))}_{'x'.join(map(str, src_mesh))}{''.join(src_pl)}_to_"
             f"{'x'.join(map(str, dst_mesh))}{''.join(dst_pl)}_{side}_colmajor")
     return _size_buffers(Workload(name, ts), nsb, ndb)
 
