@@ -322,6 +322,9 @@ __device__ __forceinline__ uint32_t mag_max2(uint32_t w) { return max(w & 0x7FFF
 #ifndef RESHARD_MXFP8_ELEMS
 #define RESHARD_MXFP8_ELEMS 16
 #endif
+#ifndef RESHARD_MXFP8_WIDE
+#define RESHARD_MXFP8_WIDE 0
+#endif
 constexpr int kQBlock = RESHARD_MXFP8_BLOCK;    // threads per CTA
 constexpr int kQUnroll = RESHARD_MXFP8_UNROLL;  // lane slots in flight per thread
 constexpr int kQE = RESHARD_MXFP8_ELEMS;        // BF16 elements per lane slot (8 or 16)
@@ -371,6 +374,8 @@ __global__ void __launch_bounds__(kQBlock, RESHARD_MXFP8_MIN_BLOCKS) reshard_mxf
     const int total = it.rows * per_row;
     const int64_t sp_b = it.src_pitch * 2;
     const bool vec = ((reinterpret_cast<uintptr_t>(src) | (it.rows > 1 ? (uintptr_t)sp_b : 0)) & 15) == 0;
+    const bool vec32 = ((reinterpret_cast<uintptr_t>(src) | (it.rows > 1 ? (uintptr_t)sp_b : 0)) & 31) == 0;
+    (void)vec32;
     for (int f0 = 0; f0 < nrep; f0 += kQMaxFan) {
       const int nf = min(kQMaxFan, nrep - f0);
       uint8_t *dq[kQMaxFan];
@@ -404,8 +409,12 @@ __global__ void __launch_bounds__(kQBlock, RESHARD_MXFP8_MIN_BLOCKS) reshard_mxf
             const int o = j - r * per_row;
             const uint8_t *p = src + r * sp_b + 2 * kQE * (int64_t)o;
             eoff[u] = r * it.dst_pitch + kQE * (int64_t)o;
+            if (RESHARD_MXFP8_WIDE && kQV == 2 && vec32) {
+              load_stream32(p, v[u][0], v[u][kQV - 1]);
+            } else {
 #pragma unroll
-            for (int k = 0; k < kQV; ++k) v[u][k] = load_bf16x8(p + 16 * k, vec);
+              for (int k = 0; k < kQV; ++k) v[u][k] = load_bf16x8(p + 16 * k, vec);
+            }
           }
         }
 #pragma unroll

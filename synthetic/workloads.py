@@ -355,6 +355,7 @@ WORKLOAD_NAMES = {
     # reduced layer counts of the same shapes, for profiler captures (a few GB on the device)
     "dense_ffn_4x14336x4096_tp8_to_dp2tp2": lambda: dense_ffn(layers=4),
     "dense_ffn_2x14336x4096_tp8_to_dp2tp2": lambda: dense_ffn(layers=2),
+    "many_small_1000_tp4_to_dp2tp2": lambda: many_small(n=1000),
     "moe_1x32x1536x4096_ep16_to_tp4_mxfp8": lambda: moe_experts(layers=1, experts=32, dst="tp4"),
     # a generation side that keeps every FFN weight transposed (local shards column-major)
     "transpose_32x14336x4096_tp8_to_dp2tp2_dst_colmajor": lambda: transposed(tensors=32),
