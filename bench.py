@@ -217,15 +217,12 @@ def reference_arm(args, rank: int) -> None:
 # --------------------------------------------------------------------------------- our arm
 
 def launches_per_execute(R, plan, mode: str) -> int:
-    """Kernel launches one execute enqueues: per pass, one copy launch and one transposing
-    launch when the pass has items of that kind."""
-    passes = (0,) if mode == "direct" else (1, 2)
-    return sum((len(R.reshard_plan_items(plan, p)[0]) > 0) + (len(R.reshard_plan_items(plan, p + 3)[0]) > 0)
-               for p in passes)
+    """Kernel launches the last execute enqueued (the library counts them)."""
+    return R.reshard_plan_stats(plan)["last_launches"]
 
 
 def dominant_kernel(R, plan, mode: str, quant: str) -> str:
-    """The kernel that moves most of the bytes of the (last) pass."""
+    """The kernel that moves most of the bytes of the (last) pass of the last execute."""
     p = 0 if mode == "direct" else 2
     copy_items = R.reshard_plan_items(plan, p)[0]
     t_items = R.reshard_plan_items(plan, p + 3)[0]
@@ -233,7 +230,10 @@ def dominant_kernel(R, plan, mode: str, quant: str) -> str:
     t_elems = int((t_items["rows"].astype("int64") * t_items["cols"]).sum()) if len(t_items) else 0
     if t_elems > copy_elems:
         return "reshard_transpose_kernel"
-    return "reshard_mxfp8_kernel" if quant == "mxfp8" else "reshard_copy_kernel"
+    if quant == "mxfp8":
+        return "reshard_mxfp8_kernel"
+    st = R.reshard_plan_stats(plan)
+    return "reshard_copy_aligned_kernel" if st["last_aligned_items"] >= st["last_general_items"] else "reshard_copy_kernel"
 
 
 def e2e_run(R, plan, sp, dp, lay, args, quant, world, dev, dst_bytes, barrier):

@@ -39,8 +39,15 @@ namespace reshard {
 #ifndef RESHARD_MIN_BLOCKS
 #define RESHARD_MIN_BLOCKS 2
 #endif
+#ifndef RESHARD_GEN_MIN_BLOCKS
+#define RESHARD_GEN_MIN_BLOCKS 3
+#endif
+#ifndef RESHARD_GEN_UNROLL
+#define RESHARD_GEN_UNROLL 4
+#endif
 constexpr int kBlock = RESHARD_BLOCK;    // threads per CTA
-constexpr int kUnroll = RESHARD_UNROLL;  // 16-byte loads in flight per thread (aligned path)
+constexpr int kUnroll = RESHARD_UNROLL;        // 16-byte loads in flight per thread (aligned walker)
+constexpr int kGenUnroll = RESHARD_GEN_UNROLL;  // the same in the general walker's aligned path
 constexpr int kMaxFan = 8;               // destination replicas held in registers per pass
 
 // ------------------------------------------------------------------------------ helpers --
@@ -116,18 +123,42 @@ __device__ __forceinline__ uint32_t byte_of(uint4 v, int k) {
   return (w >> ((k & 3) * 8)) & 0xFF;
 }
 
+// Bytes [kmin, kmax) of the 16-byte word `o` into the 16-byte aligned `word`, each piece the
+// widest naturally aligned store that fits (at most 7 stores instead of up to 15 bytes).
+__device__ __forceinline__ void store_partial(uint8_t *word, uint4 o, int kmin, int kmax) {
+  int k = kmin;
+  while (k < kmax) {
+    const int left = kmax - k;
+    const uint32_t w = k < 4 ? o.x : k < 8 ? o.y : k < 12 ? o.z : o.w;
+    if ((k & 7) == 0 && left >= 8) {
+      *reinterpret_cast<uint2 *>(word + k) = k == 0 ? make_uint2(o.x, o.y) : make_uint2(o.z, o.w);
+      k += 8;
+    } else if ((k & 3) == 0 && left >= 4) {
+      *reinterpret_cast<uint32_t *>(word + k) = w;
+      k += 4;
+    } else if ((k & 1) == 0 && left >= 2) {
+      *reinterpret_cast<uint16_t *>(word + k) = (uint16_t)(w >> ((k & 2) * 8));
+      k += 2;
+    } else {
+      word[k] = (uint8_t)(w >> ((k & 3) * 8));
+      k += 1;
+    }
+  }
+}
+
 // ------------------------------------------------------------------- copy with fan-out --
 
 // Every source, destination, run and pitch 16-byte aligned: straight 16-byte copies.
+template <int U>
 __device__ __forceinline__ void copy_aligned(const uint8_t *__restrict__ src, uint8_t *const *dst, int nf, int rows,
                                              int64_t run_b, int64_t sp_b, int64_t dp_b) {
   const int nw = (int)(run_b >> 4);
   const int total = rows * nw;
-  for (int base = threadIdx.x; base < total; base += kBlock * kUnroll) {
-    uint4 v[kUnroll];
-    int64_t doff[kUnroll];
+  for (int base = threadIdx.x; base < total; base += kBlock * U) {
+    uint4 v[U];
+    int64_t doff[U];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int j = base + u * kBlock;
       if (j < total) {
         const int r = rows == 1 ? 0 : j / nw;
@@ -137,7 +168,7 @@ __device__ __forceinline__ void copy_aligned(const uint8_t *__restrict__ src, ui
       }
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
       if (base + u * kBlock < total) {
 #pragma unroll
         for (int f = 0; f < kMaxFan; ++f)
@@ -183,7 +214,7 @@ __device__ __forceinline__ void copy_aligned32(const uint8_t *__restrict__ src, 
 // one byte of the row, so no access leaves the 16-byte blocks (and hence the pages) the region
 // occupies.
 #ifndef RESHARD_SHIFT_UNROLL
-#define RESHARD_SHIFT_UNROLL 4
+#define RESHARD_SHIFT_UNROLL 2
 #endif
 constexpr int kShiftUnroll = RESHARD_SHIFT_UNROLL;
 
@@ -233,24 +264,22 @@ __device__ __forceinline__ void copy_shifted(const uint8_t *__restrict__ src, ui
           if (f < nf) store_stream(dst[f] + dpos[u], o);
       } else {
 #pragma unroll
-        for (int f = 0; f < kMaxFan; ++f) {
-          if (f < nf) {
-            uint8_t *word = dst[f] + dpos[u];
-            for (int k = kmin[u]; k < kmax[u]; ++k) word[k] = (uint8_t)byte_of(o, k);
-          }
-        }
+        for (int f = 0; f < kMaxFan; ++f)
+          if (f < nf) store_partial(dst[f] + dpos[u], o, kmin[u], kmax[u]);
       }
     }
   }
 }
 
-__global__ void __launch_bounds__(kBlock, RESHARD_MIN_BLOCKS) reshard_copy_kernel(const Item *__restrict__ items, int n_items,
-                                                              const uint64_t *__restrict__ ptrs,
-                                                              const int32_t *__restrict__ gstart,
-                                                              const int32_t *__restrict__ mptr,
-                                                              const int64_t *__restrict__ moff) {
-  for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
-    const Item it = items[i];
+// Resolve item k of a launch: items[idx[k]] when an index list is given, else items[k].
+__device__ __forceinline__ int item_index(const int32_t *idx, int k) { return idx ? idx[k] : k; }
+
+// The general walker: aligned, 32-byte-aligned and funnel-shift paths, any item.
+__global__ void __launch_bounds__(kBlock, RESHARD_GEN_MIN_BLOCKS) reshard_copy_kernel(
+    const Item *__restrict__ items, const int32_t *__restrict__ idx, int n_items, const uint64_t *__restrict__ ptrs,
+    const int32_t *__restrict__ gstart, const int32_t *__restrict__ mptr, const int64_t *__restrict__ moff) {
+  for (int k = blockIdx.x; k < n_items; k += gridDim.x) {
+    const Item it = items[item_index(idx, k)];
     const int64_t es = it.esize;
     const uint8_t *src = reinterpret_cast<const uint8_t *>(ptrs[it.src]) + it.src_off * es;
     const int g0 = gstart[it.group];
@@ -277,11 +306,50 @@ __global__ void __launch_bounds__(kBlock, RESHARD_MIN_BLOCKS) reshard_copy_kerne
       if (RESHARD_WIDE && (amask & 31) == 0) {
         copy_aligned32(src, dst, nf, it.rows, run_b, sp_b, dp_b);
       } else if ((amask & 15) == 0) {
-        copy_aligned(src, dst, nf, it.rows, run_b, sp_b, dp_b);
+        copy_aligned<kGenUnroll>(src, dst, nf, it.rows, run_b, sp_b, dp_b);
       } else if (same) {
         copy_shifted(src, dst, nf, it.rows, run_b, sp_b, dp_b);
       } else {
         for (int f = 0; f < nf; ++f) copy_shifted(src, dst + f, 1, it.rows, run_b, sp_b, dp_b);
+      }
+    }
+  }
+}
+
+// The aligned walker: items the host found 16-byte aligned everywhere (sources, every replica,
+// runs and pitches) for the current pointers; 16-byte copies only, more loads in flight. An
+// item that is not aligned after all is skipped and reported in bit 1 of the status word.
+__global__ void __launch_bounds__(kBlock, RESHARD_MIN_BLOCKS) reshard_copy_aligned_kernel(
+    const Item *__restrict__ items, const int32_t *__restrict__ idx, int n_items, const uint64_t *__restrict__ ptrs,
+    const int32_t *__restrict__ gstart, const int32_t *__restrict__ mptr, const int64_t *__restrict__ moff,
+    int32_t *status) {
+  for (int k = blockIdx.x; k < n_items; k += gridDim.x) {
+    const Item it = items[item_index(idx, k)];
+    const int64_t es = it.esize;
+    const uint8_t *src = reinterpret_cast<const uint8_t *>(ptrs[it.src]) + it.src_off * es;
+    const int g0 = gstart[it.group];
+    const int nrep = gstart[it.group + 1] - g0;
+    const int64_t run_b = (int64_t)it.run * es;
+    const int64_t sp_b = it.src_pitch * es, dp_b = it.dst_pitch * es;
+    const uintptr_t geo = reinterpret_cast<uintptr_t>(src) | (uintptr_t)run_b |
+                          (it.rows > 1 ? (uintptr_t)(sp_b | dp_b) : 0);
+    for (int f0 = 0; f0 < nrep; f0 += kMaxFan) {
+      const int nf = min(kMaxFan, nrep - f0);
+      uint8_t *dst[kMaxFan];
+      uintptr_t amask = geo;
+#pragma unroll
+      for (int f = 0; f < kMaxFan; ++f) {
+        dst[f] = nullptr;
+        if (f < nf) {
+          const int m = g0 + f0 + f;
+          dst[f] = reinterpret_cast<uint8_t *>(ptrs[mptr[m]]) + (moff[m] + it.dst_off) * es;
+          amask |= reinterpret_cast<uintptr_t>(dst[f]);
+        }
+      }
+      if ((amask & 15) == 0) {
+        copy_aligned<kUnroll>(src, dst, nf, it.rows, run_b, sp_b, dp_b);
+      } else if (threadIdx.x == 0) {
+        atomicOr(status, 2);
       }
     }
   }
@@ -323,7 +391,7 @@ __device__ __forceinline__ uint32_t mag_max2(uint32_t w) { return max(w & 0x7FFF
 #define RESHARD_MXFP8_ELEMS 16
 #endif
 #ifndef RESHARD_MXFP8_WIDE
-#define RESHARD_MXFP8_WIDE 0
+#define RESHARD_MXFP8_WIDE 1
 #endif
 constexpr int kQBlock = RESHARD_MXFP8_BLOCK;    // threads per CTA
 constexpr int kQUnroll = RESHARD_MXFP8_UNROLL;  // lane slots in flight per thread
@@ -717,6 +785,7 @@ int upload(T **dptr, const std::vector<T> &host) {
 
 struct LaunchCaps {
   int device = -1;
+  int aligned_grid = 0;
   int copy_grid = 0;
   int mxfp8_grid = 0;
   int transpose_grid = 0;
@@ -728,12 +797,14 @@ int launch_caps(int device, LaunchCaps &c) {
     c = g_caps;
     return RESHARD_OK;
   }
-  int sms = 0, b1 = 0, b2 = 0, b3 = 0;
+  int sms = 0, b0 = 0, b1 = 0, b2 = 0, b3 = 0;
   RS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device));
+  RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, reshard_copy_aligned_kernel, kBlock, 0));
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, reshard_copy_kernel, kBlock, 0));
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b2, reshard_mxfp8_kernel, kQBlock, 0));
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b3, reshard_transpose_kernel, kTBlock, 0));
   g_caps.device = device;
+  g_caps.aligned_grid = sms * std::max(1, b0);
   g_caps.copy_grid = sms * std::max(1, b1);
   g_caps.mxfp8_grid = sms * std::max(1, b2);
   g_caps.transpose_grid = sms * std::max(1, b3);
@@ -839,9 +910,44 @@ int launch_transpose(reshard_plan_t *p, int set, cudaStream_t stream, const Laun
   return RESHARD_OK;
 }
 
+// Split the copy items of `set` into those 16-byte aligned everywhere for the current pointers
+// (source, every replica, run, pitches) and the rest; upload the order on `stream`.
+int classify(reshard_plan_t *p, int set, cudaStream_t stream) {
+  if (p->d_cls_idx[set] && p->cls_version[set] == p->ptr_version) return RESHARD_OK;
+  const std::vector<Item> &items = p->items[set];
+  const std::vector<uint64_t> &tab = p->ptr_cache;
+  std::vector<int32_t> &idx = p->cls_idx[set];
+  idx.clear();
+  idx.reserve(items.size());
+  std::vector<int32_t> general;
+  for (size_t i = 0; i < items.size(); ++i) {
+    const Item &it = items[i];
+    const uint64_t es = (uint64_t)it.esize;
+    uint64_t m = tab[(size_t)it.src] + (uint64_t)it.src_off * es;
+    m |= (uint64_t)it.run * es;
+    if (it.rows > 1) m |= (uint64_t)it.src_pitch * es | (uint64_t)it.dst_pitch * es;
+    for (int32_t k = p->grp_start[(size_t)it.group]; k < p->grp_start[(size_t)it.group + 1]; ++k)
+      m |= tab[(size_t)p->mem_ptr[(size_t)k]] + (uint64_t)(p->mem_off[(size_t)k] + it.dst_off) * es;
+    if ((m & 15) == 0)
+      idx.push_back((int32_t)i);
+    else
+      general.push_back((int32_t)i);
+  }
+  p->n_aligned[set] = (int32_t)idx.size();
+  idx.insert(idx.end(), general.begin(), general.end());
+  if (!p->d_cls_idx[set] && !idx.empty())
+    RS_CUDA(cudaMalloc(reinterpret_cast<void **>(&p->d_cls_idx[set]), idx.size() * sizeof(int32_t)));
+  if (!idx.empty())
+    RS_CUDA(cudaMemcpyAsync(p->d_cls_idx[set], idx.data(), idx.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
+                            stream));
+  p->cls_version[set] = p->ptr_version;
+  return RESHARD_OK;
+}
+
 int launch(reshard_plan_t *p, int set, bool quant, cudaStream_t stream, const LaunchCaps &caps) {
   int rc = launch_transpose(p, set, stream, caps);
   if (rc) return rc;
+  if (!p->titems[set].empty()) ++p->last_launches;
   const int n = (int)p->items[set].size();
   if (n == 0) return RESHARD_OK;
   rc = ensure_items(p, set);
@@ -851,10 +957,23 @@ int launch(reshard_plan_t *p, int set, bool quant, cudaStream_t stream, const La
     const int grid = std::min(n, caps.mxfp8_grid);
     reshard_mxfp8_kernel<<<grid, kQBlock, 0, stream>>>(items, n, p->d_ptrs, p->d_grp_start, p->d_mem_ptr,
                                                       p->d_mem_off, p->n_dst_ptrs);
+    ++p->last_launches;
   } else {
-    const int grid = std::min(n, caps.copy_grid);
-    reshard_copy_kernel<<<grid, kBlock, 0, stream>>>(items, n, p->d_ptrs, p->d_grp_start, p->d_mem_ptr,
-                                                     p->d_mem_off);
+    if ((rc = classify(p, set, stream))) return rc;
+    const int na = p->n_aligned[set], ng = n - na;
+    const int32_t *idx = p->d_cls_idx[set];
+    p->last_aligned = na;
+    p->last_general = ng;
+    if (na > 0) {
+      reshard_copy_aligned_kernel<<<std::min(na, caps.aligned_grid), kBlock, 0, stream>>>(
+          items, idx, na, p->d_ptrs, p->d_grp_start, p->d_mem_ptr, p->d_mem_off, p->d_status);
+      ++p->last_launches;
+    }
+    if (ng > 0) {
+      reshard_copy_kernel<<<std::min(ng, caps.copy_grid), kBlock, 0, stream>>>(
+          items, idx + na, ng, p->d_ptrs, p->d_grp_start, p->d_mem_ptr, p->d_mem_off);
+      ++p->last_launches;
+    }
   }
   RS_CUDA(cudaGetLastError());
   return RESHARD_OK;
@@ -866,6 +985,10 @@ void free_device(reshard_plan_t *p) {
     d = nullptr;
   }
   for (auto &d : p->d_titems) {
+    if (d) cudaFree(d);
+    d = nullptr;
+  }
+  for (auto &d : p->d_cls_idx) {
     if (d) cudaFree(d);
     d = nullptr;
   }
@@ -947,9 +1070,11 @@ extern "C" int reshard_execute(reshard_plan_t *p, void *const *src_ptrs, void *c
     RS_CUDA(cudaMemcpyAsync(p->d_ptrs, table.data(), table.size() * sizeof(uint64_t), cudaMemcpyHostToDevice, stream));
     if ((rc = encode_maps(p, table, stream))) return rc;
     p->ptr_cache = std::move(table);
+    ++p->ptr_version;
     p->ptr_cache_valid = true;
   }
   const bool q = quant == RESHARD_QUANT_MXFP8;
+  p->last_launches = 0;
   if (mode == RESHARD_DIRECT) return launch(p, kDirect, q, stream, caps);
   if ((rc = launch(p, kPack, false, stream, caps))) return rc;
   return launch(p, kUnpack, q, stream, caps);
@@ -1084,7 +1209,7 @@ extern "C" int reshard_execute_static(const reshard_plan_t *p, void *const *src_
   const int n = (int)items.size();
   const int grid = std::min(n, caps.copy_grid);
   reshard_copy_kernel<<<grid, kBlock, 0, stream>>>(
-      reinterpret_cast<const Item *>(base), n, reinterpret_cast<const uint64_t *>(base + o_pt),
+      reinterpret_cast<const Item *>(base), nullptr, n, reinterpret_cast<const uint64_t *>(base + o_pt),
       reinterpret_cast<const int32_t *>(base + o_gs), reinterpret_cast<const int32_t *>(base + o_mp),
       reinterpret_cast<const int64_t *>(base + o_mo));
   RS_CUDA(cudaGetLastError());

@@ -662,6 +662,9 @@ extern "C" int reshard_plan_batch(const reshard_tensor_spec_t *specs, int n_tens
 extern "C" int reshard_plan_stats(const reshard_plan_t *plan, reshard_stats_t *out) {
   if (!plan || !out) return fail(RESHARD_ERR_INVALID_ARG, "plan or out is NULL");
   *out = plan->stats;
+  out->last_launches = plan->last_launches;
+  out->last_aligned_items = plan->last_aligned;
+  out->last_general_items = plan->last_general;
   return RESHARD_OK;
 }
 

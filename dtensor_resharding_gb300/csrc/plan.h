@@ -161,6 +161,16 @@ struct reshard_plan {
   int32_t *d_map_ok = nullptr; // 1 where the slab's map could be encoded
   int32_t *d_status = nullptr; // device-side status word (bit 0: a TMA wait timed out)
   std::vector<uint64_t> map_ptr_cache;  // pointers the maps were encoded for
+  // copy items split by alignment for the current pointers: cls_idx[set] lists the items that
+  // are 16-byte aligned everywhere first (n_aligned of them), then the rest
+  std::vector<int32_t> cls_idx[reshard::kNumSets];
+  int32_t n_aligned[reshard::kNumSets] = {0, 0, 0};
+  int32_t *d_cls_idx[reshard::kNumSets] = {nullptr, nullptr, nullptr};
+  uint64_t cls_version[reshard::kNumSets] = {0, 0, 0};
+  uint64_t ptr_version = 0;  // bumped whenever the pointer table changes
+  int64_t last_launches = 0; // kernel launches enqueued by the last execute
+  int64_t last_aligned = 0;  // copy items of the last pass that took the aligned walker
+  int64_t last_general = 0;  // ... and the general walker
   int32_t *d_grp_start = nullptr;
   int32_t *d_mem_ptr = nullptr;
   int64_t *d_mem_off = nullptr;

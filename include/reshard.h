@@ -134,6 +134,9 @@ typedef struct {
   int64_t message_bytes;      /* packed-mode workspace: messages with 16-byte aligned regions */
   int64_t gather_bcast_bytes; /* all-gather + broadcast payload for comparison: 2 x tensor bytes */
   int64_t global_bytes;       /* sum of global tensor bytes */
+  int64_t last_launches;      /* kernel launches enqueued by the plan's last execute */
+  int64_t last_aligned_items; /* copy items of its last pass run by the aligned walker ... */
+  int64_t last_general_items; /* ... and by the general (unaligned-capable) walker */
 } reshard_stats_t;
 
 /*
