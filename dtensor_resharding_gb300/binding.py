@@ -28,7 +28,8 @@ RESHARD_MAX_DIMS = 4
 DTYPE_CODES = {"u8": 0, "bf16": 1, "f16": 2, "f32": 3, "i32": 4, "i64": 5}
 MODES = {"direct": RESHARD_DIRECT, "packed": RESHARD_PACKED}
 QUANTS = {"none": RESHARD_QUANT_NONE, "mxfp8": RESHARD_QUANT_MXFP8}
-EXPORTED = ("reshard_plan_create", "reshard_plan_batch", "reshard_execute", "reshard_execute_static",
+EXPORTED = ("reshard_plan_create", "reshard_plan_batch", "reshard_plan_blockwise_fp8", "reshard_execute",
+            "reshard_execute_static",
             "reshard_plan_stats",
             "reshard_plan_regions", "reshard_plan_group_members", "reshard_plan_items", "reshard_plan_slabs",
             "reshard_plan_status", "reshard_plan_destroy", "reshard_last_error")
@@ -77,6 +78,8 @@ def _load(path: str = LIB_PATH):
     vp = ctypes.c_void_p
     lib.reshard_plan_create.argtypes = [ctypes.POINTER(TensorSpecT), ctypes.POINTER(vp)]
     lib.reshard_plan_batch.argtypes = [ctypes.POINTER(TensorSpecT), ctypes.c_int, ctypes.POINTER(vp)]
+    lib.reshard_plan_blockwise_fp8.argtypes = [ctypes.POINTER(TensorSpecT), ctypes.c_int, ctypes.c_int64,
+                                               ctypes.c_int64, ctypes.POINTER(vp)]
     lib.reshard_execute.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.c_int, ctypes.c_int, vp]
     lib.reshard_execute_static.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp]
     lib.reshard_plan_stats.argtypes = [vp, ctypes.POINTER(StatsT)]
@@ -212,6 +215,19 @@ def reshard_plan_batch(descs: Sequence[Any], src_capacity=None, dst_capacity=Non
     h = ctypes.c_void_p()
     _check(LIB.reshard_plan_batch(arr, len(descs), ctypes.byref(h)))
     return Plan(h.value, sum(_n_ranks(d.src_mesh) for d in descs), sum(_n_ranks(d.dst_mesh) for d in descs))
+
+
+def reshard_plan_blockwise_fp8(descs: Sequence[Any], block=(128, 128), src_capacity=None, dst_capacity=None) -> Plan:
+    """FP8 weights (u8) plus their derived blockwise fp32 scales in one plan: weights first,
+    then scales, in the pointer arrays too. Capacities (optional) cover the weights only."""
+    keep: list = []
+    arr = (TensorSpecT * max(1, len(descs)))()
+    for i, d in enumerate(descs):
+        arr[i] = make_spec(d, src_capacity[i] if src_capacity else None,
+                           dst_capacity[i] if dst_capacity else None, keep)
+    h = ctypes.c_void_p()
+    _check(LIB.reshard_plan_blockwise_fp8(arr, len(descs), int(block[0]), int(block[1]), ctypes.byref(h)))
+    return Plan(h.value, 2 * sum(_n_ranks(d.src_mesh) for d in descs), 2 * sum(_n_ranks(d.dst_mesh) for d in descs))
 
 
 def pointer_array(ptrs: Sequence[int]):

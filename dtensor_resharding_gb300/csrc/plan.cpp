@@ -659,6 +659,74 @@ extern "C" int reshard_plan_batch(const reshard_tensor_spec_t *specs, int n_tens
   }
 }
 
+extern "C" int reshard_plan_blockwise_fp8(const reshard_tensor_spec_t *specs, int n, int64_t block_rows,
+                                          int64_t block_cols, reshard_plan_t **out) {
+  if (!out) return fail(RESHARD_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (n < 0 || (n > 0 && !specs)) return fail(RESHARD_ERR_INVALID_ARG, "specs is NULL or n_tensors < 0");
+  if (block_rows < 1 || block_cols < 1) return fail(RESHARD_ERR_INVALID_ARG, "block sizes must be >= 1");
+  try {
+    Violations v;
+    std::vector<reshard_tensor_spec_t> all(specs, specs + n);
+    std::vector<std::vector<int64_t>> shapes((size_t)n);
+    for (int i = 0; i < n; ++i) {
+      const reshard_tensor_spec_t &d = specs[i];
+      const std::string pre = "tensor " + std::to_string(i) + ": ";
+      if (d.dtype != RESHARD_U8) v.add(RESHARD_ERR_INVALID_ARG, pre + "blockwise FP8 weights are RESHARD_U8");
+      if (d.ndim < 2 || d.ndim > kMaxDims || !d.global_shape) {
+        v.add(RESHARD_ERR_INVALID_ARG, pre + "blockwise FP8 weights need 2..4 dims");
+        continue;
+      }
+      shapes[(size_t)i].assign(d.global_shape, d.global_shape + d.ndim);
+      auto &sh = shapes[(size_t)i];
+      sh[(size_t)d.ndim - 2] = (sh[(size_t)d.ndim - 2] + block_rows - 1) / block_rows;
+      sh[(size_t)d.ndim - 1] = (sh[(size_t)d.ndim - 1] + block_cols - 1) / block_cols;
+    }
+    if (!v.lines.empty()) return v.report();
+    for (int i = 0; i < n; ++i) {
+      reshard_tensor_spec_t sc = specs[i];
+      sc.global_shape = shapes[(size_t)i].data();
+      sc.dtype = RESHARD_F32;
+      sc.src_views = nullptr;
+      sc.dst_views = nullptr;
+      all.push_back(sc);
+    }
+    // every weight shard boundary on a block boundary, and every scale shard = its blocks
+    for (int i = 0; i < n; ++i) {
+      const reshard_tensor_spec_t &d = specs[i];
+      const reshard_tensor_spec_t &sc = all[(size_t)(n + i)];
+      for (int side = 0; side < 2; ++side) {
+        const reshard_mesh_t &m = side ? d.dst_mesh : d.src_mesh;
+        const reshard_placement_t *pl = side ? d.dst_pl : d.src_pl;
+        if (m.ndim < 1 || m.ndim > RESHARD_MAX_MESH_DIMS || !m.shape || !pl) continue;  // reported by build
+        int64_t nr = 1;
+        for (int k = 0; k < m.ndim; ++k) nr *= std::max<int64_t>(1, m.shape[k]);
+        for (int64_t pos = 0; pos < nr; ++pos) {
+          const Box db = rank_box(d, m, pl, pos), sb = rank_box(sc, m, pl, pos);
+          for (int k = 0; k < 2; ++k) {
+            const int dim = d.ndim - 2 + k;
+            const int64_t bs = k ? block_cols : block_rows, L = d.global_shape[dim];
+            const bool lo_ok = db.lo[dim] % bs == 0 && sb.lo[dim] == db.lo[dim] / bs;
+            const bool hi_ok = (db.hi[dim] % bs == 0 || db.hi[dim] == L) && sb.hi[dim] == (db.hi[dim] + bs - 1) / bs;
+            const bool empty = db.hi[dim] == db.lo[dim] && sb.hi[dim] == sb.lo[dim];
+            if (!empty && !(lo_ok && hi_ok)) {
+              v.add(RESHARD_ERR_UNSUPPORTED, "tensor " + std::to_string(i) + ": " + (side ? "destination" : "source") +
+                                                 " rank " + std::to_string(pos) + " splits dim " + std::to_string(dim) +
+                                                 " off the " + std::to_string(bs) + "-element block grid");
+              pos = nr;  // one line per tensor side
+              break;
+            }
+          }
+        }
+      }
+    }
+    if (!v.lines.empty()) return v.report();
+    return build(all.data(), (int)all.size(), out);
+  } catch (const std::bad_alloc &) {
+    return fail(RESHARD_ERR_OOM, "host allocation failed while planning");
+  }
+}
+
 extern "C" int reshard_plan_stats(const reshard_plan_t *plan, reshard_stats_t *out) {
   if (!plan || !out) return fail(RESHARD_ERR_INVALID_ARG, "plan or out is NULL");
   *out = plan->stats;

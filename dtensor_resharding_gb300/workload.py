@@ -7,13 +7,18 @@ pointers through ``src_ptrs(wl, t)`` / ``dst_ptrs(wl, t)``.
 """
 from __future__ import annotations
 
-from .binding import Plan, pointer_array, reshard_plan_batch
+from .binding import Plan, pointer_array, reshard_plan_batch, reshard_plan_blockwise_fp8
 
 
 def plan_workload(wl) -> Plan:
     """One batched plan over every tensor of the workload (view capacities bound-checked)."""
     src_cap = [[wl.src_buffer_numel[v.buffer] for v in t.src_views] for t in wl.tensors]
     dst_cap = [[wl.dst_buffer_numel[v.buffer] for v in t.dst_views] for t in wl.tensors]
+    block = getattr(wl, "block", None)
+    if block:
+        # blockwise FP8: the first half of the tensors are the weights, the second their scales
+        n = len(wl.tensors) // 2
+        return reshard_plan_blockwise_fp8(wl.tensors[:n], block, src_cap[:n], dst_cap[:n])
     return reshard_plan_batch(wl.tensors, src_cap, dst_cap)
 
 

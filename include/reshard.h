@@ -158,6 +158,21 @@ int reshard_plan_create(const reshard_tensor_spec_t *spec, reshard_plan_t **out)
 int reshard_plan_batch(const reshard_tensor_spec_t *specs, int n_tensors, reshard_plan_t **out);
 
 /*
+ * reshard_plan_blockwise_fp8 -- plan FP8 weights together with their blockwise scales, the
+ * blockwise-FP8 train <-> FP8 gen path of the design doc ("Enabling It"; the FP8 "_scale_inv"
+ * siblings of "Design Overview"). specs: n_tensors FP8 weights (dtype RESHARD_U8, ndim >= 2).
+ * For each, a scale tensor is derived: global shape with the last two dims ceil-divided by
+ * block_rows / block_cols, dtype RESHARD_F32, the same meshes and placements, dense views.
+ * The plan is a batch of 2 n_tensors tensors: the weights in spec order, then their scales in
+ * the same order; pointer arrays follow that order (weights' pointers, then scales').
+ * Every shard boundary of a weight along the two blocked dims must fall on a block boundary
+ * (or at the tensor's end) on both sides, so that each scale shard is exactly the blocks of
+ * its weight shard; otherwise UNSUPPORTED, listing the offending tensors and dims.
+ */
+int reshard_plan_blockwise_fp8(const reshard_tensor_spec_t *specs, int n_tensors, int64_t block_rows,
+                               int64_t block_cols, reshard_plan_t **out);
+
+/*
  * reshard_execute -- enqueue the reshard on `stream` and return (asynchronous).
  * src_ptrs / dst_ptrs: HOST arrays of DEVICE pointers, caller-owned, laid out as above. A rank
  *   whose shard is empty may pass NULL. Under RESHARD_QUANT_MXFP8 dst_ptrs holds two entries

@@ -79,6 +79,7 @@ class Workload:
     src_buffer_dtype: List[str] = field(default_factory=list)
     dst_buffer_numel: List[int] = field(default_factory=list)
     dst_buffer_dtype: List[str] = field(default_factory=list)
+    block: Optional[Tuple[int, int]] = None  # blockwise FP8: tensors = weights, then their scales
 
     def src_bytes(self) -> int:
         return sum(n * DTYPES[d][1] for n, d in zip(self.src_buffer_numel, self.src_buffer_dtype) if n)
@@ -312,6 +313,121 @@ def transposed(shape=(14336, 4096), src_mesh=(8,), src_pl=("S0",), dst_mesh=(2, 
     return _size_buffers(Workload(name, ts), nsb, ndb)
 
 
+def qkv_kv_below_tp(layers: int = 4, q_heads: int = 64, kv_heads: int = 2, head_dim: int = 128,
+                    hidden: int = 8192, tp_src: int = 8, tp_dst: int = 8, seed: int = 8, std: float = 0.02) -> Workload:
+    """Fused QKV projections with fewer KV heads than TP ranks, on both sides.
+
+    Each rank's fused buffer holds [q rows; k rows; v rows] of its heads. Q rows are Shard(0)
+    over TP. With KV heads below TP, K and V are split over KV groups of TP ranks and replicated
+    inside a group, i.e. a (kv, tp / kv) mesh with [Shard(0), Replicate] in the same rank order
+    (the ModelExpress reshard PR: "Nemotron-style layers can have fewer KV heads than TP ranks").
+    """
+    tensors: List[TensorDesc] = []
+    nsb = ndb = 0
+
+    def side(tp):
+        if kv_heads >= tp:
+            return (tp,), ("S0",)
+        return (kv_heads, tp // kv_heads), ("S0", "R")
+
+    for layer in range(layers):
+        s = seed * 1_000_003 + layer * 3
+        ql_src, ql_dst = q_heads // tp_src * head_dim, q_heads // tp_dst * head_dim
+        kvl_src = max(1, kv_heads // tp_src) * head_dim
+        kvl_dst = max(1, kv_heads // tp_dst) * head_dim
+        fs = list(range(nsb, nsb + tp_src)); nsb += tp_src
+        fd = list(range(ndb, ndb + tp_dst)); ndb += tp_dst
+        kvm_s, kvp_s = side(tp_src)
+        kvm_d, kvp_d = side(tp_dst)
+        for j, (nm, rows, off_s, off_d, ms, ps, md, pd) in enumerate((
+                ("q_proj", q_heads * head_dim, 0, 0, (tp_src,), ("S0",), (tp_dst,), ("S0",)),
+                ("k_proj", kv_heads * head_dim, ql_src, ql_dst, kvm_s, kvp_s, kvm_d, kvp_d),
+                ("v_proj", kv_heads * head_dim, ql_src + kvl_src, ql_dst + kvl_dst, kvm_s, kvp_s, kvm_d, kvp_d))):
+            sv = [View(fs[r], off_s * hidden) for r in range(tp_src)]
+            dv = [View(fd[r], off_d * hidden) for r in range(tp_dst)]
+            tensors.append(TensorDesc(f"layers.{layer}.self_attn.{nm}.weight", (rows, hidden), "bf16",
+                                      ms, ps, md, pd, sv, dv, s + j, std))
+    name = f"qkv_{layers}x{q_heads}q{kv_heads}kv{head_dim}x{hidden}_tp{tp_src}_to_tp{tp_dst}"
+    return _size_buffers(Workload(name, tensors), nsb, ndb)
+
+
+def moe_w13(layers: int = 2, experts: int = 64, hidden: int = 2048, ffn: int = 768, ep_src: int = 8,
+            tp_dst: int = 4, per_expert_src: bool = True, seed: int = 9, std: float = 0.02) -> Workload:
+    """MoE experts into vLLM's fused layout: per rank w13 [E, 2 I_local, H] (gate rows then up
+    rows of each expert) and w2 [E, H, I_local], TP over the expert FFN dim.
+
+    ``per_expert_src``: the training side keeps every expert's gate/up/down in its own
+    allocation (no stacking copy): each expert is its own tensor [1, ...] whose source mesh is
+    the single rank that owns it, and whose destination views point into the fused buffers.
+    Otherwise the source is the grouped [E, ...] tensor over EP (stacked).
+    """
+    tensors: List[TensorDesc] = []
+    nsb = ndb = 0
+    il = ffn // tp_dst
+    for layer in range(layers):
+        s = seed * 1_000_003 + layer * 1000
+        w13 = list(range(ndb, ndb + tp_dst)); ndb += tp_dst
+        w2 = list(range(ndb, ndb + tp_dst)); ndb += tp_dst
+        st13 = (2 * il * hidden, hidden, 1)
+        if per_expert_src:
+            for e in range(experts):
+                for j, (nm, shape) in enumerate((("gate_proj", (1, ffn, hidden)), ("up_proj", (1, ffn, hidden)),
+                                                 ("down_proj", (1, hidden, ffn)))):
+                    sv = [View(nsb)]; nsb += 1
+                    if nm == "down_proj":
+                        dv = [View(w2[r], e * hidden * il) for r in range(tp_dst)]
+                        dpl = ("S2",)
+                    else:
+                        base = e * 2 * il * hidden + (il * hidden if nm == "up_proj" else 0)
+                        dv = [View(w13[r], base, st13) for r in range(tp_dst)]
+                        dpl = ("S1",)
+                    tensors.append(TensorDesc(f"layers.{layer}.mlp.experts.{e}.{nm}.weight", shape, "bf16",
+                                              (1,), ("R",), (tp_dst,), dpl, sv, dv, s + 3 * e + j, std))
+        else:
+            for j, (nm, shape) in enumerate((("gate_proj", (experts, ffn, hidden)), ("up_proj", (experts, ffn, hidden)),
+                                             ("down_proj", (experts, hidden, ffn)))):
+                sv = _dense_views(ep_src, nsb); nsb += ep_src
+                if nm == "down_proj":
+                    dv = [View(w2[r]) for r in range(tp_dst)]
+                    dpl = ("S2",)
+                else:
+                    dv = [View(w13[r], il * hidden if nm == "up_proj" else 0, st13) for r in range(tp_dst)]
+                    dpl = ("S1",)
+                tensors.append(TensorDesc(f"layers.{layer}.mlp.experts.{nm}.weight", shape, "bf16",
+                                          (ep_src,), ("S0",), (tp_dst,), dpl, sv, dv, s + j, std))
+    src = "per_expert" if per_expert_src else f"ep{ep_src}"
+    name = f"moe_w13_{layers}x{experts}x{ffn}x{hidden}_{src}_to_tp{tp_dst}"
+    return _size_buffers(Workload(name, tensors), nsb, ndb)
+
+
+def moe_fp8_blockwise(layers: int = 8, experts: int = 128, hidden: int = 2048, ffn: int = 768, ep_src: int = 8,
+                      dp_src: int = 2, tp_dst: int = 2, dp_dst: int = 8, block=(128, 128), seed: int = 10) -> Workload:
+    """Blockwise-FP8 MoE experts with their fp32 scales (one per block of the last two dims).
+
+    Training side (DP, EP) [Replicate, Shard(0)]; generation side (DP, TP) [Replicate, Shard]
+    with gate/up split on the FFN rows and down on the FFN columns, as the design doc's FP8 row
+    (EP8 x DP2 -> TP2 x DP8). Weights are random bytes; the scale tensors' shapes are the weight
+    shapes ceil-divided by the block.
+    """
+    data, scales = [], []
+    nsb = ndb = 0
+    ns, nd = dp_src * ep_src, dp_dst * tp_dst
+    for layer in range(layers):
+        s = seed * 1_000_003 + layer * 6
+        for j, (nm, shape) in enumerate((("gate_proj", (experts, ffn, hidden)), ("up_proj", (experts, ffn, hidden)),
+                                         ("down_proj", (experts, hidden, ffn)))):
+            dpl = ("R", "S2") if nm == "down_proj" else ("R", "S1")
+            sshape = shape[:-2] + tuple(-(-x // b) for x, b in zip(shape[-2:], block))
+            for arr, shp, dt, tag in ((data, shape, "u8", "weight"), (scales, sshape, "f32", "weight_scale_inv")):
+                sv = _dense_views(ns, nsb); nsb += ns
+                dv = _dense_views(nd, ndb); ndb += nd
+                arr.append(TensorDesc(f"layers.{layer}.mlp.experts.{nm}.{tag}", shp, dt, (dp_src, ep_src), ("R", "S0"),
+                                      (dp_dst, tp_dst), dpl, sv, dv, s + 2 * j + (tag != "weight"), 1.0))
+    name = f"moe_fp8_{layers}x{experts}x{ffn}x{hidden}_dp{dp_src}ep{ep_src}_to_dp{dp_dst}tp{tp_dst}_b{block[0]}x{block[1]}"
+    wl = Workload(name, data + scales, block=tuple(block))
+    return _size_buffers(wl, nsb, ndb)
+
+
 def brute_force_cases(n_cases: int, seed: int = 7, max_mesh_dims: int = 3, max_mesh: int = 4,
                       max_tensor_dims: int = 3, max_len: int = 9, dtype: str = "i32") -> List[Workload]:
     """Random small problems: every placement kind, nested mesh dims, uneven and empty chunks.
@@ -356,6 +472,12 @@ WORKLOAD_NAMES = {
     "dense_ffn_4x14336x4096_tp8_to_dp2tp2": lambda: dense_ffn(layers=4),
     "dense_ffn_2x14336x4096_tp8_to_dp2tp2": lambda: dense_ffn(layers=2),
     "many_small_1000_tp4_to_dp2tp2": lambda: many_small(n=1000),
+    # KV heads below TP (Q=64, KV=2, head_dim 128) and vLLM fused expert layouts
+    "qkv_4x64q2kv128x8192_tp8_to_tp8": lambda: qkv_kv_below_tp(),
+    "qkv_32x64q2kv128x8192_tp8_to_tp4": lambda: qkv_kv_below_tp(layers=32, tp_dst=4),
+    "moe_w13_48x128x768x2048_ep8_to_tp4": lambda: moe_w13(layers=48, experts=128, per_expert_src=False),
+    "moe_w13_4x128x768x2048_per_expert_to_tp4": lambda: moe_w13(layers=4, experts=128, per_expert_src=True),
+    "moe_fp8_8x128x768x2048_dp2ep8_to_dp8tp2_b128x128": lambda: moe_fp8_blockwise(),
     "moe_1x32x1536x4096_ep16_to_tp4_mxfp8": lambda: moe_experts(layers=1, experts=32, dst="tp4"),
     # a generation side that keeps every FFN weight transposed (local shards column-major)
     "transpose_32x14336x4096_tp8_to_dp2tp2_dst_colmajor": lambda: transposed(tensors=32),

@@ -79,13 +79,15 @@ def sampled_check(wl, lay, per_tensor=8, seed=0, max_tensors=None):
             src_off.append(lay.src_off[sv.buffer] + es * G.element_offset(sv, _src_shape(t, s), sidx))
             dst_off.append(lay.dst_off[dv.buffer] + es * G.element_offset(dv, shp, idx))
             es_list.append(es)
-    assert len(set(es_list)) == 1
-    es = es_list[0]
-    a = _gather(lay.src_slab, np.array(src_off, np.int64), es)
-    b = _gather(lay.dst_slab, np.array(dst_off, np.int64), es)
-    bad = np.nonzero((a != b).any(axis=1))[0]
-    assert bad.size == 0, f"{wl.name}: {bad.size} of {len(a)} sampled elements differ"
-    return len(a)
+    n = 0
+    for es in sorted(set(es_list)):
+        sel = [i for i, e in enumerate(es_list) if e == es]
+        a = _gather(lay.src_slab, np.array([src_off[i] for i in sel], np.int64), es)
+        b = _gather(lay.dst_slab, np.array([dst_off[i] for i in sel], np.int64), es)
+        bad = np.nonzero((a != b).any(axis=1))[0]
+        assert bad.size == 0, f"{wl.name}: {bad.size} of {len(a)} sampled {es}-byte elements differ"
+        n += len(a)
+    return n
 
 
 def sampled_check_mxfp8(wl, lay, per_tensor=8, seed=0):

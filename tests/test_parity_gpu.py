@@ -40,6 +40,16 @@ SMALL = {
                                               dst_pl=("S1", "R"), side="both", dtype="u8"),
     "transpose_3d_i64": lambda: S.transposed(shape=(3, 70, 90), src_mesh=(3,), src_pl=("S0",), dst_mesh=(2,),
                                              dst_pl=("S2",), dtype="i64"),
+    "qkv_kv_below_tp_8_to_8": lambda: S.qkv_kv_below_tp(layers=1, q_heads=16, kv_heads=2, head_dim=16, hidden=96),
+    "qkv_kv_below_tp_8_to_4": lambda: S.qkv_kv_below_tp(layers=2, q_heads=16, kv_heads=2, head_dim=16, hidden=96,
+                                                        tp_dst=4),
+    "qkv_kv_below_tp_4_to_8": lambda: S.qkv_kv_below_tp(layers=1, q_heads=16, kv_heads=2, head_dim=24, hidden=80,
+                                                        tp_src=4, tp_dst=8),
+    "moe_w13_per_expert": lambda: S.moe_w13(layers=1, experts=8, hidden=96, ffn=64, tp_dst=4, per_expert_src=True),
+    "moe_w13_stacked_ep4": lambda: S.moe_w13(layers=1, experts=8, hidden=96, ffn=64, ep_src=4, tp_dst=4,
+                                             per_expert_src=False),
+    "moe_fp8_blockwise": lambda: S.moe_fp8_blockwise(layers=1, experts=4, hidden=256, ffn=384, ep_src=2, dp_src=2,
+                                                     tp_dst=3, dp_dst=2),
 }
 
 
@@ -61,7 +71,7 @@ def _cleanup():
 @pytest.mark.parametrize("name", sorted(SMALL))
 def test_small_workloads_bit_exact(name, misalign, mode):
     wl = SMALL[name]()
-    if misalign % max(S.DTYPES[wl.tensors[0].dtype][1], 1):
+    if any(misalign % S.DTYPES[t.dtype][1] for t in wl.tensors):
         pytest.skip("buffer offset must be a multiple of the element size")
     lay, plan = run_gpu(wl, mode=mode, misalign=misalign)
     assert_matches_oracle(wl, lay)
@@ -204,6 +214,13 @@ def test_full_edge_mix_bit_exact():
         for mode in ("direct", "packed"):
             lay, plan = run_gpu(wl, mode=mode)
             assert_matches_oracle(wl, lay)
+
+
+@pytest.mark.parametrize("name", ["qkv_32x64q2kv128x8192_tp8_to_tp4", "moe_w13_48x128x768x2048_ep8_to_tp4",
+                                  "moe_w13_4x128x768x2048_per_expert_to_tp4",
+                                  "moe_fp8_8x128x768x2048_dp2ep8_to_dp8tp2_b128x128"])
+def test_full_next_rows_sampled(name):
+    _full(lambda: S.workload_by_name(name), "direct", sampled_check, per_tensor=16, max_tensors=400)
 
 
 def test_full_many_small_sampled():
