@@ -278,8 +278,12 @@ __device__ __forceinline__ int item_index(const int32_t *idx, int k) { return id
 __global__ void __launch_bounds__(kBlock, RESHARD_GEN_MIN_BLOCKS) reshard_copy_kernel(
     const Item *__restrict__ items, const int32_t *__restrict__ idx, int n_items, const uint64_t *__restrict__ ptrs,
     const int32_t *__restrict__ gstart, const int32_t *__restrict__ mptr, const int64_t *__restrict__ moff) {
+  Item nxt;
+  if (blockIdx.x < n_items) nxt = items[item_index(idx, blockIdx.x)];
   for (int k = blockIdx.x; k < n_items; k += gridDim.x) {
-    const Item it = items[item_index(idx, k)];
+    const Item it = nxt;
+    // the next item's descriptor is in flight while this one is copied
+    if (k + (int)gridDim.x < n_items) nxt = items[item_index(idx, k + gridDim.x)];
     const int64_t es = it.esize;
     const uint8_t *src = reinterpret_cast<const uint8_t *>(ptrs[it.src]) + it.src_off * es;
     const int g0 = gstart[it.group];
@@ -323,8 +327,12 @@ __global__ void __launch_bounds__(kBlock, RESHARD_MIN_BLOCKS) reshard_copy_align
     const Item *__restrict__ items, const int32_t *__restrict__ idx, int n_items, const uint64_t *__restrict__ ptrs,
     const int32_t *__restrict__ gstart, const int32_t *__restrict__ mptr, const int64_t *__restrict__ moff,
     int32_t *status) {
+  Item nxt;
+  if (blockIdx.x < n_items) nxt = items[item_index(idx, blockIdx.x)];
   for (int k = blockIdx.x; k < n_items; k += gridDim.x) {
-    const Item it = items[item_index(idx, k)];
+    const Item it = nxt;
+    // the next item's descriptor is in flight while this one is copied
+    if (k + (int)gridDim.x < n_items) nxt = items[item_index(idx, k + gridDim.x)];
     const int64_t es = it.esize;
     const uint8_t *src = reinterpret_cast<const uint8_t *>(ptrs[it.src]) + it.src_off * es;
     const int g0 = gstart[it.group];

@@ -159,7 +159,7 @@ def _oracle(wl, lay):
 @pytest.mark.parametrize("name", sorted(SMALL))
 def test_item_tables_reproduce_oracle(name, mode):
     wl = SMALL[name]()
-    lay = S.allocate(wl, "cpu", misalign=2 if wl.tensors[0].dtype in ("bf16", "u8") else 0)
+    lay = S.allocate(wl, "cpu", misalign=2 if all(t.dtype in ("bf16", "u8") for t in wl.tensors) else 0)
     S.fill_sources(wl, lay)
     plan = R.plan_workload(wl)
     for which in (DIRECT, PACK, UNPACK):
