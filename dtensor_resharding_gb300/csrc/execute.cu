@@ -40,10 +40,10 @@ namespace reshard {
 #define RESHARD_MIN_BLOCKS 2
 #endif
 #ifndef RESHARD_GEN_MIN_BLOCKS
-#define RESHARD_GEN_MIN_BLOCKS 3
+#define RESHARD_GEN_MIN_BLOCKS 4
 #endif
 #ifndef RESHARD_GEN_UNROLL
-#define RESHARD_GEN_UNROLL 4
+#define RESHARD_GEN_UNROLL 2
 #endif
 constexpr int kBlock = RESHARD_BLOCK;    // threads per CTA
 constexpr int kUnroll = RESHARD_UNROLL;        // 16-byte loads in flight per thread (aligned walker)
