@@ -352,7 +352,7 @@ def our_arm(args, rank: int, world: int, local_rank: int) -> None:
     launch_ms = statistics.mean(per)
     achieved = algo / (launch_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(kernel, wl.name, args.mode),
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(kernel, args.workload, args.mode),
                 "kernel": kernel, "algorithmic_bytes_per_launch": algo, "peak_source": peak_kind,
                 "launch_ms_median": round(statistics.median(per), 4),
                 "launch_ms_min": round(min(per), 4), "launch_ms_max": round(max(per), 4)}
@@ -390,7 +390,7 @@ def our_arm(args, rank: int, world: int, local_rank: int) -> None:
             "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": wl.name, "mode": args.mode, "quant": quant, "tensors": len(wl.tensors),
+            "config": {"workload": args.workload, "mode": args.mode, "quant": quant, "tensors": len(wl.tensors),
                        "src_bytes": st["bytes_read"], "dst_bytes": dst_bytes,
                        "regions": st["regions"], "items": st["items"],
                        "l2": "inputs larger than L2 (every step streams all sources and destinations)",

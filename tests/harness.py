@@ -21,6 +21,8 @@ def run_gpu(wl, mode="direct", misalign=0, plan=None, execute=True):
         sp, dp = R.workload_pointers(wl, lay)
         R.reshard_execute(plan, sp, dp, mode=mode, quant=wl.quant, stream=torch.cuda.current_stream().cuda_stream)
         torch.cuda.synchronize()
+        # no TMA wait timed out and no item reached the aligned walker unaligned
+        assert R.reshard_plan_status(plan) == 0
     return lay, plan
 
 
