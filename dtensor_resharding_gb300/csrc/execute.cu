@@ -768,6 +768,127 @@ __global__ void __launch_bounds__(kTBlock, 2) reshard_transpose_kernel(
   }
 }
 
+// -------------------------------------------------------------- bulk copy walker (TMA) --
+//
+// reshard_bulk_kernel copies aligned items with the TMA bulk-copy unit instead of load/store
+// instructions: one thread per CTA walks its items as (row, chunk) pieces of up to kBulkChunk
+// bytes, loads each piece into a ring of shared-memory stages (cp.async.bulk, completion on an
+// mbarrier), and writes it to every replica with bulk stores (one bulk group per piece). Loads
+// run kBulkStages - 1 pieces ahead; a stage is reloaded only after the stores that read it are
+// done reading (cp.async.bulk.wait_group.read). Waits on the mbarriers are bounded like the
+// transposing kernel's (status bit 0).
+
+#ifndef RESHARD_BULK
+#define RESHARD_BULK 0
+#endif
+#ifndef RESHARD_BULK_STAGES
+#define RESHARD_BULK_STAGES 4
+#endif
+#ifndef RESHARD_BULK_CHUNK
+#define RESHARD_BULK_CHUNK 49152
+#endif
+constexpr int kBulkStages = RESHARD_BULK_STAGES;
+constexpr int kBulkChunk = RESHARD_BULK_CHUNK;  // bytes per stage (multiple of 16)
+constexpr size_t kBulkSmem = (size_t)kBulkStages * kBulkChunk;
+
+__device__ __forceinline__ bool bulk_wait(uint32_t bar, uint32_t parity) {
+  const unsigned long long deadline = global_ns() + kWaitLimitNs;
+  return bar_wait(bar, parity, deadline);
+}
+
+struct BulkPiece {
+  const uint8_t *src;
+  int64_t dst_off;  // bytes from each member's item base
+  int len;
+};
+
+__global__ void __launch_bounds__(32, 1) reshard_bulk_kernel(const Item *__restrict__ items,
+                                                             const int32_t *__restrict__ idx, int n_items,
+                                                             const uint64_t *__restrict__ ptrs,
+                                                             const int32_t *__restrict__ gstart,
+                                                             const int32_t *__restrict__ mptr,
+                                                             const int64_t *__restrict__ moff, int32_t *status) {
+  extern __shared__ __align__(128) uint8_t bulk_buf[];
+  __shared__ __align__(8) uint64_t bar[kBulkStages];
+  if (threadIdx.x != 0) return;
+  for (int s = 0; s < kBulkStages; ++s) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar[s])));
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+
+  // piece cursor over this CTA's items: item k, row r, byte offset c within the row
+  int k = blockIdx.x, r = 0;
+  int64_t c = 0;
+  Item it{};
+  if (k < n_items) it = items[item_index(idx, k)];
+  auto next_piece = [&](BulkPiece &pc, Item &owner) -> bool {
+    while (k < n_items) {
+      const int64_t run_b = (int64_t)it.run * it.esize;
+      if (r < it.rows && c < run_b) {
+        pc.src = reinterpret_cast<const uint8_t *>(ptrs[it.src]) + (it.src_off + r * it.src_pitch) * it.esize + c;
+        pc.dst_off = (it.dst_off + (int64_t)r * it.dst_pitch) * it.esize + c;
+        pc.len = (int)(run_b - c < kBulkChunk ? run_b - c : (int64_t)kBulkChunk);
+        owner = it;
+        c += pc.len;
+        if (c >= run_b) {
+          c = 0;
+          ++r;
+        }
+        return true;
+      }
+      k += gridDim.x;
+      r = 0;
+      c = 0;
+      if (k < n_items) it = items[item_index(idx, k)];
+    }
+    return false;
+  };
+
+  BulkPiece ring[kBulkStages];
+  Item owner[kBulkStages];
+  uint32_t phases = 0;
+  int issued = 0;  // pieces whose load was issued
+  auto issue_load = [&](int stage) -> bool {
+    if (!next_piece(ring[stage], owner[stage])) return false;
+    const uint32_t b = smem_u32(&bar[stage]);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(ring[stage].len) : "memory");
+    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(bulk_buf + (size_t)stage * kBulkChunk)),
+                 "l"(ring[stage].src), "r"(ring[stage].len), "r"(b)
+                 : "memory");
+    ++issued;
+    return true;
+  };
+  int loaded = 0;
+  for (int s = 0; s < kBulkStages - 1; ++s)
+    if (issue_load(s)) ++loaded;
+  for (int t = 0; t < loaded; ++t) {
+    const int stage = t % kBulkStages;
+    if (!bulk_wait(smem_u32(&bar[stage]), (phases >> stage) & 1)) {
+      // a load never completed: report, give every load in flight one more bounded wait, stop
+      atomicOr(status, 1);
+      for (int u = t; u < loaded; ++u) {
+        const int su = u % kBulkStages;
+        bulk_wait(smem_u32(&bar[su]), (phases >> su) & 1);
+      }
+      break;
+    }
+    phases ^= 1u << stage;
+    const Item &o = owner[stage];
+    const int g0 = gstart[o.group], g1 = gstart[o.group + 1];
+    for (int m = g0; m < g1; ++m) {
+      uint8_t *d = reinterpret_cast<uint8_t *>(ptrs[mptr[m]]) + moff[m] * o.esize + ring[stage].dst_off;
+      asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(d),
+                   "r"(smem_u32(bulk_buf + (size_t)stage * kBulkChunk)), "r"(ring[stage].len)
+                   : "memory");
+    }
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    // reload the stage the previous piece's stores were reading, once they are done reading it
+    const int next_stage = (t + kBulkStages - 1) % kBulkStages;
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+    if (issue_load(next_stage)) ++loaded;
+  }
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------- host side --
 
 namespace {
@@ -793,6 +914,7 @@ int upload(T **dptr, const std::vector<T> &host) {
 
 struct LaunchCaps {
   int device = -1;
+  int bulk_grid = 0;
   int aligned_grid = 0;
   int copy_grid = 0;
   int mxfp8_grid = 0;
@@ -808,11 +930,17 @@ int launch_caps(int device, LaunchCaps &c) {
   int sms = 0, b0 = 0, b1 = 0, b2 = 0, b3 = 0;
   RS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device));
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, reshard_copy_aligned_kernel, kBlock, 0));
+  int bb = 0;
+  if (RESHARD_BULK) {
+    RS_CUDA(cudaFuncSetAttribute(reshard_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBulkSmem));
+    RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bb, reshard_bulk_kernel, 32, kBulkSmem));
+  }
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, reshard_copy_kernel, kBlock, 0));
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b2, reshard_mxfp8_kernel, kQBlock, 0));
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b3, reshard_transpose_kernel, kTBlock, 0));
   g_caps.device = device;
   g_caps.aligned_grid = sms * std::max(1, b0);
+  g_caps.bulk_grid = sms * std::max(1, bb);
   g_caps.copy_grid = sms * std::max(1, b1);
   g_caps.mxfp8_grid = sms * std::max(1, b2);
   g_caps.transpose_grid = sms * std::max(1, b3);
@@ -972,7 +1100,11 @@ int launch(reshard_plan_t *p, int set, bool quant, cudaStream_t stream, const La
     const int32_t *idx = p->d_cls_idx[set];
     p->last_aligned = na;
     p->last_general = ng;
-    if (na > 0) {
+    if (na > 0 && RESHARD_BULK) {
+      reshard_bulk_kernel<<<std::min(na, caps.bulk_grid), 32, kBulkSmem, stream>>>(
+          items, idx, na, p->d_ptrs, p->d_grp_start, p->d_mem_ptr, p->d_mem_off, p->d_status);
+      ++p->last_launches;
+    } else if (na > 0) {
       reshard_copy_aligned_kernel<<<std::min(na, caps.aligned_grid), kBlock, 0, stream>>>(
           items, idx, na, p->d_ptrs, p->d_grp_start, p->d_mem_ptr, p->d_mem_off, p->d_status);
       ++p->last_launches;
