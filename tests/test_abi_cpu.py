@@ -180,3 +180,31 @@ def test_empty_batch_and_empty_tensor():
     plan = R.reshard_plan_create(d)
     assert R.reshard_plan_stats(plan)["regions"] == 0
     R.reshard_execute(plan, [0, 0], [0] * 4)
+
+
+def test_static_entry_rejects_transposing_plans_before_any_cuda_call():
+    wl = S.transposed(shape=(300, 200), src_mesh=(2,), src_pl=("S0",), dst_mesh=(2,), dst_pl=("S1",))
+    plan = R.plan_workload(wl)
+    with pytest.raises(R.ReshardError) as e:
+        R.reshard_execute_static(plan, [1] * plan.n_src_ptrs, [1] * plan.n_dst_ptrs)
+    assert e.value.code == R.RESHARD_ERR_UNSUPPORTED and "transposing" in str(e.value)
+
+
+def test_status_is_zero_before_any_execute():
+    plan = R.plan_workload(S.example_8x8())
+    assert R.reshard_plan_status(plan) == 0
+
+
+def test_dp8_replicas_are_read_once():
+    """The planner reads one of the eight DP replicas: naive per-replica reading moves 8x more."""
+    _, meta = read_fixture("dp8_dedup.txt")
+    d = S.TensorDesc("w", (4096, 2560), "bf16", (8, 2), ("R", "S0"), (4, 4), ("R", "S0"),
+                     [S.View(i) for i in range(16)], [S.View(i) for i in range(16)])
+    st = R.reshard_plan_stats(R.reshard_plan_create(d))
+    total = 4096 * 2560 * 2
+    assert st["bytes_read"] == total
+    naive = int(meta["replicas_on_source"][0]) * total
+    assert naive // st["bytes_read"] == int(meta["bytes_read_ratio_naive_over_planned"][0])
+    assert st["bytes_written"] == 4 * total   # four engines, each a full TP4 copy
+    # every region's source is the lowest-index replica (dp = 0): pointer indices 0 and 1
+    assert {s for _, s, _, _ in R.reshard_plan_regions(R.reshard_plan_create(d))} == {0, 1}
