@@ -207,103 +207,23 @@ __device__ __forceinline__ void copy_aligned32(const uint8_t *__restrict__ src, 
   }
 }
 
-// General alignment: destination replicas must agree modulo 16. A warp owns 32 consecutive
-// aligned 16-byte destination words of one row (kShiftUnroll such chunks per pass, loads
-// first). Within a row every word needs the same byte shift sh of the source, so lane i loads
-// the one aligned source block under its word and takes the next block from lane i + 1 with
-// shfl.down (lane 31 loads that block itself); the word is funnel-shifted into place and stored
-// whole, or at the row's two ends in naturally aligned 8/4/2/1-byte pieces. A source block is
-// loaded only when it holds at least one byte of the row, so no access leaves the 16-byte
-// blocks (and hence the pages) the region occupies.
-#ifndef RESHARD_SHIFT_UNROLL
-#define RESHARD_SHIFT_UNROLL 2
-#endif
-#ifndef RESHARD_SHIFT_WARP
-#define RESHARD_SHIFT_WARP 0
-#endif
-constexpr int kShiftUnroll = RESHARD_SHIFT_UNROLL;
-
-__device__ __forceinline__ uint4 shfl_down4(uint4 v) {
-  uint4 o;
-  o.x = __shfl_down_sync(0xffffffffu, v.x, 1);
-  o.y = __shfl_down_sync(0xffffffffu, v.y, 1);
-  o.z = __shfl_down_sync(0xffffffffu, v.z, 1);
-  o.w = __shfl_down_sync(0xffffffffu, v.w, 1);
-  return o;
-}
-
-template <int NF>
-__device__ __forceinline__ void copy_shifted(const uint8_t *__restrict__ src, uint8_t *const *dst, int nf, int rows,
-                                             int64_t run_b, int64_t sp_b, int64_t dp_b) {
-  constexpr int kWarps = kBlock / 32;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nwmax = (int)((run_b + 15) >> 4) + 1;  // destination words a row can touch
-  const int nq = (nwmax + 31) >> 5;                 // 32-word chunks per row
-  const int units = rows * nq;
-  const uintptr_t d0 = reinterpret_cast<uintptr_t>(dst[0]);
-  for (int base = warp; base < units; base += kWarps * kShiftUnroll) {
-    uint4 lo[kShiftUnroll], nx[kShiftUnroll];
-    int64_t dpos[kShiftUnroll];  // destination byte offset of the word's byte 0, from dst[f]
-    int kmin[kShiftUnroll], kmax[kShiftUnroll], sh[kShiftUnroll];
-#pragma unroll
-    for (int u = 0; u < kShiftUnroll; ++u) {
-      const int unit = base + u * kWarps;  // warp-uniform
-      kmin[u] = 16;
-      kmax[u] = 0;
-      sh[u] = 0;
-      dpos[u] = 0;
-      lo[u] = make_uint4(0, 0, 0, 0);
-      nx[u] = make_uint4(0, 0, 0, 0);
-      if (unit < units) {
-        const int r = rows == 1 ? 0 : unit / nq;
-        const int w = (unit - r * nq) * 32 + lane;
-        const int64_t drow = r * dp_b;
-        const int a = (int)((d0 + drow) & 15);
-        const int64_t start = 16 * (int64_t)w - a;  // row byte of this word's byte 0
-        const uintptr_t s0 = reinterpret_cast<uintptr_t>(src) + r * sp_b;  // row start in the source
-        const uintptr_t p0 = s0 + start;
-        sh[u] = (int)(p0 & 15);
-        const uintptr_t blk = p0 - sh[u];
-        if (blk < s0 + run_b && blk + 16 > s0) lo[u] = __ldg(reinterpret_cast<const uint4 *>(blk));
-        if (lane == 31 && sh[u] && blk + 16 < s0 + run_b && blk + 32 > s0)
-          nx[u] = __ldg(reinterpret_cast<const uint4 *>(blk + 16));
-        if (start < run_b) {
-          kmin[u] = start < 0 ? (int)-start : 0;
-          kmax[u] = run_b - start < 16 ? (int)(run_b - start) : 16;
-          dpos[u] = drow + start;
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kShiftUnroll; ++u) {
-      if (base + u * kWarps >= units) break;  // warp-uniform: every lane takes part in the shuffle
-      uint4 hi = shfl_down4(lo[u]);
-      if (lane == 31) hi = nx[u];
-      if (kmin[u] >= kmax[u]) continue;
-      const uint4 o = sh[u] ? shift_bytes(lo[u], hi, sh[u]) : lo[u];
-      if (kmin[u] == 0 && kmax[u] == 16) {
-#pragma unroll
-        for (int f = 0; f < NF; ++f)
-          if (f < nf) store_stream(dst[f] + dpos[u], o);
-      } else {
-#pragma unroll
-        for (int f = 0; f < NF; ++f)
-          if (f < nf) store_partial(dst[f] + dpos[u], o, kmin[u], kmax[u]);
-      }
-    }
-  }
-}
-
-// The same move with thread-owned words (two loads per word), kept for comparison.
 // General alignment: destination replicas must agree modulo 16. Each thread owns aligned
 // 16-byte destination words (kShiftUnroll of them per pass, loads first), assembles each from
 // the (at most two) aligned 16-byte source blocks that hold its bytes, and stores it whole, or
-// byte by byte at the two ends of a row. A source block is loaded only when it holds at least
-// one byte of the row, so no access leaves the 16-byte blocks (and hence the pages) the region
-// occupies.
+// at the two ends of a row in naturally aligned 8/4/2/1-byte pieces. A source block is loaded
+// only when it holds at least one byte of the row, so no access leaves the 16-byte blocks (and
+// hence the pages) the region occupies.
+#ifndef RESHARD_SHIFT_UNROLL
+#define RESHARD_SHIFT_UNROLL 2
+#endif
+#ifndef RESHARD_SHIFT_WORDS
+#define RESHARD_SHIFT_WORDS 1
+#endif
+constexpr int kShiftUnroll = RESHARD_SHIFT_UNROLL;
+constexpr int kShiftWords = RESHARD_SHIFT_WORDS;
 
 template <int NF>
-__device__ __forceinline__ void copy_shifted_slots(const uint8_t *__restrict__ src, uint8_t *const *dst, int nf, int rows,
+__device__ __forceinline__ void copy_shifted(const uint8_t *__restrict__ src, uint8_t *const *dst, int nf, int rows,
                                              int64_t run_b, int64_t sp_b, int64_t dp_b) {
   const int nwmax = (int)((run_b + 15) >> 4) + 1;  // destination words a row can touch
   const int total = rows * nwmax;
@@ -351,6 +271,55 @@ __device__ __forceinline__ void copy_shifted_slots(const uint8_t *__restrict__ s
 #pragma unroll
         for (int f = 0; f < NF; ++f)
           if (f < nf) store_partial(dst[f] + dpos[u], o, kmin[u], kmax[u]);
+      }
+    }
+  }
+}
+
+// The same move with W consecutive destination words per thread: the row, alignment and shift
+// arithmetic is done once per group and the W + 1 aligned source blocks under the group are
+// each loaded once (W loads plus one for the shifted tail), so the path issues about W times
+// fewer address instructions per byte.
+template <int NF, int W>
+__device__ __forceinline__ void copy_shifted_wide(const uint8_t *__restrict__ src, uint8_t *const *dst, int nf, int rows,
+                                                  int64_t run_b, int64_t sp_b, int64_t dp_b) {
+  const int nwmax = (int)((run_b + 15) >> 4) + 1;  // destination words a row can touch
+  const int ng = (nwmax + W - 1) / W;               // word groups per row
+  const int total = rows * ng;
+  const uintptr_t d0 = reinterpret_cast<uintptr_t>(dst[0]);
+  for (int j = threadIdx.x; j < total; j += kBlock) {
+    const int r = rows == 1 ? 0 : j / ng;
+    const int g = j - r * ng;
+    const int64_t drow = r * dp_b;
+    const int a = (int)((d0 + drow) & 15);
+    const int64_t start0 = 16 * (int64_t)(g * W) - a;  // row byte of the group's byte 0
+    if (start0 >= run_b) continue;
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(src) + r * sp_b;  // row start in the source
+    const uintptr_t p0 = s0 + start0;
+    const int sh = (int)(p0 & 15);
+    const uintptr_t blk0 = p0 - sh;
+    uint4 b[W + 1];
+#pragma unroll
+    for (int k = 0; k <= W; ++k) {
+      const uintptr_t blk = blk0 + 16 * k;
+      b[k] = make_uint4(0, 0, 0, 0);
+      if ((k < W || sh) && blk < s0 + run_b && blk + 16 > s0) b[k] = __ldg(reinterpret_cast<const uint4 *>(blk));
+    }
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+      const int64_t st = start0 + 16 * k;
+      if (st >= run_b) break;
+      const int kmin = st < 0 ? (int)-st : 0;
+      const int kmax = run_b - st < 16 ? (int)(run_b - st) : 16;
+      const uint4 o = sh ? shift_bytes(b[k], b[k + 1], sh) : b[k];
+      if (kmin == 0 && kmax == 16) {
+#pragma unroll
+        for (int f = 0; f < NF; ++f)
+          if (f < nf) store_stream(dst[f] + drow + st, o);
+      } else {
+#pragma unroll
+        for (int f = 0; f < NF; ++f)
+          if (f < nf) store_partial(dst[f] + drow + st, o, kmin, kmax);
       }
     }
   }
@@ -405,18 +374,15 @@ __global__ void __launch_bounds__(kBlock, RESHARD_GEN_MIN_BLOCKS) reshard_copy_k
       } else if ((amask & 15) == 0) {
         copy_aligned<kGenUnroll>(src, dst, nf, it.rows, run_b, sp_b, dp_b);
       } else if (same && nf <= 2) {
-        if (RESHARD_SHIFT_WARP)
-          copy_shifted<2>(src, dst, nf, it.rows, run_b, sp_b, dp_b);
+        if (kShiftWords > 1)
+          copy_shifted_wide<2, kShiftWords>(src, dst, nf, it.rows, run_b, sp_b, dp_b);
         else
-          copy_shifted_slots<2>(src, dst, nf, it.rows, run_b, sp_b, dp_b);
+          copy_shifted<2>(src, dst, nf, it.rows, run_b, sp_b, dp_b);
       } else {
         // replicas differ modulo 16 (or many of them): one replica per pass
         for (int f = 0; f < nf; ++f) {
           uint8_t *one[1] = {pick(dst, f)};
-          if (RESHARD_SHIFT_WARP)
-            copy_shifted<1>(src, one, 1, it.rows, run_b, sp_b, dp_b);
-          else
-            copy_shifted_slots<1>(src, one, 1, it.rows, run_b, sp_b, dp_b);
+          copy_shifted<1>(src, one, 1, it.rows, run_b, sp_b, dp_b);
         }
       }
     }

@@ -184,8 +184,11 @@ int reshard_plan_blockwise_fp8(const reshard_tensor_spec_t *specs, int n_tensors
  *   a multiple of 32; dense destination views; otherwise UNSUPPORTED).
  * The first execute binds the plan to the current device and uploads its descriptor tables
  * (synchronous device allocations: do it outside stream capture); RESHARD_PACKED also
- * allocates the message workspace (stats.message_bytes) on first use. The pointer table is
- * re-uploaded on `stream` only when the pointers differ from the previous call's.
+ * allocates the message workspace (stats.message_bytes) on first use. When the pointers differ
+ * from the previous call's, the pointer table is re-uploaded on `stream`, the TMA tensor maps of
+ * transposing regions are re-encoded, and the copy items are re-sorted on the host into those
+ * 16-byte aligned everywhere (run by the aligned walker) and the rest (run by the general
+ * walker): host work proportional to the plan's items, none when the pointers repeat.
  * Buffers must stay valid until the stream reaches the end of the work. Executes of one plan
  * on different streams that overlap in time race on its tables and workspace.
  * Errors: INVALID_ARG (NULL pointer for a non-empty shard, other device), UNSUPPORTED,
