@@ -216,11 +216,7 @@ __device__ __forceinline__ void copy_aligned32(const uint8_t *__restrict__ src, 
 #ifndef RESHARD_SHIFT_UNROLL
 #define RESHARD_SHIFT_UNROLL 2
 #endif
-#ifndef RESHARD_SHIFT_WORDS
-#define RESHARD_SHIFT_WORDS 1
-#endif
 constexpr int kShiftUnroll = RESHARD_SHIFT_UNROLL;
-constexpr int kShiftWords = RESHARD_SHIFT_WORDS;
 
 template <int NF>
 __device__ __forceinline__ void copy_shifted(const uint8_t *__restrict__ src, uint8_t *const *dst, int nf, int rows,
@@ -276,55 +272,6 @@ __device__ __forceinline__ void copy_shifted(const uint8_t *__restrict__ src, ui
   }
 }
 
-// The same move with W consecutive destination words per thread: the row, alignment and shift
-// arithmetic is done once per group and the W + 1 aligned source blocks under the group are
-// each loaded once (W loads plus one for the shifted tail), so the path issues about W times
-// fewer address instructions per byte.
-template <int NF, int W>
-__device__ __forceinline__ void copy_shifted_wide(const uint8_t *__restrict__ src, uint8_t *const *dst, int nf, int rows,
-                                                  int64_t run_b, int64_t sp_b, int64_t dp_b) {
-  const int nwmax = (int)((run_b + 15) >> 4) + 1;  // destination words a row can touch
-  const int ng = (nwmax + W - 1) / W;               // word groups per row
-  const int total = rows * ng;
-  const uintptr_t d0 = reinterpret_cast<uintptr_t>(dst[0]);
-  for (int j = threadIdx.x; j < total; j += kBlock) {
-    const int r = rows == 1 ? 0 : j / ng;
-    const int g = j - r * ng;
-    const int64_t drow = r * dp_b;
-    const int a = (int)((d0 + drow) & 15);
-    const int64_t start0 = 16 * (int64_t)(g * W) - a;  // row byte of the group's byte 0
-    if (start0 >= run_b) continue;
-    const uintptr_t s0 = reinterpret_cast<uintptr_t>(src) + r * sp_b;  // row start in the source
-    const uintptr_t p0 = s0 + start0;
-    const int sh = (int)(p0 & 15);
-    const uintptr_t blk0 = p0 - sh;
-    uint4 b[W + 1];
-#pragma unroll
-    for (int k = 0; k <= W; ++k) {
-      const uintptr_t blk = blk0 + 16 * k;
-      b[k] = make_uint4(0, 0, 0, 0);
-      if ((k < W || sh) && blk < s0 + run_b && blk + 16 > s0) b[k] = __ldg(reinterpret_cast<const uint4 *>(blk));
-    }
-#pragma unroll
-    for (int k = 0; k < W; ++k) {
-      const int64_t st = start0 + 16 * k;
-      if (st >= run_b) break;
-      const int kmin = st < 0 ? (int)-st : 0;
-      const int kmax = run_b - st < 16 ? (int)(run_b - st) : 16;
-      const uint4 o = sh ? shift_bytes(b[k], b[k + 1], sh) : b[k];
-      if (kmin == 0 && kmax == 16) {
-#pragma unroll
-        for (int f = 0; f < NF; ++f)
-          if (f < nf) store_stream(dst[f] + drow + st, o);
-      } else {
-#pragma unroll
-        for (int f = 0; f < NF; ++f)
-          if (f < nf) store_partial(dst[f] + drow + st, o, kmin, kmax);
-      }
-    }
-  }
-}
-
 // dst[f] for a runtime f without indexing the array (keeps it in registers).
 __device__ __forceinline__ uint8_t *pick(uint8_t *const *dst, int f) {
   uint8_t *p = dst[0];
@@ -374,10 +321,7 @@ __global__ void __launch_bounds__(kBlock, RESHARD_GEN_MIN_BLOCKS) reshard_copy_k
       } else if ((amask & 15) == 0) {
         copy_aligned<kGenUnroll>(src, dst, nf, it.rows, run_b, sp_b, dp_b);
       } else if (same && nf <= 2) {
-        if (kShiftWords > 1)
-          copy_shifted_wide<2, kShiftWords>(src, dst, nf, it.rows, run_b, sp_b, dp_b);
-        else
-          copy_shifted<2>(src, dst, nf, it.rows, run_b, sp_b, dp_b);
+        copy_shifted<2>(src, dst, nf, it.rows, run_b, sp_b, dp_b);
       } else {
         // replicas differ modulo 16 (or many of them): one replica per pass
         for (int f = 0; f < nf; ++f) {
