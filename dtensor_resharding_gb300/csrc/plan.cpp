@@ -11,6 +11,7 @@
 #include <algorithm>
 #include <cstring>
 #include <map>
+#include <memory>
 #include <new>
 #include <sstream>
 #include <utility>
@@ -399,7 +400,8 @@ int build(const reshard_tensor_spec_t *specs, int n, reshard_plan_t **out) {
   *out = nullptr;
   if (n < 0 || (n > 0 && !specs)) return fail(RESHARD_ERR_INVALID_ARG, "specs is NULL or n_tensors < 0");
   Violations v;
-  auto plan = new reshard_plan();
+  std::unique_ptr<reshard_plan> owner(new reshard_plan());
+  reshard_plan *plan = owner.get();
   plan->tensors.resize((size_t)n);
 
   // 1. validate every tensor and compute every rank's box and view
@@ -442,10 +444,7 @@ int build(const reshard_tensor_spec_t *specs, int n, reshard_plan_t **out) {
     plan->n_src_ptrs += t.n_src;
     plan->n_dst_ptrs += t.n_dst;
   }
-  if (!v.lines.empty()) {
-    delete plan;
-    return v.report();
-  }
+  if (!v.lines.empty()) return v.report();
 
   // 2. replica groups, intersections and source choice
   plan->quant_ok = true;
@@ -520,7 +519,6 @@ int build(const reshard_tensor_spec_t *specs, int n, reshard_plan_t **out) {
         plan->regions.push_back(r);
       }
       if (covered != volume(grp.box, nd)) {
-        delete plan;
         return fail(RESHARD_ERR_COVERAGE, pre + "sources cover " + std::to_string(covered) + " of " +
                                               std::to_string(volume(grp.box, nd)) + " destination elements");
       }
@@ -629,10 +627,9 @@ int build(const reshard_tensor_spec_t *specs, int n, reshard_plan_t **out) {
   st.global_bytes = global_bytes;
   if (st.items > INT32_MAX || (int64_t)plan->mem_ptr.size() > INT32_MAX || (int64_t)plan->slabs.size() > INT32_MAX ||
       pointer_table_size(plan) > INT32_MAX) {
-    delete plan;
     return fail(RESHARD_ERR_UNSUPPORTED, "plan too large (more than 2^31 items, members or pointers)");
   }
-  *out = plan;
+  *out = owner.release();
   set_error("");
   return RESHARD_OK;
 }

@@ -428,6 +428,59 @@ def moe_fp8_blockwise(layers: int = 8, experts: int = 128, hidden: int = 2048, f
     return _size_buffers(wl, nsb, ndb)
 
 
+def fuzz_cases(n_cases: int, seed: int = 13, max_len: int = 300) -> List[Workload]:
+    """Random problems with random buffer layouts: per rank a dense, padded-pitch, column-major
+    (last two dims swapped) or offset view, over 2-D/3-D tensors, 1-D/2-D meshes and four dtypes.
+    Values are seeded random numbers of the dtype."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = []
+    for k in range(n_cases):
+        nd = int(rng.integers(2, 4))
+        shape = tuple(int(x) for x in rng.integers(1, max_len + 1, size=nd))
+        if nd == 3:
+            shape = (int(rng.integers(1, 5)),) + shape[1:]
+        dtype = str(rng.choice(["bf16", "f32", "u8", "i64"]))
+
+        def mesh_and_pl():
+            md = int(rng.integers(1, 3))
+            mesh = tuple(int(x) for x in rng.integers(1, 5, size=md))
+            pls = tuple("R" if c == nd else f"S{c}" for c in rng.integers(0, nd + 1, size=md))
+            return mesh, pls
+
+        sm, sp = mesh_and_pl()
+        dm, dp = mesh_and_pl()
+        views = {}
+        nbuf = {"src": 0, "dst": 0}
+        for side, mesh, pls in (("src", sm, sp), ("dst", dm, dp)):
+            vs = []
+            for coord in mesh_coords(mesh):
+                shp = local_shape(shape, mesh, pls, coord)
+                kind = int(rng.integers(0, 4))
+                off = int(rng.integers(0, 9)) if rng.random() < 0.3 else 0
+                st = None
+                if kind == 1:    # padded row pitch
+                    pad = int(rng.integers(1, 40))
+                    st = [0] * nd
+                    st[-1] = 1
+                    st[-2] = max(1, shp[-1]) + pad
+                    if nd == 3:
+                        st[0] = st[-2] * max(1, shp[-2])
+                    st = tuple(st)
+                elif kind == 2:  # column-major in the last two dims
+                    st = [0] * nd
+                    st[-2] = 1
+                    st[-1] = max(1, shp[-2])
+                    if nd == 3:
+                        st[0] = max(1, shp[-2]) * max(1, shp[-1])
+                    st = tuple(st)
+                vs.append(View(nbuf[side], off, st))
+                nbuf[side] += 1
+            views[side] = vs
+        t = TensorDesc(f"fz{k}", shape, dtype, sm, sp, dm, dp, views["src"], views["dst"], seed=seed * 7919 + k)
+        out.append(_size_buffers(Workload(f"fuzz_{k}", [t]), nbuf["src"], nbuf["dst"]))
+    return out
+
+
 def brute_force_cases(n_cases: int, seed: int = 7, max_mesh_dims: int = 3, max_mesh: int = 4,
                       max_tensor_dims: int = 3, max_len: int = 9, dtype: str = "i32") -> List[Workload]:
     """Random small problems: every placement kind, nested mesh dims, uneven and empty chunks.

@@ -200,3 +200,16 @@ def test_full_size_item_bounds(name):
     for which in (DIRECT, PACK, UNPACK):
         check_bounds(wl, lay, plan, which, quant=wl.quant == "mxfp8")
         check_transpose_bounds(wl, lay, plan, which)
+
+
+def test_item_tables_fuzzed_layouts():
+    """Random shapes, meshes, dtypes and per-rank layouts (dense, padded, column-major, offset)."""
+    for wl in S.fuzz_cases(60, seed=23):
+        lay = S.allocate(wl, "cpu")
+        S.fill_sources(wl, lay)
+        plan = R.plan_workload(wl)
+        for which in (DIRECT, PACK, UNPACK):
+            check_bounds(wl, lay, plan, which)
+            check_transpose_bounds(wl, lay, plan, which)
+        for mode in ("direct", "packed"):
+            assert np.array_equal(emulate(wl, lay, plan, mode), _oracle(wl, lay)), (wl.tensors[0], mode)

@@ -232,3 +232,11 @@ def test_full_transposed_destination_sampled(mode):
     wl, lay, plan = _full(lambda: S.workload_by_name("transpose_32x14336x4096_tp8_to_dp2tp2_dst_colmajor"), mode,
                           sampled_check, per_tensor=64)
     assert R.reshard_plan_status(plan) == 0
+
+
+@pytest.mark.parametrize("mode", ["direct", "packed"])
+def test_fuzzed_layouts_bit_exact(mode):
+    """Random shapes, meshes, dtypes and per-rank layouts; copy, funnel-shift and TMA paths."""
+    for i, wl in enumerate(S.fuzz_cases(60, seed=23)):
+        lay, plan = run_gpu(wl, mode=mode, misalign=[0, 8][i % 2])
+        assert_matches_oracle(wl, lay)
