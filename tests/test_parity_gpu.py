@@ -240,3 +240,19 @@ def test_fuzzed_layouts_bit_exact(mode):
     for i, wl in enumerate(S.fuzz_cases(60, seed=23)):
         lay, plan = run_gpu(wl, mode=mode, misalign=[0, 8][i % 2])
         assert_matches_oracle(wl, lay)
+
+
+def test_execute_replays_from_a_cuda_graph():
+    """Once a plan has run with some pointers, executes with the same pointers only launch
+    kernels, so they can be captured into a CUDA graph and replayed."""
+    wl = S.dense_ffn(layers=1, hidden=256, ffn=1024)
+    lay, plan = run_gpu(wl)                      # binds the plan and uploads its tables
+    S.fill_canary(lay)
+    sp, dp = R.workload_pointers(wl, lay)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        R.reshard_execute(plan, sp, dp, stream=s.cuda_stream)
+    g.replay()
+    torch.cuda.synchronize()
+    assert_matches_oracle(wl, lay)
