@@ -179,8 +179,13 @@ def test_item_tables_brute_force():
             assert np.array_equal(emulate(wl, lay, plan, mode), _oracle(wl, lay))
 
 
-def test_mxfp8_item_tables_small():
-    wl = S.moe_experts(layers=1, experts=16, hidden=256, ffn=256, dst="tp4")
+@pytest.mark.parametrize("case", ["moe_tp4", "six_replicas"])
+def test_mxfp8_item_tables_small(case):
+    if case == "moe_tp4":
+        wl = S.moe_experts(layers=1, experts=16, hidden=256, ffn=256, dst="tp4")
+    else:  # more destination replicas than one quantizer pass writes
+        from test_parity_gpu import _one
+        wl = _one((64, 128), (2,), ("S0",), (6, 2), ("R", "S1"), quant="mxfp8")
     lay = S.allocate(wl, "meta")
     plan = R.plan_workload(wl)
     # the plan accepts MXFP8: with NULL pointers the execute stops at the pointer check

@@ -50,7 +50,19 @@ SMALL = {
                                              per_expert_src=False),
     "moe_fp8_blockwise": lambda: S.moe_fp8_blockwise(layers=1, experts=4, hidden=256, ffn=384, ep_src=2, dp_src=2,
                                                      tp_dst=3, dp_dst=2),
+    "identity_tp4": lambda: _one((1000, 333), (4,), ("S0",), (4,), ("S0",)),
+    "broadcast_16_replicas": lambda: _one((100, 300), (1,), ("R",), (16,), ("R",)),
+    "nearly_empty_1x1": lambda: _one((1, 1), (2,), ("S0",), (3,), ("S1",)),
+    "replicated_source_to_2d": lambda: _one((257, 130), (3, 2), ("R", "S1"), (2, 2), ("S0", "S1")),
 }
+
+
+def _one(shape, sm, sp, dm, dp, dtype="bf16", quant="none"):
+    import numpy as _np
+    ns, nd = int(_np.prod(sm)), int(_np.prod(dm))
+    t = S.TensorDesc("w", shape, dtype, sm, sp, dm, dp, [S.View(i) for i in range(ns)], [S.View(i) for i in range(nd)],
+                     seed=31)
+    return S.workloads._size_buffers(S.Workload("one", [t], quant=quant), ns, nd)
 
 
 def _as_i16(x):
@@ -102,6 +114,14 @@ def test_brute_force_small_meshes(mode):
 def test_mxfp8_small_bit_exact(mode, misalign):
     wl = S.moe_experts(layers=1, experts=16, hidden=256, ffn=256, dst="tp4")
     lay, plan = run_gpu(wl, mode=mode, misalign=misalign)
+    assert_matches_oracle(wl, lay)
+
+
+@pytest.mark.parametrize("mode", ["direct", "packed"])
+def test_mxfp8_six_replicas(mode):
+    """A quantized destination replicated 6 ways: more replicas than one quantizer pass holds."""
+    wl = _one((64, 128), (2,), ("S0",), (6, 2), ("R", "S1"), quant="mxfp8")
+    lay, plan = run_gpu(wl, mode=mode)
     assert_matches_oracle(wl, lay)
 
 
