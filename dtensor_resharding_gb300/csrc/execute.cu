@@ -21,6 +21,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -1000,10 +1001,58 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return g_encode;
 }
 
+// Every pointer the kernels dereference must be reachable from `device`: memory of that device,
+// managed memory, or page-locked host memory mapped into the device's address space
+// (cudaHostAlloc, cudaMallocHost, cudaHostRegister). The kernels then read and write host memory
+// in place over the host link. A host pointer whose device alias differs from it is replaced by
+// the alias in `table`; `host[i]` marks host memory, over which no TMA tensor map is encoded.
+// Pageable host memory and other devices' memory are refused, naming up to eight entries.
+int check_pointers(const reshard_plan_t *p, std::vector<uint64_t> &table, std::vector<uint8_t> &host) {
+  const int64_t Ns = p->n_src_ptrs, Nd = p->n_dst_ptrs;
+  host.assign(table.size(), 0);
+  std::string bad;
+  int n_bad = 0;
+  for (int64_t i = 0; i < Ns + 2 * Nd; ++i) {
+    const uint64_t v = table[(size_t)i];
+    if (!v) continue;
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, reinterpret_cast<const void *>(v)) != cudaSuccess) {
+      (void)cudaGetLastError();
+      a.type = cudaMemoryTypeUnregistered;
+    }
+    const char *why = nullptr;
+    if (a.type == cudaMemoryTypeDevice) {
+      if (a.device != p->device) why = "is memory of another device";
+    } else if (a.type == cudaMemoryTypeHost) {
+      if (!a.devicePointer) {
+        why = "is page-locked host memory without a device mapping";
+      } else {
+        table[(size_t)i] = reinterpret_cast<uint64_t>(a.devicePointer);
+        host[(size_t)i] = 1;
+      }
+    } else if (a.type != cudaMemoryTypeManaged) {
+      why = "is pageable host memory (page-lock it with cudaHostRegister or use device memory)";
+    }
+    if (why && n_bad++ < 8) {
+      const std::string which = i < Ns        ? "source pointer " + std::to_string(i)
+                                : i < Ns + Nd ? "destination pointer " + std::to_string(i - Ns)
+                                              : "scale pointer " + std::to_string(i - Ns - Nd);
+      char addr[32];
+      std::snprintf(addr, sizeof addr, "0x%llx", (unsigned long long)v);
+      bad += "\n  " + which + " (" + addr + ") " + why;
+    }
+  }
+  if (n_bad)
+    return fail(RESHARD_ERR_INVALID_ARG,
+                std::to_string(n_bad) + " pointer(s) the device cannot dereference:" + bad);
+  return RESHARD_OK;
+}
+
 // One 2-D tensor map per source slab of the transposing items, for the current pointers. A slab
 // whose base or row pitch is not 16-byte aligned (or that the driver rejects) gets map_ok = 0:
 // its tiles are then loaded with plain loads.
-int encode_maps(reshard_plan_t *p, const std::vector<uint64_t> &table, cudaStream_t stream) {
+int encode_maps(reshard_plan_t *p, const std::vector<uint64_t> &table, const std::vector<uint8_t> &host,
+                cudaStream_t stream) {
   const size_t n = p->slabs.size();
   if (!n) return RESHARD_OK;
   std::vector<CUtensorMap> maps(n);
@@ -1013,7 +1062,7 @@ int encode_maps(reshard_plan_t *p, const std::vector<uint64_t> &table, cudaStrea
     const SlabSpec &sl = p->slabs[i];
     const uint64_t base = table[(size_t)sl.ptr] + (uint64_t)sl.base_off * (uint64_t)sl.esize;
     const uint64_t stride = (uint64_t)sl.pitch * (uint64_t)sl.esize;
-    if (!table[(size_t)sl.ptr] || base % 16 || stride % 16 || stride == 0 || stride >= (1ull << 40) || sl.cols < 1 ||
+    if (!table[(size_t)sl.ptr] || host[(size_t)sl.ptr] || base % 16 || stride % 16 || stride == 0 || stride >= (1ull << 40) || sl.cols < 1 ||
         sl.rows < 1 || sl.cols > (1ll << 32) || sl.rows > (1ll << 32))
       continue;
     const CUtensorMapDataType dt = sl.esize == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
@@ -1064,7 +1113,7 @@ int launch_transpose(reshard_plan_t *p, int set, cudaStream_t stream, const Laun
 int classify(reshard_plan_t *p, int set, cudaStream_t stream) {
   if (p->d_cls_idx[set] && p->cls_version[set] == p->ptr_version) return RESHARD_OK;
   const std::vector<Item> &items = p->items[set];
-  const std::vector<uint64_t> &tab = p->ptr_cache;
+  const std::vector<uint64_t> &tab = p->dev_ptrs;
   std::vector<int32_t> &idx = p->cls_idx[set];
   idx.clear();
   idx.reserve(items.size());
@@ -1113,7 +1162,7 @@ int launch(reshard_plan_t *p, int set, bool quant, cudaStream_t stream, const La
     const int32_t *idx = p->d_cls_idx[set];
     p->last_aligned = na;
     p->last_general = ng;
-    if (na > 0 && RESHARD_BULK) {
+    if (na > 0 && RESHARD_BULK && !p->any_host) {  // bulk copies over device memory only
       reshard_bulk_kernel<<<std::min(na, caps.bulk_grid), 32, kBulkSmem, stream>>>(
           items, idx, na, p->d_ptrs, p->d_grp_start, p->d_mem_ptr, p->d_mem_off, p->d_status);
       ++p->last_launches;
@@ -1219,9 +1268,16 @@ extern "C" int reshard_execute(reshard_plan_t *p, void *const *src_ptrs, void *c
   table[(size_t)p->workspace_ptr] = reinterpret_cast<uint64_t>(p->d_workspace);
 
   if (!p->ptr_cache_valid || p->ptr_cache != table) {
-    // pageable source: the runtime stages the bytes before returning, so `table` may die
-    RS_CUDA(cudaMemcpyAsync(p->d_ptrs, table.data(), table.size() * sizeof(uint64_t), cudaMemcpyHostToDevice, stream));
-    if ((rc = encode_maps(p, table, stream))) return rc;
+    p->ptr_cache_valid = false;
+    std::vector<uint64_t> dev_table = table;
+    std::vector<uint8_t> host;
+    if ((rc = check_pointers(p, dev_table, host))) return rc;
+    // pageable source: the runtime stages the bytes before returning, so `dev_table` may die
+    RS_CUDA(cudaMemcpyAsync(p->d_ptrs, dev_table.data(), dev_table.size() * sizeof(uint64_t), cudaMemcpyHostToDevice,
+                            stream));
+    if ((rc = encode_maps(p, dev_table, host, stream))) return rc;
+    p->any_host = std::find(host.begin(), host.end(), 1) != host.end();
+    p->dev_ptrs = std::move(dev_table);
     p->ptr_cache = std::move(table);
     ++p->ptr_version;
     p->ptr_cache_valid = true;

@@ -160,7 +160,6 @@ struct reshard_plan {
   void *d_maps = nullptr;      // one 128-byte CUtensorMap per slab (64-byte aligned)
   int32_t *d_map_ok = nullptr; // 1 where the slab's map could be encoded
   int32_t *d_status = nullptr; // device-side status word (bit 0: a TMA wait timed out)
-  std::vector<uint64_t> map_ptr_cache;  // pointers the maps were encoded for
   // copy items split by alignment for the current pointers: cls_idx[set] lists the items that
   // are 16-byte aligned everywhere first (n_aligned of them), then the rest
   std::vector<int32_t> cls_idx[reshard::kNumSets];
@@ -176,7 +175,9 @@ struct reshard_plan {
   int64_t *d_mem_off = nullptr;
   uint64_t *d_ptrs = nullptr;
   void *d_workspace = nullptr;
-  std::vector<uint64_t> ptr_cache;
+  std::vector<uint64_t> ptr_cache;  // the caller's pointers of the last execute
+  std::vector<uint64_t> dev_ptrs;   // ... as the kernels see them (host memory by its device alias)
+  bool any_host = false;            // some pointer is page-locked host memory
   bool ptr_cache_valid = false;
 };
 

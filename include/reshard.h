@@ -174,8 +174,14 @@ int reshard_plan_blockwise_fp8(const reshard_tensor_spec_t *specs, int n_tensors
 
 /*
  * reshard_execute -- enqueue the reshard on `stream` and return (asynchronous).
- * src_ptrs / dst_ptrs: HOST arrays of DEVICE pointers, caller-owned, laid out as above. A rank
- *   whose shard is empty may pass NULL. Under RESHARD_QUANT_MXFP8 dst_ptrs holds two entries
+ * src_ptrs / dst_ptrs: HOST arrays of pointers, caller-owned, laid out as above. A rank whose
+ *   shard is empty may pass NULL. Each pointer is memory of the plan's device, managed memory,
+ *   or page-locked host memory mapped into the device's address space (cudaHostAlloc,
+ *   cudaMallocHost, cudaHostRegister). The kernels read and write host memory in place over
+ *   the host link, so a host-to-host reshard needs no staging copies in device memory; the
+ *   transposing regions then read it with plain loads instead of TMA. Pageable host memory
+ *   and another device's memory are refused (INVALID_ARG, naming up to eight pointers); the
+ *   check (cudaPointerGetAttributes per pointer) runs whenever the pointers change. Under RESHARD_QUANT_MXFP8 dst_ptrs holds two entries
  *   per destination rank: the E4M3 data buffer (1 byte per element, dense row-major of the
  *   local shape, at element offset offset_elems) and the E8M0 scale buffer (1 byte per 32
  *   elements, row-major [..., K_local / 32], at offset_elems / 32).
@@ -191,7 +197,8 @@ int reshard_plan_blockwise_fp8(const reshard_tensor_spec_t *specs, int n_tensors
  * walker): host work proportional to the plan's items, none when the pointers repeat.
  * Buffers must stay valid until the stream reaches the end of the work. Executes of one plan
  * on different streams that overlap in time race on its tables and workspace.
- * Errors: INVALID_ARG (NULL pointer for a non-empty shard, other device), UNSUPPORTED,
+ * Errors: INVALID_ARG (NULL pointer for a non-empty shard, a pointer the device cannot
+ *   dereference, plan bound to another device), UNSUPPORTED,
  *   CUDA (launch or copy failure), OOM. After an error the destinations are undefined.
  */
 int reshard_execute(reshard_plan_t *plan, void *const *src_ptrs, void *const *dst_ptrs, int mode,
@@ -212,8 +219,11 @@ int reshard_execute(reshard_plan_t *plan, void *const *src_ptrs, void *const *ds
  * device current; make that first call before any stream capture. Calls on one device share the
  * array and it keeps the last call's contents (nothing in it needs to start at zero): calls that
  * overlap on the GPU race, so serialise them (for example, all on one stream).
- * Arguments as in reshard_execute (one destination pointer per rank). The plan is only read and
- * is not bound to a device; plans with transposing regions are UNSUPPORTED here (their tensor
+ * Arguments as in reshard_execute (one destination pointer per rank), except that the pointers
+ * reach the kernel as given, unchecked: device memory of the current device, managed memory, or
+ * page-locked host memory whose device address equals its host address (cudaHostAlloc and
+ * cudaMallocHost memory under unified addressing). The plan is only read and is not bound to a
+ * device; plans with transposing regions are UNSUPPORTED here (their tensor
  * maps live with the plan). Errors: INVALID_ARG (NULL plan or pointer of a non-empty shard);
  * UNSUPPORTED when the tables need more than RESHARD_STATIC_SCRATCH_BYTES (the message gives the
  * size; split the batch or use reshard_execute); CUDA. Calls no cudaMalloc or cudaFree.

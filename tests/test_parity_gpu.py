@@ -276,3 +276,61 @@ def test_execute_replays_from_a_cuda_graph():
     g.replay()
     torch.cuda.synchronize()
     assert_matches_oracle(wl, lay)
+
+
+def _pinned_like(t, fill=None):
+    h = torch.empty(t.numel(), dtype=t.dtype, pin_memory=True)
+    if fill is None:
+        h.copy_(t)
+    else:
+        h.fill_(fill)
+    return h
+
+
+HOST_CASES = {
+    "dense": lambda: S.dense_ffn(layers=1, hidden=256, ffn=1000),
+    "transposed": lambda: S.transposed(shape=(300, 256), src_mesh=(4,), src_pl=("S0",)),
+    "moe_tp4_mxfp8": lambda: S.moe_experts(layers=1, experts=16, hidden=256, ffn=128, dst="tp4"),
+    "many_small": lambda: S.many_small(n=20),
+}
+
+
+@pytest.mark.parametrize("where", ["host_host", "host_dev", "dev_host"])
+@pytest.mark.parametrize("mode", ["direct", "packed"])
+@pytest.mark.parametrize("name", sorted(HOST_CASES))
+def test_page_locked_host_buffers(name, mode, where):
+    """Sources and/or destinations in page-locked host memory: the kernels read and write it in
+    place (transposing regions through plain loads, not TMA); bytes equal the oracle's."""
+    import dataclasses
+    wl = HOST_CASES[name]()
+    lay, _ = run_gpu(wl, execute=False, misalign=2 if name == "many_small" else 0)
+    kw = {}
+    if where in ("host_host", "host_dev"):
+        kw["src_slab"] = _pinned_like(lay.src_slab)
+    if where in ("host_host", "dev_host"):
+        kw["dst_slab"] = _pinned_like(lay.dst_slab, 0xA5)
+        if lay.scale_slab is not None:
+            kw["scale_slab"] = _pinned_like(lay.scale_slab, 0xA5)
+    hl = dataclasses.replace(lay, **kw)
+    plan = R.plan_workload(wl)
+    sp, dp = R.workload_pointers(wl, hl)
+    R.reshard_execute(plan, sp, dp, mode=mode, quant=wl.quant, stream=torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert R.reshard_plan_status(plan) == 0
+    assert_matches_oracle(wl, hl)
+
+
+def test_pageable_host_memory_is_refused_before_any_launch():
+    wl = S.dense_ffn(layers=1, hidden=256, ffn=1000)
+    lay, plan = run_gpu(wl, execute=False)
+    pageable = torch.empty(lay.src_slab.numel(), dtype=torch.uint8)   # not page-locked
+    import dataclasses
+    sp, dp = R.workload_pointers(wl, dataclasses.replace(lay, src_slab=pageable))
+    with pytest.raises(R.ReshardError) as e:
+        R.reshard_execute(plan, sp, dp)
+    assert e.value.code == R.RESHARD_ERR_INVALID_ARG and "pageable" in str(e.value)
+    # the plan stays usable with valid pointers afterwards
+    sp, dp = R.workload_pointers(wl, lay)
+    R.reshard_execute(plan, sp, dp, stream=torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert_matches_oracle(wl, lay)
