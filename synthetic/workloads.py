@@ -313,6 +313,25 @@ def transposed(shape=(14336, 4096), src_mesh=(8,), src_pl=("S0",), dst_mesh=(2, 
     return _size_buffers(Workload(name, ts), nsb, ndb)
 
 
+def large_offsets(rows: int = 65536, cols: int = 49152, seed: int = 9, transposing: bool = True) -> Workload:
+    """Buffers of more than 2^31 elements on both sides, so that element offsets need 64 bits:
+    one replica into a 2-way column split, a 2-way column split back into one replica, and
+    (``transposing``) a 2-way row split into one column-major replica."""
+    ts = [
+        TensorDesc("rep_to_tp2", (rows, cols), "bf16", (1,), ("R",), (2,), ("S1",),
+                   _dense_views(1, 0), _dense_views(2, 0), seed=seed, std=1.0),
+        TensorDesc("tp2_to_rep", (rows, cols), "bf16", (2,), ("S1",), (1,), ("R",),
+                   _dense_views(2, 1), _dense_views(1, 2), seed=seed + 1, std=1.0),
+    ]
+    nsb, ndb = 3, 3
+    if transposing:
+        ts.append(TensorDesc("tp2_to_rep_colmajor", (rows, cols), "bf16", (2,), ("S0",), (1,), ("R",),
+                             _dense_views(2, 3), _colmajor_views((rows, cols), (1,), ("R",), 3),
+                             seed=seed + 2, std=1.0))
+        nsb, ndb = 5, 4
+    return _size_buffers(Workload(f"large_offsets_{rows}x{cols}", ts), nsb, ndb)
+
+
 def qkv_kv_below_tp(layers: int = 4, q_heads: int = 64, kv_heads: int = 2, head_dim: int = 128,
                     hidden: int = 8192, tp_src: int = 8, tp_dst: int = 8, seed: int = 8, std: float = 0.02) -> Workload:
     """Fused QKV projections with fewer KV heads than TP ranks, on both sides.
@@ -537,6 +556,8 @@ WORKLOAD_NAMES = {
     "transpose_2x14336x4096_tp8_to_dp2tp2_dst_colmajor": lambda: transposed(tensors=2),
     "moe_1x128x1536x4096_ep16_to_ep8": lambda: moe_experts(layers=1, dst="ep8"),
     "moe_1x128x1536x4096_ep16_to_tp4_mxfp8": lambda: moe_experts(layers=1, dst="tp4"),
+    # buffers of more than 2^31 elements (64-bit element offsets)
+    "large_offsets_65536x49152": lambda: large_offsets(),
 }
 
 

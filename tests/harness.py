@@ -59,9 +59,10 @@ def _src_shape(t, s):
     return G.box_shape(G.shard_box(t.global_shape, t.src_mesh, t.src_placements, G.mesh_coords(t.src_mesh)[s]))
 
 
-def sampled_check(wl, lay, per_tensor=8, seed=0, max_tensors=None):
+def sampled_check(wl, lay, per_tensor=8, seed=0, max_tensors=None, corners=False):
     """Sampled parity at full size: the oracle maps each sampled destination element to the
-    source element that must supply it; the bytes must be equal (copy workloads)."""
+    source element that must supply it; the bytes must be equal (copy workloads). With
+    ``corners`` the first and last element of every destination shard are sampled too."""
     rng = np.random.Generator(np.random.PCG64(seed))
     tids = range(len(wl.tensors))
     if max_tensors and len(wl.tensors) > max_tensors:
@@ -70,12 +71,19 @@ def sampled_check(wl, lay, per_tensor=8, seed=0, max_tensors=None):
     for ti in tids:
         t = wl.tensors[ti]
         es = G.ESIZE[t.dtype]
+        picks = []
         for _ in range(per_tensor):
             r = int(rng.integers(0, t.n_dst))
             shp = _dst_shape(t, r)
             if int(np.prod(shp)) == 0:
                 continue
-            idx = tuple(int(rng.integers(0, n)) for n in shp)
+            picks.append((r, shp, tuple(int(rng.integers(0, n)) for n in shp)))
+        if corners:
+            for r in range(t.n_dst):
+                shp = _dst_shape(t, r)
+                if int(np.prod(shp)) > 0:
+                    picks += [(r, shp, tuple(0 for _ in shp)), (r, shp, tuple(n - 1 for n in shp))]
+        for r, shp, idx in picks:
             s, sidx = G.dst_element_source(t, r, idx)
             sv, dv = t.src_views[s], t.dst_views[r]
             src_off.append(lay.src_off[sv.buffer] + es * G.element_offset(sv, _src_shape(t, s), sidx))

@@ -202,7 +202,7 @@ def _full(wl_fn, mode, sampler, **kw):
 
 @pytest.mark.parametrize("mode", ["direct", "packed"])
 def test_full_dense_ffn_sampled_and_round_trip(mode):
-    wl, lay, plan = _full(S.dense_ffn, mode, sampled_check, per_tensor=64)
+    wl, lay, plan = _full(S.dense_ffn, mode, sampled_check, per_tensor=64, corners=True)
     # A -> B -> A: the destinations resharded back reproduce the (fused) sources exactly
     back = S.Workload(wl.name + ".back", [round_trip_desc(t) for t in wl.tensors],
                       src_buffer_numel=wl.dst_buffer_numel, src_buffer_dtype=wl.dst_buffer_dtype,
@@ -221,7 +221,7 @@ def test_full_dense_ffn_sampled_and_round_trip(mode):
 
 
 def test_full_moe_ep16_to_ep8_sampled():
-    _full(lambda: S.moe_experts(dst="ep8"), "direct", sampled_check, per_tensor=64)
+    _full(lambda: S.moe_experts(dst="ep8"), "direct", sampled_check, per_tensor=64, corners=True)
 
 
 @pytest.mark.parametrize("mode", ["direct", "packed"])
@@ -240,7 +240,7 @@ def test_full_edge_mix_bit_exact():
                                   "moe_w13_4x128x768x2048_per_expert_to_tp4",
                                   "moe_fp8_8x128x768x2048_dp2ep8_to_dp8tp2_b128x128"])
 def test_full_next_rows_sampled(name):
-    _full(lambda: S.workload_by_name(name), "direct", sampled_check, per_tensor=16, max_tensors=400)
+    _full(lambda: S.workload_by_name(name), "direct", sampled_check, per_tensor=16, max_tensors=400, corners=True)
 
 
 def test_full_many_small_sampled():
@@ -250,8 +250,17 @@ def test_full_many_small_sampled():
 @pytest.mark.parametrize("mode", ["direct", "packed"])
 def test_full_transposed_destination_sampled(mode):
     wl, lay, plan = _full(lambda: S.workload_by_name("transpose_32x14336x4096_tp8_to_dp2tp2_dst_colmajor"), mode,
-                          sampled_check, per_tensor=64)
+                          sampled_check, per_tensor=64, corners=True)
     assert R.reshard_plan_status(plan) == 0
+
+
+@pytest.mark.parametrize("mode", ["direct", "packed"])
+def test_full_large_offsets_sampled(mode):
+    """Buffers of 3.2e9 elements (6.4 GB) on both sides, beyond 32-bit element offsets: copy
+    items and TMA tiles far into them, and every shard's first and last element."""
+    wl, lay, plan = _full(S.large_offsets, mode, sampled_check, per_tensor=512, corners=True)
+    assert R.reshard_plan_status(plan) == 0
+    assert max(wl.src_buffer_numel) > 2 ** 31 and max(wl.dst_buffer_numel) > 2 ** 31
 
 
 @pytest.mark.parametrize("mode", ["direct", "packed"])
