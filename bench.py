@@ -256,7 +256,9 @@ def dominant_kernel(R, plan, mode: str, quant: str) -> str:
     if quant == "mxfp8":
         return "reshard_mxfp8_kernel"
     st = R.reshard_plan_stats(plan)
-    return "reshard_copy_aligned_kernel" if st["last_aligned_items"] >= st["last_general_items"] else "reshard_copy_kernel"
+    if st["last_aligned_items"] >= st["last_general_items"]:
+        return "reshard_copy_aligned_kernel"
+    return "reshard_copy_rows_kernel" if st["last_rows_kernel"] else "reshard_copy_kernel"
 
 
 def e2e_run(R, wl, plan, sp, dp, lay, args, quant, world, dev, dst_bytes, barrier, st):

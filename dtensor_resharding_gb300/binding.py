@@ -58,7 +58,7 @@ class TensorSpecT(ctypes.Structure):
 
 STATS_FIELDS = ("n_tensors", "regions", "items", "dst_groups", "messages", "bytes_read", "bytes_written",
                 "wire_bytes", "message_bytes", "gather_bcast_bytes", "global_bytes", "last_launches",
-                "last_aligned_items", "last_general_items")
+                "last_aligned_items", "last_general_items", "last_rows_kernel")
 
 
 class StatsT(ctypes.Structure):

@@ -46,10 +46,26 @@ namespace reshard {
 #ifndef RESHARD_GEN_UNROLL
 #define RESHARD_GEN_UNROLL 2
 #endif
+#ifndef RESHARD_ROWS_MIN_BLOCKS
+#define RESHARD_ROWS_MIN_BLOCKS 6
+#endif
+#ifndef RESHARD_ROWS_GEN_UNROLL
+#define RESHARD_ROWS_GEN_UNROLL 1
+#endif
+#ifndef RESHARD_ROWS_MAX_RUN
+#define RESHARD_ROWS_MAX_RUN 4096
+#endif
 constexpr int kBlock = RESHARD_BLOCK;    // threads per CTA
 constexpr int kUnroll = RESHARD_UNROLL;        // 16-byte loads in flight per thread (aligned walker)
 constexpr int kGenUnroll = RESHARD_GEN_UNROLL;  // the same in the general walker's aligned path
 constexpr int kMaxFan = 8;               // destination replicas held in registers per pass
+#ifndef RESHARD_GEN_SMEM_ITEM
+#define RESHARD_GEN_SMEM_ITEM 1
+#endif
+#ifndef RESHARD_GEN_FAN
+#define RESHARD_GEN_FAN 8
+#endif
+constexpr int kGenFan = RESHARD_GEN_FAN;  // the same in the general walker
 
 // ------------------------------------------------------------------------------ helpers --
 
@@ -150,7 +166,7 @@ __device__ __forceinline__ void store_partial(uint8_t *word, uint4 o, int kmin, 
 // ------------------------------------------------------------------- copy with fan-out --
 
 // Every source, destination, run and pitch 16-byte aligned: straight 16-byte copies.
-template <int U>
+template <int U, int NF>
 __device__ __forceinline__ void copy_aligned(const uint8_t *__restrict__ src, uint8_t *const *dst, int nf, int rows,
                                              int64_t run_b, int64_t sp_b, int64_t dp_b) {
   const int nw = (int)(run_b >> 4);
@@ -172,7 +188,7 @@ __device__ __forceinline__ void copy_aligned(const uint8_t *__restrict__ src, ui
     for (int u = 0; u < U; ++u) {
       if (base + u * kBlock < total) {
 #pragma unroll
-        for (int f = 0; f < kMaxFan; ++f)
+        for (int f = 0; f < NF; ++f)
           if (f < nf) store_stream(dst[f] + doff[u], v[u]);
       }
     }
@@ -180,6 +196,7 @@ __device__ __forceinline__ void copy_aligned(const uint8_t *__restrict__ src, ui
 }
 
 // Every source, destination, run and pitch 32-byte aligned: 32-byte copies.
+template <int NF>
 __device__ __forceinline__ void copy_aligned32(const uint8_t *__restrict__ src, uint8_t *const *dst, int nf, int rows,
                                                int64_t run_b, int64_t sp_b, int64_t dp_b) {
   const int nw = (int)(run_b >> 5);
@@ -201,99 +218,135 @@ __device__ __forceinline__ void copy_aligned32(const uint8_t *__restrict__ src, 
     for (int u = 0; u < kUnroll; ++u) {
       if (base + u * kBlock < total) {
 #pragma unroll
-        for (int f = 0; f < kMaxFan; ++f)
+        for (int f = 0; f < NF; ++f)
           if (f < nf) store_stream32(dst[f] + doff[u], va[u], vb[u]);
       }
     }
   }
 }
 
-// General alignment: destination replicas must agree modulo 16. Each thread owns aligned
-// 16-byte destination words (kShiftUnroll of them per pass, loads first), assembles each from
-// the (at most two) aligned 16-byte source blocks that hold its bytes, and stores it whole, or
-// at the two ends of a row in naturally aligned 8/4/2/1-byte pieces. A source block is loaded
-// only when it holds at least one byte of the row, so no access leaves the 16-byte blocks (and
-// hence the pages) the region occupies.
-#ifndef RESHARD_SHIFT_UNROLL
-#define RESHARD_SHIFT_UNROLL 2
+// The same funnel-shift copy with one warp per row: the row's destination misalignment, its
+// source phase and hence the shift are computed once per row, the lanes walk the row's
+// destination words, and the shift amount is warp-uniform. Word w of a row holds row bytes
+// [16 w - a, 16 w - a + 16), a the row's destination misalignment. A single-row item is cut
+// into virtual rows of kVRow bytes whose boundaries fall on destination 16-byte boundaries, so
+// that no destination word is shared by two rows.
+#ifndef RESHARD_ROW_UNROLL
+#define RESHARD_ROW_UNROLL 2
 #endif
-constexpr int kShiftUnroll = RESHARD_SHIFT_UNROLL;
+#ifndef RESHARD_VROW_PASSES
+#define RESHARD_VROW_PASSES 2
+#endif
+constexpr int kRowUnroll = RESHARD_ROW_UNROLL;
+constexpr int kVRow = 32 * 16 * kRowUnroll * RESHARD_VROW_PASSES;  // bytes per virtual row
 
 template <int NF>
-__device__ __forceinline__ void copy_shifted(const uint8_t *__restrict__ src, uint8_t *const *dst, int nf, int rows,
-                                             int64_t run_b, int64_t sp_b, int64_t dp_b) {
-  const int nwmax = (int)((run_b + 15) >> 4) + 1;  // destination words a row can touch
-  const int total = rows * nwmax;
+__device__ __forceinline__ void copy_shifted_rows(const uint8_t *__restrict__ src, uint8_t *const *dst, int nf,
+                                                  int rows, int64_t run_b, int64_t sp_b, int64_t dp_b) {
+  const int lane = threadIdx.x & 31;
   const uintptr_t d0 = reinterpret_cast<uintptr_t>(dst[0]);
-  for (int base = threadIdx.x; base < total; base += kBlock * kShiftUnroll) {
-    uint4 lo[kShiftUnroll], hi[kShiftUnroll];
-    int64_t dpos[kShiftUnroll];  // destination byte offset of the word's byte 0, from dst[f]
-    int kmin[kShiftUnroll], kmax[kShiftUnroll], sh[kShiftUnroll];
+  const int a0 = (int)(d0 & 15);
+  const bool split = rows == 1;
+  const int nrow = split ? (int)((run_b + a0 + kVRow - 1) / kVRow) : rows;
+  for (int r = threadIdx.x >> 5; r < nrow; r += kBlock / 32) {
+    int64_t sb, db, rb;  // source and destination byte offset of the row, its length
+    if (split) {
+      sb = r ? (int64_t)r * kVRow - a0 : 0;
+      const int64_t e = (int64_t)(r + 1) * kVRow - a0;
+      rb = (e < run_b ? e : run_b) - sb;
+      db = sb;
+    } else {
+      sb = r * sp_b;
+      db = r * dp_b;
+      rb = run_b;
+    }
+    const int a = (int)((d0 + db) & 15);
+    const int nw = (int)((a + rb + 15) >> 4);  // destination words the row touches
+    const uintptr_t p00 = reinterpret_cast<uintptr_t>(src) + sb - a;  // source of word 0's byte 0
+    const int sh = (int)(p00 & 15);
+    const uint8_t *blk0 = reinterpret_cast<const uint8_t *>(p00 - sh);
+    const int64_t dbase = db - a;  // destination offset of word 0's byte 0
+    for (int w0 = lane; w0 < nw; w0 += 32 * kRowUnroll) {
+      uint4 lo[kRowUnroll], hi[kRowUnroll];
+      int kmin[kRowUnroll], kmax[kRowUnroll];
 #pragma unroll
-    for (int u = 0; u < kShiftUnroll; ++u) {
-      const int j = base + u * kBlock;
-      kmin[u] = 16;
-      kmax[u] = 0;
-      sh[u] = 0;
-      dpos[u] = 0;
-      lo[u] = make_uint4(0, 0, 0, 0);
-      hi[u] = make_uint4(0, 0, 0, 0);
-      if (j < total) {
-        const int r = rows == 1 ? 0 : j / nwmax;
-        const int w = j - r * nwmax;
-        const int64_t drow = r * dp_b;
-        const int a = (int)((d0 + drow) & 15);
-        const int64_t start = 16 * (int64_t)w - a;  // row byte of this word's byte 0
-        if (start < run_b) {
-          kmin[u] = start < 0 ? (int)-start : 0;
-          kmax[u] = run_b - start < 16 ? (int)(run_b - start) : 16;
-          dpos[u] = drow + start;
-          const uintptr_t p0 = reinterpret_cast<uintptr_t>(src) + r * sp_b + start;
-          sh[u] = (int)(p0 & 15);
-          const uint8_t *blk = reinterpret_cast<const uint8_t *>(p0 - sh[u]);
-          if (kmin[u] < 16 - sh[u]) lo[u] = __ldg(reinterpret_cast<const uint4 *>(blk));
-          if (sh[u] && kmax[u] > 16 - sh[u]) hi[u] = __ldg(reinterpret_cast<const uint4 *>(blk + 16));
+      for (int u = 0; u < kRowUnroll; ++u) {
+        const int w = w0 + 32 * u;
+        kmin[u] = 16;
+        kmax[u] = 0;
+        lo[u] = make_uint4(0, 0, 0, 0);
+        hi[u] = make_uint4(0, 0, 0, 0);
+        if (w < nw) {
+          const int64_t start = 16 * (int64_t)w - a;
+          kmin[u] = w == 0 ? a : 0;
+          kmax[u] = rb - start < 16 ? (int)(rb - start) : 16;
+          const uint8_t *blk = blk0 + 16 * (int64_t)w;
+          if (kmin[u] < 16 - sh) lo[u] = __ldg(reinterpret_cast<const uint4 *>(blk));
+          if (sh && kmax[u] > 16 - sh) hi[u] = __ldg(reinterpret_cast<const uint4 *>(blk + 16));
         }
       }
-    }
 #pragma unroll
-    for (int u = 0; u < kShiftUnroll; ++u) {
-      if (kmin[u] >= kmax[u]) continue;
-      const uint4 o = sh[u] ? shift_bytes(lo[u], hi[u], sh[u]) : lo[u];
-      if (kmin[u] == 0 && kmax[u] == 16) {
+      for (int u = 0; u < kRowUnroll; ++u) {
+        if (kmin[u] >= kmax[u]) continue;
+        const uint4 o = sh ? shift_bytes(lo[u], hi[u], sh) : lo[u];
+        const int64_t dpos = dbase + 16 * (int64_t)(w0 + 32 * u);
+        if (kmin[u] == 0 && kmax[u] == 16) {
 #pragma unroll
-        for (int f = 0; f < NF; ++f)
-          if (f < nf) store_stream(dst[f] + dpos[u], o);
-      } else {
+          for (int f = 0; f < NF; ++f)
+            if (f < nf) store_stream(dst[f] + dpos, o);
+        } else {
 #pragma unroll
-        for (int f = 0; f < NF; ++f)
-          if (f < nf) store_partial(dst[f] + dpos[u], o, kmin[u], kmax[u]);
+          for (int f = 0; f < NF; ++f)
+            if (f < nf) store_partial(dst[f] + dpos, o, kmin[u], kmax[u]);
+        }
       }
     }
   }
 }
 
 // dst[f] for a runtime f without indexing the array (keeps it in registers).
+template <int NF>
 __device__ __forceinline__ uint8_t *pick(uint8_t *const *dst, int f) {
   uint8_t *p = dst[0];
 #pragma unroll
-  for (int g = 1; g < kMaxFan; ++g) p = f == g ? dst[g] : p;
+  for (int g = 1; g < NF; ++g) p = f == g ? dst[g] : p;
   return p;
 }
 
 // Resolve item k of a launch: items[idx[k]] when an index list is given, else items[k].
 __device__ __forceinline__ int item_index(const int32_t *idx, int k) { return idx ? idx[k] : k; }
 
-// The general walker: aligned, 32-byte-aligned and funnel-shift paths, any item.
-__global__ void __launch_bounds__(kBlock, RESHARD_GEN_MIN_BLOCKS) reshard_copy_kernel(
-    const Item *__restrict__ items, const int32_t *__restrict__ idx, int n_items, const uint64_t *__restrict__ ptrs,
-    const int32_t *__restrict__ gstart, const int32_t *__restrict__ mptr, const int64_t *__restrict__ moff) {
+// The general walker: aligned, 32-byte-aligned and funnel-shift paths, any item. GU is the
+// unroll of its aligned path (which serves items found misaligned after all, and every item of
+// the allocation-free entry point).
+template <int GU>
+__device__ __forceinline__ void general_walk(const Item *__restrict__ items, const int32_t *__restrict__ idx,
+                                             int n_items, const uint64_t *__restrict__ ptrs,
+                                             const int32_t *__restrict__ gstart, const int32_t *__restrict__ mptr,
+                                             const int64_t *__restrict__ moff) {
+#if RESHARD_GEN_SMEM_ITEM
+  // item descriptors double-buffered in shared memory: 16 threads fetch the next one while the
+  // current one is copied, so no thread holds a prefetched descriptor in registers
+  __shared__ Item s_item[2];
+  constexpr int kWords = (int)(sizeof(Item) / sizeof(uint32_t));
+  if (threadIdx.x < kWords && blockIdx.x < n_items)
+    reinterpret_cast<uint32_t *>(&s_item[0])[threadIdx.x] =
+        __ldg(reinterpret_cast<const uint32_t *>(items + item_index(idx, blockIdx.x)) + threadIdx.x);
+  __syncthreads();
+  int buf = 0;
+  for (int k = blockIdx.x; k < n_items; k += gridDim.x, buf ^= 1) {
+    if (threadIdx.x < kWords && k + (int)gridDim.x < n_items)
+      reinterpret_cast<uint32_t *>(&s_item[buf ^ 1])[threadIdx.x] =
+          __ldg(reinterpret_cast<const uint32_t *>(items + item_index(idx, k + gridDim.x)) + threadIdx.x);
+    const Item &it = s_item[buf];
+#else
   Item nxt;
   if (blockIdx.x < n_items) nxt = items[item_index(idx, blockIdx.x)];
   for (int k = blockIdx.x; k < n_items; k += gridDim.x) {
     const Item it = nxt;
     // the next item's descriptor is in flight while this one is copied
     if (k + (int)gridDim.x < n_items) nxt = items[item_index(idx, k + gridDim.x)];
+#endif
     const int64_t es = it.esize;
     const uint8_t *src = reinterpret_cast<const uint8_t *>(ptrs[it.src]) + it.src_off * es;
     const int g0 = gstart[it.group];
@@ -302,13 +355,13 @@ __global__ void __launch_bounds__(kBlock, RESHARD_GEN_MIN_BLOCKS) reshard_copy_k
     const int64_t sp_b = it.src_pitch * es, dp_b = it.dst_pitch * es;
     const uintptr_t geo = reinterpret_cast<uintptr_t>(src) | (uintptr_t)run_b |
                           (it.rows > 1 ? (uintptr_t)(sp_b | dp_b) : 0);
-    for (int f0 = 0; f0 < nrep; f0 += kMaxFan) {
-      const int nf = min(kMaxFan, nrep - f0);
-      uint8_t *dst[kMaxFan];
+    for (int f0 = 0; f0 < nrep; f0 += kGenFan) {
+      const int nf = min(kGenFan, nrep - f0);
+      uint8_t *dst[kGenFan];
       uintptr_t amask = geo;
       bool same = true;
 #pragma unroll
-      for (int f = 0; f < kMaxFan; ++f) {
+      for (int f = 0; f < kGenFan; ++f) {
         dst[f] = nullptr;
         if (f < nf) {
           const int m = g0 + f0 + f;
@@ -318,20 +371,38 @@ __global__ void __launch_bounds__(kBlock, RESHARD_GEN_MIN_BLOCKS) reshard_copy_k
         }
       }
       if (RESHARD_WIDE && (amask & 31) == 0) {
-        copy_aligned32(src, dst, nf, it.rows, run_b, sp_b, dp_b);
+        copy_aligned32<kGenFan>(src, dst, nf, it.rows, run_b, sp_b, dp_b);
       } else if ((amask & 15) == 0) {
-        copy_aligned<kGenUnroll>(src, dst, nf, it.rows, run_b, sp_b, dp_b);
+        copy_aligned<GU, kGenFan>(src, dst, nf, it.rows, run_b, sp_b, dp_b);
       } else if (same && nf <= 2) {
-        copy_shifted<2>(src, dst, nf, it.rows, run_b, sp_b, dp_b);
+        copy_shifted_rows<2>(src, dst, nf, it.rows, run_b, sp_b, dp_b);
       } else {
         // replicas differ modulo 16 (or many of them): one replica per pass
         for (int f = 0; f < nf; ++f) {
-          uint8_t *one[1] = {pick(dst, f)};
-          copy_shifted<1>(src, one, 1, it.rows, run_b, sp_b, dp_b);
+          uint8_t *one[1] = {pick<kGenFan>(dst, f)};
+          copy_shifted_rows<1>(src, one, 1, it.rows, run_b, sp_b, dp_b);
         }
       }
     }
+#if RESHARD_GEN_SMEM_ITEM
+    __syncthreads();  // everyone is done with s_item[buf]; s_item[buf ^ 1] is complete
+#endif
   }
+}
+
+// Two builds of the general walker. reshard_copy_kernel (4 CTAs/SM) suits long single-row
+// items; reshard_copy_rows_kernel (6 CTAs/SM, fewer registers) suits items of many short rows,
+// where one warp walks one row and more resident warps hide more load latency.
+__global__ void __launch_bounds__(kBlock, RESHARD_GEN_MIN_BLOCKS) reshard_copy_kernel(
+    const Item *__restrict__ items, const int32_t *__restrict__ idx, int n_items, const uint64_t *__restrict__ ptrs,
+    const int32_t *__restrict__ gstart, const int32_t *__restrict__ mptr, const int64_t *__restrict__ moff) {
+  general_walk<kGenUnroll>(items, idx, n_items, ptrs, gstart, mptr, moff);
+}
+
+__global__ void __launch_bounds__(kBlock, RESHARD_ROWS_MIN_BLOCKS) reshard_copy_rows_kernel(
+    const Item *__restrict__ items, const int32_t *__restrict__ idx, int n_items, const uint64_t *__restrict__ ptrs,
+    const int32_t *__restrict__ gstart, const int32_t *__restrict__ mptr, const int64_t *__restrict__ moff) {
+  general_walk<RESHARD_ROWS_GEN_UNROLL>(items, idx, n_items, ptrs, gstart, mptr, moff);
 }
 
 // The aligned walker: items the host found 16-byte aligned everywhere (sources, every replica,
@@ -369,7 +440,7 @@ __global__ void __launch_bounds__(kBlock, RESHARD_MIN_BLOCKS) reshard_copy_align
         }
       }
       if ((amask & 15) == 0) {
-        copy_aligned<kUnroll>(src, dst, nf, it.rows, run_b, sp_b, dp_b);
+        copy_aligned<kUnroll, kMaxFan>(src, dst, nf, it.rows, run_b, sp_b, dp_b);
       } else if (threadIdx.x == 0) {
         atomicOr(status, 2);
       }
@@ -931,6 +1002,7 @@ struct LaunchCaps {
   int bulk_grid = 0;
   int aligned_grid = 0;
   int copy_grid = 0;
+  int rows_grid = 0;
   int mxfp8_grid = 0;
   int transpose_grid = 0;
 };
@@ -941,7 +1013,7 @@ int launch_caps(int device, LaunchCaps &c) {
     c = g_caps;
     return RESHARD_OK;
   }
-  int sms = 0, b0 = 0, b1 = 0, b2 = 0, b3 = 0;
+  int sms = 0, b0 = 0, b1 = 0, b2 = 0, b3 = 0, b4 = 0;
   RS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device));
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, reshard_copy_aligned_kernel, kBlock, 0));
   int bb = 0;
@@ -950,12 +1022,14 @@ int launch_caps(int device, LaunchCaps &c) {
     RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bb, reshard_bulk_kernel, 32, kBulkSmem));
   }
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, reshard_copy_kernel, kBlock, 0));
+  RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b4, reshard_copy_rows_kernel, kBlock, 0));
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b2, reshard_mxfp8_kernel, kQBlock, 0));
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b3, reshard_transpose_kernel, kTBlock, 0));
   g_caps.device = device;
   g_caps.aligned_grid = sms * std::max(1, b0);
   g_caps.bulk_grid = sms * std::max(1, bb);
   g_caps.copy_grid = sms * std::max(1, b1);
+  g_caps.rows_grid = sms * std::max(1, b4);
   g_caps.mxfp8_grid = sms * std::max(1, b2);
   g_caps.transpose_grid = sms * std::max(1, b3);
   c = g_caps;
@@ -1118,6 +1192,7 @@ int classify(reshard_plan_t *p, int set, cudaStream_t stream) {
   idx.clear();
   idx.reserve(items.size());
   std::vector<int32_t> general;
+  int64_t gen_bytes = 0, row_bytes = 0;
   for (size_t i = 0; i < items.size(); ++i) {
     const Item &it = items[i];
     const uint64_t es = (uint64_t)it.esize;
@@ -1126,12 +1201,18 @@ int classify(reshard_plan_t *p, int set, cudaStream_t stream) {
     if (it.rows > 1) m |= (uint64_t)it.src_pitch * es | (uint64_t)it.dst_pitch * es;
     for (int32_t k = p->grp_start[(size_t)it.group]; k < p->grp_start[(size_t)it.group + 1]; ++k)
       m |= tab[(size_t)p->mem_ptr[(size_t)k]] + (uint64_t)(p->mem_off[(size_t)k] + it.dst_off) * es;
-    if ((m & 15) == 0)
+    if ((m & 15) == 0) {
       idx.push_back((int32_t)i);
-    else
+    } else {
       general.push_back((int32_t)i);
+      const int64_t b = (int64_t)it.rows * it.run * (int64_t)es;
+      gen_bytes += b;
+      if (it.rows > 1 && (int64_t)it.run * (int64_t)es < RESHARD_ROWS_MAX_RUN) row_bytes += b;
+    }
   }
   p->n_aligned[set] = (int32_t)idx.size();
+  // the general items run in the many-rows build when most of their bytes are short rows
+  p->gen_rows[set] = 2 * row_bytes > gen_bytes;
   idx.insert(idx.end(), general.begin(), general.end());
   if (!p->d_cls_idx[set] && !idx.empty())
     RS_CUDA(cudaMalloc(reinterpret_cast<void **>(&p->d_cls_idx[set]), idx.size() * sizeof(int32_t)));
@@ -1171,7 +1252,12 @@ int launch(reshard_plan_t *p, int set, bool quant, cudaStream_t stream, const La
           items, idx, na, p->d_ptrs, p->d_grp_start, p->d_mem_ptr, p->d_mem_off, p->d_status);
       ++p->last_launches;
     }
-    if (ng > 0) {
+    p->last_rows_kernel = ng > 0 && p->gen_rows[set];
+    if (ng > 0 && p->gen_rows[set]) {
+      reshard_copy_rows_kernel<<<std::min(ng, caps.rows_grid), kBlock, 0, stream>>>(
+          items, idx + na, ng, p->d_ptrs, p->d_grp_start, p->d_mem_ptr, p->d_mem_off);
+      ++p->last_launches;
+    } else if (ng > 0) {
       reshard_copy_kernel<<<std::min(ng, caps.copy_grid), kBlock, 0, stream>>>(
           items, idx + na, ng, p->d_ptrs, p->d_grp_start, p->d_mem_ptr, p->d_mem_off);
       ++p->last_launches;

@@ -730,6 +730,7 @@ extern "C" int reshard_plan_stats(const reshard_plan_t *plan, reshard_stats_t *o
   out->last_launches = plan->last_launches;
   out->last_aligned_items = plan->last_aligned;
   out->last_general_items = plan->last_general;
+  out->last_rows_kernel = plan->last_rows_kernel;
   return RESHARD_OK;
 }
 

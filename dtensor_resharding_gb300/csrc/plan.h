@@ -170,6 +170,8 @@ struct reshard_plan {
   int64_t last_launches = 0; // kernel launches enqueued by the last execute
   int64_t last_aligned = 0;  // copy items of the last pass that took the aligned walker
   int64_t last_general = 0;  // ... and the general walker
+  int64_t last_rows_kernel = 0;  // 1 when those ran in the many-rows build of the general walker
+  bool gen_rows[reshard::kNumSets] = {false, false, false};  // general items mostly short rows
   int32_t *d_grp_start = nullptr;
   int32_t *d_mem_ptr = nullptr;
   int64_t *d_mem_off = nullptr;

@@ -137,6 +137,8 @@ typedef struct {
   int64_t last_launches;      /* kernel launches enqueued by the plan's last execute */
   int64_t last_aligned_items; /* copy items of its last pass run by the aligned walker ... */
   int64_t last_general_items; /* ... and by the general (unaligned-capable) walker */
+  int64_t last_rows_kernel;   /* 1 if those ran in its many-short-rows build
+                                 (reshard_copy_rows_kernel), 0 if in reshard_copy_kernel */
 } reshard_stats_t;
 
 /*

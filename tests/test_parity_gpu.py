@@ -343,3 +343,18 @@ def test_pageable_host_memory_is_refused_before_any_launch():
     R.reshard_execute(plan, sp, dp, stream=torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     assert_matches_oracle(wl, lay)
+
+
+def test_general_walker_build_follows_the_item_shapes():
+    """Misaligned items of many short rows run in reshard_copy_rows_kernel; misaligned single
+    long rows in reshard_copy_kernel. Both are bit-exact."""
+    wl = S.mesh2d_to_1d(rows=512, cols=4096, variant="1d")      # destination pitch 2732 bytes
+    lay, plan = run_gpu(wl)
+    st = R.reshard_plan_stats(plan)
+    assert st["last_general_items"] > 0 and st["last_rows_kernel"] == 1
+    assert_matches_oracle(wl, lay)
+    wl = S.dense_ffn(layers=1, hidden=256, ffn=1000)               # contiguous runs, shifted by 2
+    lay, plan = run_gpu(wl, misalign=2)
+    st = R.reshard_plan_stats(plan)
+    assert st["last_general_items"] > 0 and st["last_rows_kernel"] == 0
+    assert_matches_oracle(wl, lay)
