@@ -37,6 +37,30 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def copy_rate_same_run(dev, nbytes: int = 4 << 30, reps: int = 10) -> float:
+    """The box's device-to-device copy rate, re-measured in this run: read + write bytes per
+    second of a torch copy between two 4 GiB buffers (far above the 129 MB L2), CUDA events."""
+    import torch
+    a = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    b = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    a.fill_(1)
+    s = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            b.copy_(a)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(s)
+        for _ in range(reps):
+            b.copy_(a)
+        t1.record(s)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / reps
+    del a, b
+    torch.cuda.empty_cache()
+    return 2 * nbytes / (ms / 1e3) / 1e9
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for f in ("execute.cu", "plan.h"):
@@ -417,6 +441,9 @@ def our_arm(args, rank: int, world: int, local_rank: int) -> None:
                 "launch_ms_min": round(min(per), 4), "launch_ms_max": round(max(per), 4)}
     if args.mode == "packed":
         roofline["note"] = "packed mode: step = pack + unpack launches; achieved counts the unpack bytes only"
+    same = copy_rate_same_run(dev)
+    roofline["copy_rate_same_run"] = round(same, 1)
+    roofline["frac_of_same_run_copy"] = round(achieved / same, 4)
 
     # the other mode on the same inputs, for context
     other = "packed" if args.mode == "direct" else "direct"
