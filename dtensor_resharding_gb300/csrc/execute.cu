@@ -469,7 +469,6 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-__device__ __forceinline__ uint32_t mag_max2(uint32_t w) { return max(w & 0x7FFFu, (w >> 16) & 0x7FFFu); }
 
 #ifndef RESHARD_MXFP8_UNROLL
 #define RESHARD_MXFP8_UNROLL 2
@@ -483,6 +482,9 @@ __device__ __forceinline__ uint32_t mag_max2(uint32_t w) { return max(w & 0x7FFF
 #ifndef RESHARD_MXFP8_ELEMS
 #define RESHARD_MXFP8_ELEMS 16
 #endif
+#ifndef RESHARD_MXFP8_FAN
+#define RESHARD_MXFP8_FAN 2
+#endif
 #ifndef RESHARD_MXFP8_WIDE
 #define RESHARD_MXFP8_WIDE 1
 #endif
@@ -491,18 +493,40 @@ constexpr int kQUnroll = RESHARD_MXFP8_UNROLL;  // lane slots in flight per thre
 constexpr int kQE = RESHARD_MXFP8_ELEMS;        // BF16 elements per lane slot (8 or 16)
 constexpr int kQV = kQE / 8;                    // 16-byte loads per slot
 constexpr int kQLanes = 32 / kQE;               // lanes sharing one 32-element block
-constexpr int kQMaxFan = 4;                     // replicas per pass (pointer pairs in registers)
+constexpr int kQMaxFan = RESHARD_MXFP8_FAN;      // replicas per pass (pointer pairs in registers)
 static_assert(kQE == 8 || kQE == 16, "a lane holds 8 or 16 elements of a 32-element block");
+
+// Per-halfword unsigned max of two packed 16-bit pairs.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Largest BF16 magnitude (15-bit pattern) among the 8 values of a 16-byte load, folded into
+// the running packed maximum `m` (two halfword lanes, combined by amax_of).
+__device__ __forceinline__ uint32_t fold_mag8(uint32_t m, uint4 v) {
+  m = max_u16x2(m, v.x & 0x7FFF7FFFu);
+  m = max_u16x2(m, v.y & 0x7FFF7FFFu);
+  m = max_u16x2(m, v.z & 0x7FFF7FFFu);
+  return max_u16x2(m, v.w & 0x7FFF7FFFu);
+}
+
+__device__ __forceinline__ uint32_t amax_of(uint32_t m) { return max(m & 0xFFFFu, m >> 16); }
+
+// Quantize 8 BF16 values (one 16-byte load) by 2^-X, `inv` = 2^-X of the block.
+__device__ __forceinline__ uint2 quantize8_by(uint4 v, float inv) {
+  uint2 q;
+  q.x = cvt_e4m3x2(bf16_lo(v.x) * inv, bf16_hi(v.x) * inv) | (cvt_e4m3x2(bf16_lo(v.y) * inv, bf16_hi(v.y) * inv) << 16);
+  q.y = cvt_e4m3x2(bf16_lo(v.z) * inv, bf16_hi(v.z) * inv) | (cvt_e4m3x2(bf16_lo(v.w) * inv, bf16_hi(v.w) * inv) << 16);
+  return q;
+}
 
 // Quantize 8 BF16 values (one 16-byte load) under the block amax shared by its lanes.
 __device__ __forceinline__ uint2 quantize8(uint4 v, uint32_t amax) {
   if (amax >= 0x7F80u) return make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);  // Inf/NaN block: E4M3 NaN
   const int x = block_exponent(amax);
-  const float inv = __uint_as_float((uint32_t)(127 - x) << 23);  // 2^-X, X in [-127, 119]
-  uint2 q;
-  q.x = cvt_e4m3x2(bf16_lo(v.x) * inv, bf16_hi(v.x) * inv) | (cvt_e4m3x2(bf16_lo(v.y) * inv, bf16_hi(v.y) * inv) << 16);
-  q.y = cvt_e4m3x2(bf16_lo(v.z) * inv, bf16_hi(v.z) * inv) | (cvt_e4m3x2(bf16_lo(v.w) * inv, bf16_hi(v.w) * inv) << 16);
-  return q;
+  return quantize8_by(v, __uint_as_float((uint32_t)(127 - x) << 23));  // 2^-X, X in [-127, 119]
 }
 
 // E8M0 byte of a block: 0xFF (NaN) when the block holds Inf/NaN, else X + 127.
@@ -555,8 +579,16 @@ __global__ void __launch_bounds__(kQBlock, RESHARD_MXFP8_MIN_BLOCKS) reshard_mxf
         }
       }
       const bool stv = (amask & (kQE - 1)) == 0;  // one kQE-byte store per slot
+      // slot j of the item is (row j / per_row, lane slot j % per_row); each pass advances every
+      // slot of this thread by kStride, so (row, slot) step by a quotient and remainder taken
+      // once per item instead of a division per slot
+      constexpr int kStride = kQBlock * kQUnroll;
+      const int q_step = kStride / per_row, r_step = kStride - q_step * per_row;
+      const int q_blk = kQBlock / per_row, r_blk = kQBlock - q_blk * per_row;  // slot u + 1 from slot u
+      int row0 = (int)threadIdx.x / per_row;
+      int col0 = (int)threadIdx.x - row0 * per_row;
       // j0 is warp-uniform, so every lane takes part in every shuffle
-      for (int j0 = threadIdx.x - lane; j0 < total; j0 += kQBlock * kQUnroll) {
+      for (int j0 = threadIdx.x - lane; j0 < total; j0 += kStride) {
         uint4 v[kQUnroll][kQV];
         int64_t eoff[kQUnroll];  // element offset of this slot's first value within the item
 #pragma unroll
@@ -565,9 +597,17 @@ __global__ void __launch_bounds__(kQBlock, RESHARD_MXFP8_MIN_BLOCKS) reshard_mxf
 #pragma unroll
           for (int k = 0; k < kQV; ++k) v[u][k] = make_uint4(0, 0, 0, 0);
           eoff[u] = -1;
+          int r = row0, o = col0;
+#pragma unroll
+          for (int w = 0; w < u; ++w) {
+            o += r_blk;
+            r += q_blk;
+            if (o >= per_row) {
+              o -= per_row;
+              ++r;
+            }
+          }
           if (j < total) {
-            const int r = it.rows == 1 ? 0 : j / per_row;
-            const int o = j - r * per_row;
             const uint8_t *p = src + r * sp_b + 2 * kQE * (int64_t)o;
             eoff[u] = r * it.dst_pitch + kQE * (int64_t)o;
             if (RESHARD_MXFP8_WIDE && kQV == 2 && vec32) {
@@ -578,20 +618,29 @@ __global__ void __launch_bounds__(kQBlock, RESHARD_MXFP8_MIN_BLOCKS) reshard_mxf
             }
           }
         }
+        col0 += r_step;
+        row0 += q_step;
+        if (col0 >= per_row) {
+          col0 -= per_row;
+          ++row0;
+        }
 #pragma unroll
         for (int u = 0; u < kQUnroll; ++u) {
-          uint32_t amax = 0;
+          uint32_t m = 0;
 #pragma unroll
-          for (int k = 0; k < kQV; ++k)
-            amax = max(amax, max(max(mag_max2(v[u][k].x), mag_max2(v[u][k].y)),
-                                 max(mag_max2(v[u][k].z), mag_max2(v[u][k].w))));
+          for (int k = 0; k < kQV; ++k) m = fold_mag8(m, v[u][k]);
+          uint32_t amax = amax_of(m);
 #pragma unroll
           for (int s = 1; s < kQLanes; s <<= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, s));
           if (eoff[u] < 0) continue;
           uint2 q[kQV];
+          const bool special = amax >= 0x7F80u;  // Inf/NaN in the block: E4M3 NaN, scale NaN
+          const int x = block_exponent(amax);
+          const float inv = __uint_as_float((uint32_t)(127 - x) << 23);  // 2^-X, X in [-127, 119]
 #pragma unroll
-          for (int k = 0; k < kQV; ++k) q[k] = quantize8(v[u][k], amax);
-          const uint32_t sbyte = scale_byte(amax);
+          for (int k = 0; k < kQV; ++k)
+            q[k] = special ? make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu) : quantize8_by(v[u][k], inv);
+          const uint32_t sbyte = special ? 0xFFu : (uint32_t)(x + 127);
 #pragma unroll
           for (int f = 0; f < kQMaxFan; ++f) {
             if (f < nf) {
