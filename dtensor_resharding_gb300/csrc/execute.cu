@@ -171,18 +171,34 @@ __device__ __forceinline__ void copy_aligned(const uint8_t *__restrict__ src, ui
                                              int64_t run_b, int64_t sp_b, int64_t dp_b) {
   const int nw = (int)(run_b >> 4);
   const int total = rows * nw;
+  // word j is (row j / nw, word j % nw); consecutive slots of a thread are kBlock apart and its
+  // passes kBlock * U apart, so (row, word) step by quotients and remainders taken once
+  const int q_blk = kBlock / nw, r_blk = kBlock - q_blk * nw;
+  const int q_pass = (kBlock * U) / nw, r_pass = kBlock * U - q_pass * nw;
+  int row0 = (int)threadIdx.x / nw, col0 = (int)threadIdx.x - row0 * nw;
   for (int base = threadIdx.x; base < total; base += kBlock * U) {
     uint4 v[U];
     int64_t doff[U];
+    int r = row0, w = col0;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int j = base + u * kBlock;
       if (j < total) {
-        const int r = rows == 1 ? 0 : j / nw;
-        const int w = j - r * nw;
         v[u] = load_stream(src + r * sp_b + 16 * (int64_t)w);
         doff[u] = r * dp_b + 16 * (int64_t)w;
       }
+      w += r_blk;
+      r += q_blk;
+      if (w >= nw) {
+        w -= nw;
+        ++r;
+      }
+    }
+    col0 += r_pass;
+    row0 += q_pass;
+    if (col0 >= nw) {
+      col0 -= nw;
+      ++row0;
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
