@@ -441,6 +441,10 @@ def our_arm(args, rank: int, world: int, local_rank: int) -> None:
                 "launch_ms_min": round(min(per), 4), "launch_ms_max": round(max(per), 4)}
     if args.mode == "packed":
         roofline["note"] = "packed mode: step = pack + unpack launches; achieved counts the unpack bytes only"
+    elif launches > 1:
+        roofline["note"] = (f"the step is {launches} launches (aligned walker, general walker and/or "
+                            "transposing kernel, back to back on one stream): achieved and frac cover "
+                            "the whole step; the kernel named is the one with the most items")
     same = copy_rate_same_run(dev)
     roofline["copy_rate_same_run"] = round(same, 1)
     roofline["frac_of_same_run_copy"] = round(achieved / same, 4)

@@ -253,12 +253,15 @@ __device__ __forceinline__ void copy_aligned32(const uint8_t *__restrict__ src, 
 #ifndef RESHARD_VROW_PASSES
 #define RESHARD_VROW_PASSES 2
 #endif
-constexpr int kRowUnroll = RESHARD_ROW_UNROLL;
-constexpr int kVRow = 32 * 16 * kRowUnroll * RESHARD_VROW_PASSES;  // bytes per virtual row
+#ifndef RESHARD_GEN_ROW_UNROLL
+#define RESHARD_GEN_ROW_UNROLL 3
+#endif
 
-template <int NF>
+// RU: destination words per lane in flight; a virtual row is RESHARD_VROW_PASSES passes long.
+template <int NF, int RU>
 __device__ __forceinline__ void copy_shifted_rows(const uint8_t *__restrict__ src, uint8_t *const *dst, int nf,
                                                   int rows, int64_t run_b, int64_t sp_b, int64_t dp_b) {
+  constexpr int kVRow = 32 * 16 * RU * RESHARD_VROW_PASSES;  // bytes per virtual row
   const int lane = threadIdx.x & 31;
   const uintptr_t d0 = reinterpret_cast<uintptr_t>(dst[0]);
   const int a0 = (int)(d0 & 15);
@@ -282,11 +285,11 @@ __device__ __forceinline__ void copy_shifted_rows(const uint8_t *__restrict__ sr
     const int sh = (int)(p00 & 15);
     const uint8_t *blk0 = reinterpret_cast<const uint8_t *>(p00 - sh);
     const int64_t dbase = db - a;  // destination offset of word 0's byte 0
-    for (int w0 = lane; w0 < nw; w0 += 32 * kRowUnroll) {
-      uint4 lo[kRowUnroll], hi[kRowUnroll];
-      int kmin[kRowUnroll], kmax[kRowUnroll];
+    for (int w0 = lane; w0 < nw; w0 += 32 * RU) {
+      uint4 lo[RU], hi[RU];
+      int kmin[RU], kmax[RU];
 #pragma unroll
-      for (int u = 0; u < kRowUnroll; ++u) {
+      for (int u = 0; u < RU; ++u) {
         const int w = w0 + 32 * u;
         kmin[u] = 16;
         kmax[u] = 0;
@@ -302,7 +305,7 @@ __device__ __forceinline__ void copy_shifted_rows(const uint8_t *__restrict__ sr
         }
       }
 #pragma unroll
-      for (int u = 0; u < kRowUnroll; ++u) {
+      for (int u = 0; u < RU; ++u) {
         if (kmin[u] >= kmax[u]) continue;
         const uint4 o = sh ? shift_bytes(lo[u], hi[u], sh) : lo[u];
         const int64_t dpos = dbase + 16 * (int64_t)(w0 + 32 * u);
@@ -335,7 +338,7 @@ __device__ __forceinline__ int item_index(const int32_t *idx, int k) { return id
 // The general walker: aligned, 32-byte-aligned and funnel-shift paths, any item. GU is the
 // unroll of its aligned path (which serves items found misaligned after all, and every item of
 // the allocation-free entry point).
-template <int GU>
+template <int GU, int RU>
 __device__ __forceinline__ void general_walk(const Item *__restrict__ items, const int32_t *__restrict__ idx,
                                              int n_items, const uint64_t *__restrict__ ptrs,
                                              const int32_t *__restrict__ gstart, const int32_t *__restrict__ mptr,
@@ -391,12 +394,12 @@ __device__ __forceinline__ void general_walk(const Item *__restrict__ items, con
       } else if ((amask & 15) == 0) {
         copy_aligned<GU, kGenFan>(src, dst, nf, it.rows, run_b, sp_b, dp_b);
       } else if (same && nf <= 2) {
-        copy_shifted_rows<2>(src, dst, nf, it.rows, run_b, sp_b, dp_b);
+        copy_shifted_rows<2, RU>(src, dst, nf, it.rows, run_b, sp_b, dp_b);
       } else {
         // replicas differ modulo 16 (or many of them): one replica per pass
         for (int f = 0; f < nf; ++f) {
           uint8_t *one[1] = {pick<kGenFan>(dst, f)};
-          copy_shifted_rows<1>(src, one, 1, it.rows, run_b, sp_b, dp_b);
+          copy_shifted_rows<1, RU>(src, one, 1, it.rows, run_b, sp_b, dp_b);
         }
       }
     }
@@ -412,13 +415,13 @@ __device__ __forceinline__ void general_walk(const Item *__restrict__ items, con
 __global__ void __launch_bounds__(kBlock, RESHARD_GEN_MIN_BLOCKS) reshard_copy_kernel(
     const Item *__restrict__ items, const int32_t *__restrict__ idx, int n_items, const uint64_t *__restrict__ ptrs,
     const int32_t *__restrict__ gstart, const int32_t *__restrict__ mptr, const int64_t *__restrict__ moff) {
-  general_walk<kGenUnroll>(items, idx, n_items, ptrs, gstart, mptr, moff);
+  general_walk<kGenUnroll, RESHARD_GEN_ROW_UNROLL>(items, idx, n_items, ptrs, gstart, mptr, moff);
 }
 
 __global__ void __launch_bounds__(kBlock, RESHARD_ROWS_MIN_BLOCKS) reshard_copy_rows_kernel(
     const Item *__restrict__ items, const int32_t *__restrict__ idx, int n_items, const uint64_t *__restrict__ ptrs,
     const int32_t *__restrict__ gstart, const int32_t *__restrict__ mptr, const int64_t *__restrict__ moff) {
-  general_walk<RESHARD_ROWS_GEN_UNROLL>(items, idx, n_items, ptrs, gstart, mptr, moff);
+  general_walk<RESHARD_ROWS_GEN_UNROLL, RESHARD_ROW_UNROLL>(items, idx, n_items, ptrs, gstart, mptr, moff);
 }
 
 // The aligned walker: items the host found 16-byte aligned everywhere (sources, every replica,
