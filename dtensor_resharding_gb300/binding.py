@@ -9,6 +9,8 @@ import ctypes
 import os
 from typing import Any, Dict, List, Optional, Sequence
 
+import numpy as np
+
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libreshard.so")
 
@@ -174,6 +176,116 @@ def make_spec(desc, src_capacity: Optional[Sequence[int]] = None, dst_capacity: 
     return s
 
 
+def _spec_dtype():
+    """numpy record type laid out exactly like reshard_tensor_spec_t (offsets taken from ctypes)."""
+    names, formats, offsets = [], [], []
+
+    def add(name, fmt, off):
+        names.append(name)
+        formats.append(fmt)
+        offsets.append(off)
+    add("ndim", "<i4", TensorSpecT.ndim.offset)
+    add("global_shape", "<u8", TensorSpecT.global_shape.offset)
+    add("dtype", "<i4", TensorSpecT.dtype.offset)
+    for side in ("src", "dst"):
+        m = getattr(TensorSpecT, f"{side}_mesh").offset
+        add(f"{side}_ndim", "<i4", m + MeshT.ndim.offset)
+        add(f"{side}_shape", "<u8", m + MeshT.shape.offset)
+        add(f"{side}_ranks", "<u8", m + MeshT.ranks.offset)
+        add(f"{side}_pl", "<u8", getattr(TensorSpecT, f"{side}_pl").offset)
+        add(f"{side}_views", "<u8", getattr(TensorSpecT, f"{side}_views").offset)
+    return np.dtype({"names": names, "formats": formats, "offsets": offsets, "itemsize": ctypes.sizeof(TensorSpecT)})
+
+
+_VIEW_DTYPE = None
+_SPEC_DTYPE = None
+
+
+def pack_specs(descs: Sequence[Any], src_capacity=None, dst_capacity=None):
+    """Marshal many tensor descriptions into one contiguous reshard_tensor_spec_t array.
+
+    Every integer goes into a few flat numpy pools (int64: shapes, meshes, strides; int32:
+    ranks; placement pairs; view records) and each spec field points into them, so a batch of
+    thousands of tensors costs a handful of allocations. Returns (specs, keep): ``specs`` is the
+    record array, ``keep`` the pools, which must outlive the C call.
+    """
+    global _VIEW_DTYPE, _SPEC_DTYPE
+    if _SPEC_DTYPE is None:
+        _SPEC_DTYPE = _spec_dtype()
+        _VIEW_DTYPE = np.dtype({"names": ["offset", "strides", "capacity"], "formats": ["<i8", "<u8", "<i8"],
+                                "offsets": [ViewT.offset_elems.offset, ViewT.strides_elems.offset,
+                                            ViewT.capacity_elems.offset], "itemsize": ctypes.sizeof(ViewT)})
+    n = len(descs)
+    i64: List[int] = []
+    i32: List[int] = []
+    pls: List[int] = []
+    views: List[tuple] = []   # (offset, strides index in i64 or -1, capacity)
+    rows = []                 # per tensor: field values, pool indices where pointers go
+    for t, d in enumerate(descs):
+        gs = d.global_shape
+        rec = [len(gs), len(i64), DTYPE_CODES[d.dtype] if isinstance(d.dtype, str) else int(d.dtype)]
+        i64.extend(int(x) for x in gs)
+        for side, caps in (("src", src_capacity), ("dst", dst_capacity)):
+            mesh = getattr(d, f"{side}_mesh")
+            rec += [len(mesh), len(i64)]
+            i64.extend(int(x) for x in mesh)
+            ranks = getattr(d, f"{side}_ranks", None)
+            if ranks is not None:
+                rec.append(len(i32))
+                i32.extend(int(x) for x in ranks)
+            else:
+                rec.append(-1)
+            rec.append(len(pls) // 2)
+            for p_ in getattr(d, f"{side}_placements"):
+                if isinstance(p_, str):
+                    pls += (RESHARD_REPLICATE, 0) if p_ == "R" else (RESHARD_SHARD, int(p_[1:]))
+                else:
+                    pls += (int(p_[0]), int(p_[1]))
+            vs = getattr(d, f"{side}_views", None)
+            if vs is None:
+                rec.append(-1)
+            else:
+                rec.append(len(views))
+                cap = caps[t] if caps else None
+                for k, v in enumerate(vs):
+                    st = getattr(v, "strides", None)
+                    si = -1
+                    if st is not None:
+                        si = len(i64)
+                        i64.extend(int(x) for x in st)
+                    views.append((int(getattr(v, "offset", 0)), si, int(cap[k]) if cap is not None else 0))
+        rows.append(rec)
+    pool64 = np.array(i64 or [0], dtype=np.int64)
+    pool32 = np.array(i32 or [0], dtype=np.int32)
+    poolpl = np.array(pls or [0, 0], dtype=np.int32)
+    vrec = np.zeros(max(1, len(views)), dtype=_VIEW_DTYPE)
+    b64, b32, bpl, bv = (pool64.ctypes.data, pool32.ctypes.data, poolpl.ctypes.data, vrec.ctypes.data)
+    if views:
+        va = np.array(views, dtype=np.int64)
+        vrec["offset"] = va[:, 0]
+        vrec["strides"] = np.where(va[:, 1] >= 0, b64 + 8 * va[:, 1], 0).astype(np.uint64)
+        vrec["capacity"] = va[:, 2]
+    specs = np.zeros(max(1, n), dtype=_SPEC_DTYPE)
+    if n:
+        r = np.array(rows, dtype=np.int64)
+        specs["ndim"][:n] = r[:, 0]
+        specs["global_shape"][:n] = (b64 + 8 * r[:, 1]).astype(np.uint64)
+        specs["dtype"][:n] = r[:, 2]
+        for k, side in enumerate(("src", "dst")):
+            c = 3 + 5 * k
+            specs[f"{side}_ndim"][:n] = r[:, c]
+            specs[f"{side}_shape"][:n] = (b64 + 8 * r[:, c + 1]).astype(np.uint64)
+            specs[f"{side}_ranks"][:n] = np.where(r[:, c + 2] >= 0, b32 + 4 * r[:, c + 2], 0).astype(np.uint64)
+            specs[f"{side}_pl"][:n] = (bpl + 8 * r[:, c + 3]).astype(np.uint64)
+            specs[f"{side}_views"][:n] = np.where(r[:, c + 4] >= 0, bv + ctypes.sizeof(ViewT) * r[:, c + 4],
+                                                  0).astype(np.uint64)
+    return specs, [pool64, pool32, poolpl, vrec]
+
+
+def _spec_ptr(specs):
+    return ctypes.cast(ctypes.c_void_p(specs.ctypes.data), ctypes.POINTER(TensorSpecT))
+
+
 # ------------------------------------------------------------------------------- the calls
 
 class Plan:
@@ -207,26 +319,20 @@ def reshard_plan_create(desc, src_capacity=None, dst_capacity=None) -> Plan:
 
 def reshard_plan_batch(descs: Sequence[Any], src_capacity=None, dst_capacity=None) -> Plan:
     """One plan over many tensors. Capacities (optional) are per tensor lists of per-rank counts."""
-    keep: list = []
-    arr = (TensorSpecT * max(1, len(descs)))()
-    for i, d in enumerate(descs):
-        arr[i] = make_spec(d, src_capacity[i] if src_capacity else None,
-                           dst_capacity[i] if dst_capacity else None, keep)
+    specs, keep = pack_specs(descs, src_capacity, dst_capacity)
     h = ctypes.c_void_p()
-    _check(LIB.reshard_plan_batch(arr, len(descs), ctypes.byref(h)))
+    _check(LIB.reshard_plan_batch(_spec_ptr(specs), len(descs), ctypes.byref(h)))
+    del keep
     return Plan(h.value, sum(_n_ranks(d.src_mesh) for d in descs), sum(_n_ranks(d.dst_mesh) for d in descs))
 
 
 def reshard_plan_blockwise_fp8(descs: Sequence[Any], block=(128, 128), src_capacity=None, dst_capacity=None) -> Plan:
     """FP8 weights (u8) plus their derived blockwise fp32 scales in one plan: weights first,
     then scales, in the pointer arrays too. Capacities (optional) cover the weights only."""
-    keep: list = []
-    arr = (TensorSpecT * max(1, len(descs)))()
-    for i, d in enumerate(descs):
-        arr[i] = make_spec(d, src_capacity[i] if src_capacity else None,
-                           dst_capacity[i] if dst_capacity else None, keep)
+    specs, keep = pack_specs(descs, src_capacity, dst_capacity)
     h = ctypes.c_void_p()
-    _check(LIB.reshard_plan_blockwise_fp8(arr, len(descs), int(block[0]), int(block[1]), ctypes.byref(h)))
+    _check(LIB.reshard_plan_blockwise_fp8(_spec_ptr(specs), len(descs), int(block[0]), int(block[1]), ctypes.byref(h)))
+    del keep
     return Plan(h.value, 2 * sum(_n_ranks(d.src_mesh) for d in descs), 2 * sum(_n_ranks(d.dst_mesh) for d in descs))
 
 

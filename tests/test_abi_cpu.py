@@ -208,3 +208,25 @@ def test_dp8_replicas_are_read_once():
     assert st["bytes_written"] == 4 * total   # four engines, each a full TP4 copy
     # every region's source is the lowest-index replica (dp = 0): pointer indices 0 and 1
     assert {s for _, s, _, _ in R.reshard_plan_regions(R.reshard_plan_create(d))} == {0, 1}
+
+
+def test_batch_marshalling_equals_single_tensor_plans():
+    """The packed batch marshalling gives each tensor the same regions as planning it alone
+    (views with offsets and strides, rank permutations, capacities)."""
+    cases = list(S.fuzz_cases(40, seed=29))
+    d = S.TensorDesc("p", (8, 8), "i32", (2,), ("S0",), (4,), ("S1",), [S.View(0), S.View(1)],
+                     [S.View(i) for i in range(4)])
+    d.dst_ranks = [3, 2, 1, 0]
+    descs = [wl.tensors[0] for wl in cases] + [d]
+    caps_s = [[wl.src_buffer_numel[v.buffer] for v in wl.tensors[0].src_views] for wl in cases] + [[64, 64]]
+    caps_d = [[wl.dst_buffer_numel[v.buffer] for v in wl.tensors[0].dst_views] for wl in cases] + [[64] * 4]
+    batch = R.reshard_plan_batch(descs, caps_s, caps_d)
+    got = {}
+    for t, m, s, box in _planner_regions(batch):
+        got.setdefault(t, []).append((m, s, box))
+    for t, desc in enumerate(descs):
+        alone = R.reshard_plan_create(desc, caps_s[t], caps_d[t])
+        want = sorted((m, s, box) for _, m, s, box in _planner_regions(alone))
+        assert sorted(got.get(t, [])) == want, t
+    st = R.reshard_plan_stats(batch)
+    assert st["n_tensors"] == len(descs)
