@@ -1,20 +1,25 @@
 // Device executor of the reshard plan: persistent descriptor-walking kernels for sm_103a.
 //
-// - reshard_copy_kernel: one pass over the work-item table; every item's source rows are read
-//   once and written to every destination replica of its group (the fan-out of "xferdtensor
-//   Transports" in the NeMo-RL design doc "NCCL Reshard Refit (Experimental)"). Used for the
-//   direct mode and for both halves of the packed mode (pack: source -> contiguous message;
-//   unpack: message -> destination replicas), the messages a wire transport would carry
-//   ("NeMo-RL: Optimizing Non-Colocated Refit", "Optimization #2": pack into one contiguous
-//   buffer).
-// - reshard_mxfp8_kernel: the same walk with the receive-side BF16 -> MXFP8 epilogue
-//   (design doc, "Enabling It": generation ranks quantize each received BF16 shard), by the
-//   OCP MX v1.0 rule: per 32 contiguous elements along the destination's last dim, the E8M0
-//   scale X = floor(log2 amax) - 8 and E4M3 elements v / 2^X rounded to nearest even,
-//   saturating at 448. The block amax is combined across the 4 lanes holding a block with
-//   warp shuffles.
+// Every item's source rows are read once and written to every destination replica of its group
+// (the fan-out of "xferdtensor Transports" in the NeMo-RL design doc "NCCL Reshard Refit
+// (Experimental)"). The same walkers serve the direct mode and both halves of the packed mode
+// (pack: source -> contiguous message; unpack: message -> destination replicas), the messages a
+// wire transport would carry ("NeMo-RL: Optimizing Non-Colocated Refit", "Optimization #2":
+// pack into one contiguous buffer).
+// - reshard_copy_aligned_kernel: items 16-byte aligned on every side; 16-byte streaming copies,
+//   8 loads in flight per thread.
+// - reshard_copy_kernel / reshard_copy_rows_kernel: every other item (one warp per row,
+//   funnel-shifted 16-byte destination words); two builds of one walker, for long rows and for
+//   many short rows.
+// - reshard_transpose_kernel: regions whose two sides are contiguous along different dims; TMA
+//   box loads into swizzled shared memory, column runs stored from there.
+// - reshard_mxfp8_kernel: the copy walk with the receive-side BF16 -> MXFP8 epilogue (design
+//   doc, "Enabling It": generation ranks quantize each received BF16 shard), by the OCP MX v1.0
+//   rule: per 32 contiguous elements along the destination's last dim, the E8M0 scale
+//   X = floor(log2 amax) - 8 and E4M3 elements v / 2^X rounded to nearest even, saturating at
+//   448. The two lanes holding a block combine their amax with a warp shuffle.
 //
-// Nothing here is a contraction; both kernels are bound by HBM bandwidth. Sources and
+// Nothing here is a contraction; every kernel is bound by HBM bandwidth. Sources and
 // destinations must not overlap in memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>

@@ -54,7 +54,17 @@ SMALL = {
     "broadcast_16_replicas": lambda: _one((100, 300), (1,), ("R",), (16,), ("R",)),
     "nearly_empty_1x1": lambda: _one((1, 1), (2,), ("S0",), (3,), ("S1",)),
     "replicated_source_to_2d": lambda: _one((257, 130), (3, 2), ("R", "S1"), (2, 2), ("S0", "S1")),
+    "aligned_rows_with_byte_tails": lambda: _padded((64, 1000), 1024, 504),
+    "run_shorter_than_a_word": lambda: _one((1, 3), (1,), ("R",), (2,), ("R",)),
 }
+
+
+def _padded(shape, src_pitch, dst_pitch):
+    """One replica into a 2-way column split, both sides with padded row pitches that keep every
+    row start 16-byte aligned while the runs (1000 bytes) end 8 bytes into a word."""
+    t = S.TensorDesc("w", shape, "bf16", (1,), ("R",), (2,), ("S1",), [S.View(0, 0, (src_pitch, 1))],
+                     [S.View(0, 0, (dst_pitch, 1)), S.View(1, 0, (dst_pitch, 1))], seed=37)
+    return S.workloads._size_buffers(S.Workload("padded", [t]), 1, 2)
 
 
 def _one(shape, sm, sp, dm, dp, dtype="bf16", quant="none"):
