@@ -607,6 +607,10 @@ int build(const reshard_tensor_spec_t *specs, int n, reshard_plan_t **out) {
     bytes_read += b;
     bytes_written += b * (int64_t)g.members.size();
   }
+  // transposing items grouped by element size: the executor launches one build of its
+  // transposing kernel per element size present, each over a contiguous run of the table
+  for (auto &tv : plan->titems)
+    std::stable_sort(tv.begin(), tv.end(), [](const TItem &a, const TItem &b) { return a.esize < b.esize; });
   for (const TensorInfo &t : plan->tensors) {
     int64_t v2 = t.esize;
     for (int d = 0; d < t.ndim; ++d) v2 *= t.shape[d];
