@@ -140,11 +140,6 @@ __device__ __forceinline__ uint4 shift_bytes(uint4 lo, uint4 hi, int sh) {
   return o;
 }
 
-__device__ __forceinline__ uint32_t byte_of(uint4 v, int k) {
-  const uint32_t w = k < 4 ? v.x : k < 8 ? v.y : k < 12 ? v.z : v.w;
-  return (w >> ((k & 3) * 8)) & 0xFF;
-}
-
 // Bytes [kmin, kmax) of the 16-byte word `o` into the 16-byte aligned `word`, each piece the
 // widest naturally aligned store that fits (at most 7 stores instead of up to 15 bytes).
 __device__ __forceinline__ void store_partial(uint8_t *word, uint4 o, int kmin, int kmax) {
@@ -546,18 +541,6 @@ __device__ __forceinline__ uint2 quantize8_by(uint4 v, float inv) {
   return q;
 }
 
-// Quantize 8 BF16 values (one 16-byte load) under the block amax shared by its lanes.
-__device__ __forceinline__ uint2 quantize8(uint4 v, uint32_t amax) {
-  if (amax >= 0x7F80u) return make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);  // Inf/NaN block: E4M3 NaN
-  const int x = block_exponent(amax);
-  return quantize8_by(v, __uint_as_float((uint32_t)(127 - x) << 23));  // 2^-X, X in [-127, 119]
-}
-
-// E8M0 byte of a block: 0xFF (NaN) when the block holds Inf/NaN, else X + 127.
-__device__ __forceinline__ uint32_t scale_byte(uint32_t amax) {
-  return amax >= 0x7F80u ? 0xFFu : (uint32_t)(block_exponent(amax) + 127);
-}
-
 __device__ __forceinline__ uint4 load_bf16x8(const uint8_t *p, bool vec) {
   if (vec) return load_stream(p);
   const uint16_t *h = reinterpret_cast<const uint16_t *>(p);
@@ -584,7 +567,6 @@ __global__ void __launch_bounds__(kQBlock, RESHARD_MXFP8_MIN_BLOCKS) reshard_mxf
     const int64_t sp_b = it.src_pitch * 2;
     const bool vec = ((reinterpret_cast<uintptr_t>(src) | (it.rows > 1 ? (uintptr_t)sp_b : 0)) & 15) == 0;
     const bool vec32 = ((reinterpret_cast<uintptr_t>(src) | (it.rows > 1 ? (uintptr_t)sp_b : 0)) & 31) == 0;
-    (void)vec32;
     for (int f0 = 0; f0 < nrep; f0 += kQMaxFan) {
       const int nf = min(kQMaxFan, nrep - f0);
       uint8_t *dq[kQMaxFan];
