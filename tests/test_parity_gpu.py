@@ -368,3 +368,17 @@ def test_general_walker_build_follows_the_item_shapes():
     st = R.reshard_plan_stats(plan)
     assert st["last_general_items"] > 0 and st["last_rows_kernel"] == 0
     assert_matches_oracle(wl, lay)
+
+
+def test_readme_example():
+    """The usage example of the README, verbatim in substance: 2 row shards -> 4 column shards."""
+    from synthetic import TensorDesc, View
+    spec = TensorDesc("w", (8, 8), "bf16", (2,), ("S0",), (4,), ("S1",),
+                      [View(0), View(1)], [View(i) for i in range(4)])
+    src = [torch.randn(4, 8, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    dst = [torch.empty(8, 2, dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+    plan = R.reshard_plan_create(spec)
+    R.reshard_execute(plan, [t.data_ptr() for t in src], [t.data_ptr() for t in dst],
+                      mode="direct", quant="none", stream=torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat(dst, 1), torch.cat(src, 0))
