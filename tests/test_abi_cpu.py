@@ -230,3 +230,32 @@ def test_batch_marshalling_equals_single_tensor_plans():
         assert sorted(got.get(t, [])) == want, t
     st = R.reshard_plan_stats(batch)
     assert st["n_tensors"] == len(descs)
+
+
+def test_every_entry_point_refuses_null_and_out_of_range_arguments():
+    """NULL plans, NULL outputs and out-of-range indices return INVALID_ARG with a message, on the
+    host, before any device work; nothing crashes."""
+    import ctypes
+    L = R.binding.LIB
+    inv = R.RESHARD_ERR_INVALID_ARG
+    n = ctypes.c_int64()
+    st = R.binding.StatsT()
+    i32 = ctypes.c_int32()
+    assert L.reshard_plan_create(None, ctypes.byref(ctypes.c_void_p())) == inv
+    assert L.reshard_plan_batch(None, 1, ctypes.byref(ctypes.c_void_p())) == inv
+    assert L.reshard_plan_stats(None, ctypes.byref(st)) == inv
+    assert L.reshard_plan_regions(None, 0, None, None, None, None, None, ctypes.byref(n)) == inv
+    assert L.reshard_plan_slabs(None, 0, None, ctypes.byref(n)) == inv
+    assert L.reshard_plan_status(None, ctypes.byref(i32), 0) == inv
+    assert L.reshard_execute(None, None, None, 0, 0, None) == inv
+    assert L.reshard_execute_static(None, None, None, None) == inv
+    assert L.reshard_plan_destroy(None) == R.RESHARD_OK
+    plan = R.plan_workload(S.example_8x8())
+    assert L.reshard_plan_stats(plan.handle, None) == inv
+    assert L.reshard_plan_group_members(plan.handle, 10 ** 6, 0, None, ctypes.byref(n)) == inv
+    assert L.reshard_plan_group_members(plan.handle, -1, 0, None, ctypes.byref(n)) == inv
+    assert L.reshard_plan_items(plan.handle, 6, 0, None, ctypes.byref(n), None, None, None, None, None) == inv
+    assert L.reshard_plan_items(plan.handle, -1, 0, None, ctypes.byref(n), None, None, None, None, None) == inv
+    assert R.reshard_last_error()  # the last refusal left a message
+    with pytest.raises(R.ReshardError):
+        R.reshard_plan_group_members(plan, 10 ** 6)
