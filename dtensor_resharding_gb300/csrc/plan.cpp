@@ -18,6 +18,10 @@
 
 #include "plan.h"
 
+#ifndef RESHARD_SIZE_ORDER
+#define RESHARD_SIZE_ORDER 1
+#endif
+
 namespace reshard {
 
 namespace {
@@ -607,6 +611,13 @@ int build(const reshard_tensor_spec_t *specs, int n, reshard_plan_t **out) {
     bytes_read += b;
     bytes_written += b * (int64_t)g.members.size();
   }
+#if RESHARD_SIZE_ORDER
+  // largest items first: the persistent grid deals items round-robin, so CTAs finish together
+  for (auto &iv : plan->items)
+    std::stable_sort(iv.begin(), iv.end(), [](const Item &a, const Item &b) {
+      return (int64_t)a.rows * a.run * a.esize > (int64_t)b.rows * b.run * b.esize;
+    });
+#endif
   // transposing items grouped by element size: the executor launches one build of its
   // transposing kernel per element size present, each over a contiguous run of the table
   for (auto &tv : plan->titems)
