@@ -81,6 +81,9 @@ constexpr int kGenFan = RESHARD_GEN_FAN;  // the same in the general walker
 #ifndef RESHARD_PDL
 #define RESHARD_PDL 1
 #endif
+#ifndef RESHARD_GEN_OVERLAP
+#define RESHARD_GEN_OVERLAP RESHARD_PDL
+#endif
 __device__ __forceinline__ void pdl_enter() {
 #if RESHARD_PDL
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -438,18 +441,26 @@ __device__ __forceinline__ void general_walk(const Item *__restrict__ items, con
 // Two builds of the general walker. reshard_copy_kernel (4 CTAs/SM) suits long single-row
 // items; reshard_copy_rows_kernel (6 CTAs/SM, fewer registers) suits items of many short rows,
 // where one warp walks one row and more resident warps hide more load latency.
+// `wait_last`: the launch follows the aligned walker of the same pass, whose items touch other
+// bytes; the grid then starts while that walker drains and takes its dependency wait just before
+// it exits, so its completion still implies the aligned walker's (and the next launch on the
+// stream, waiting for this grid, is ordered after both).
 __global__ void __launch_bounds__(kBlock, RESHARD_GEN_MIN_BLOCKS) reshard_copy_kernel(
     const Item *__restrict__ items, const int32_t *__restrict__ idx, int n_items, const uint64_t *__restrict__ ptrs,
-    const int32_t *__restrict__ gstart, const int32_t *__restrict__ mptr, const int64_t *__restrict__ moff) {
-  pdl_enter();
+    const int32_t *__restrict__ gstart, const int32_t *__restrict__ mptr, const int64_t *__restrict__ moff,
+    int wait_last) {
+  if (!wait_last) pdl_enter();
   general_walk<kGenUnroll, RESHARD_GEN_ROW_UNROLL>(items, idx, n_items, ptrs, gstart, mptr, moff);
+  if (wait_last) pdl_enter();
 }
 
 __global__ void __launch_bounds__(kBlock, RESHARD_ROWS_MIN_BLOCKS) reshard_copy_rows_kernel(
     const Item *__restrict__ items, const int32_t *__restrict__ idx, int n_items, const uint64_t *__restrict__ ptrs,
-    const int32_t *__restrict__ gstart, const int32_t *__restrict__ mptr, const int64_t *__restrict__ moff) {
-  pdl_enter();
+    const int32_t *__restrict__ gstart, const int32_t *__restrict__ mptr, const int64_t *__restrict__ moff,
+    int wait_last) {
+  if (!wait_last) pdl_enter();
   general_walk<RESHARD_ROWS_GEN_UNROLL, RESHARD_ROW_UNROLL>(items, idx, n_items, ptrs, gstart, mptr, moff);
+  if (wait_last) pdl_enter();
 }
 
 // The aligned walker: items the host found 16-byte aligned everywhere (sources, every replica,
@@ -1392,13 +1403,14 @@ int launch(reshard_plan_t *p, int set, bool quant, cudaStream_t stream, const La
       ++p->last_launches;
     }
     p->last_rows_kernel = ng > 0 && p->gen_rows[set];
+    const int wait_last = RESHARD_GEN_OVERLAP && na > 0 ? 1 : 0;  // an aligned walker of this pass precedes
     if (ng > 0 && p->gen_rows[set]) {
       RS_CUDA(launch_kernel(true, reshard_copy_rows_kernel, std::min(ng, caps.rows_grid), kBlock, 0, stream, items, idx + na,
-                            ng, p->d_ptrs, p->d_grp_start, p->d_mem_ptr, p->d_mem_off));
+                            ng, p->d_ptrs, p->d_grp_start, p->d_mem_ptr, p->d_mem_off, wait_last));
       ++p->last_launches;
     } else if (ng > 0) {
       RS_CUDA(launch_kernel(true, reshard_copy_kernel, std::min(ng, caps.copy_grid), kBlock, 0, stream, items, idx + na, ng,
-                            p->d_ptrs, p->d_grp_start, p->d_mem_ptr, p->d_mem_off));
+                            p->d_ptrs, p->d_grp_start, p->d_mem_ptr, p->d_mem_off, wait_last));
       ++p->last_launches;
     }
   }
@@ -1645,7 +1657,7 @@ extern "C" int reshard_execute_static(const reshard_plan_t *p, void *const *src_
   reshard_copy_kernel<<<grid, kBlock, 0, stream>>>(
       reinterpret_cast<const Item *>(base), nullptr, n, reinterpret_cast<const uint64_t *>(base + o_pt),
       reinterpret_cast<const int32_t *>(base + o_gs), reinterpret_cast<const int32_t *>(base + o_mp),
-      reinterpret_cast<const int64_t *>(base + o_mo));
+      reinterpret_cast<const int64_t *>(base + o_mo), 0);
   RS_CUDA(cudaGetLastError());
   return RESHARD_OK;
 }
