@@ -398,23 +398,30 @@ def our_arm(args, rank: int, world: int, local_rank: int) -> None:
             dist.barrier()
 
     def run_steps(mode, k, warm):
+        """Time k executes back to back (events only around the whole run, so consecutive launches
+        overlap as they would for a caller); then time k more, each bracketed by its own event
+        pair, for the per-launch durations the roofline uses (an event between two launches is a
+        stream operation of its own and keeps them from overlapping)."""
         for _ in range(warm):
             R.reshard_execute(plan, sp, dp, mode=mode, quant=quant, stream=sh)
         stream.synchronize()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
         barrier()
         torch.cuda.synchronize()
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         start.record(stream)
-        for a, b in ev:
-            a.record(stream)
+        for _ in range(k):
             R.reshard_execute(plan, sp, dp, mode=mode, quant=quant, stream=sh)
-            b.record(stream)
         end.record(stream)
         torch.cuda.synchronize()
         barrier()
         total_ms = max_over_ranks(start.elapsed_time(end), world, dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
+        for a, b in ev:
+            a.record(stream)
+            R.reshard_execute(plan, sp, dp, mode=mode, quant=quant, stream=sh)
+            b.record(stream)
+        torch.cuda.synchronize()
         per = [a.elapsed_time(b) for a, b in ev]
         return total_ms, per
 
