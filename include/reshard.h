@@ -265,7 +265,9 @@ int reshard_plan_group_members(const reshard_plan_t *plan, int64_t g, int64_t ca
  * esize, slab, x, y. Element (r, c) moves from src_off + r * src_pitch + c to
  * member_offset + dst_off + c * dst_pitch + r; (x, y) are (c = 0, r = 0) in slab coordinates.
  * Pointer table: [sources | destination data | destination scales | packed workspace]. Up to
- * cap items go to `items` (may be NULL); *n_out gets the count.
+ * cap items go to `items` (may be NULL); *n_out gets the count. Copy items are ordered largest
+ * first (the walkers deal them round-robin to a persistent grid); transposing items are grouped
+ * by element size (one launch per size).
  * Groups: group_start (n_groups + 2 entries incl. the workspace group), member_ptr and
  * member_off (elements) are copied when non-NULL; *n_groups_out / *n_members_out get sizes.
  */
@@ -283,7 +285,9 @@ int reshard_plan_slabs(const reshard_plan_t *plan, int64_t cap, int64_t *out, in
 
 /*
  * reshard_plan_status -- the plan's device status word (0 = fine; bit 0: a TMA wait in the
- * transposing kernel gave up after its time limit and that launch's output is incomplete).
+ * transposing kernel gave up after its time limit and that launch's output is incomplete;
+ * bit 1: the aligned walker met an item that was not 16-byte aligned for the launch's pointers
+ * and skipped it, so that output is incomplete too).
  * Synchronizes the device, then reads the word; reset != 0 clears it. 0 before any execute.
  */
 int reshard_plan_status(reshard_plan_t *plan, int32_t *status, int reset);
