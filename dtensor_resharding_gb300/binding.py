@@ -118,13 +118,24 @@ def _arr(ctype, vals):
     return (ctype * max(1, len(vals)))(*vals)
 
 
+def placement_pair(p) -> tuple:
+    """(kind, dim) of one placement: "R" / "S<d>", a (kind, dim) pair, or a PyTorch DTensor
+    placement object (torch.distributed.tensor.Shard(d) / Replicate())."""
+    if isinstance(p, str):
+        return (RESHARD_REPLICATE, 0) if p == "R" else (RESHARD_SHARD, int(p[1:]))
+    if hasattr(p, "is_shard") and hasattr(p, "is_replicate"):
+        if p.is_shard():
+            return (RESHARD_SHARD, int(p.dim))
+        if p.is_replicate():
+            return (RESHARD_REPLICATE, 0)
+        raise ReshardError(RESHARD_ERR_UNSUPPORTED, f"placement {p!r} is neither Shard nor Replicate")
+    return int(p[0]), int(p[1])
+
+
 def _placements(pls: Sequence[Any]):
     out = (PlacementT * max(1, len(pls)))()
     for i, p in enumerate(pls):
-        if isinstance(p, str):
-            out[i].kind, out[i].dim = (RESHARD_REPLICATE, 0) if p == "R" else (RESHARD_SHARD, int(p[1:]))
-        else:
-            out[i].kind, out[i].dim = int(p[0]), int(p[1])
+        out[i].kind, out[i].dim = placement_pair(p)
     return out
 
 
@@ -237,10 +248,7 @@ def pack_specs(descs: Sequence[Any], src_capacity=None, dst_capacity=None):
                 rec.append(-1)
             rec.append(len(pls) // 2)
             for p_ in getattr(d, f"{side}_placements"):
-                if isinstance(p_, str):
-                    pls += (RESHARD_REPLICATE, 0) if p_ == "R" else (RESHARD_SHARD, int(p_[1:]))
-                else:
-                    pls += (int(p_[0]), int(p_[1]))
+                pls += placement_pair(p_)
             vs = getattr(d, f"{side}_views", None)
             if vs is None:
                 rec.append(-1)

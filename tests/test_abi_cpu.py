@@ -259,3 +259,16 @@ def test_every_entry_point_refuses_null_and_out_of_range_arguments():
     assert R.reshard_last_error()  # the last refusal left a message
     with pytest.raises(R.ReshardError):
         R.reshard_plan_group_members(plan, 10 ** 6)
+
+
+def test_torch_placement_objects_are_accepted():
+    """PyTorch's own DTensor placements (Shard(d), Replicate(), e.g. a model's
+    DTensor.placements) plan exactly like their string spellings, in both marshalling paths."""
+    from torch.distributed.tensor import Replicate, Shard
+    a = S.TensorDesc("w", (12, 10), "bf16", (2, 2), ("S0", "R"), (4,), ("S1",),
+                     [S.View(i) for i in range(4)], [S.View(i) for i in range(4)])
+    b = S.TensorDesc("w", (12, 10), "bf16", (2, 2), (Shard(0), Replicate()), (4,), (Shard(1),),
+                     [S.View(i) for i in range(4)], [S.View(i) for i in range(4)])
+    want = sorted(_planner_regions(R.reshard_plan_create(a)))
+    assert sorted(_planner_regions(R.reshard_plan_create(b))) == want
+    assert sorted(_planner_regions(R.reshard_plan_batch([b]))) == want
