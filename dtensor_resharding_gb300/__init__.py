@@ -6,7 +6,7 @@ The public calls mirror the C ABI in include/reshard.h:
 ``reshard_last_error``. Importing the package loads libreshard.so and raises if it is not built.
 """
 from .binding import (  # noqa: F401
-    Plan, ReshardError, LIB_PATH, EXPORTED, STATS_FIELDS, pointer_array,
+    Plan, ReshardError, Spec, View, LIB_PATH, EXPORTED, STATS_FIELDS, pointer_array,
     reshard_plan_create, reshard_plan_batch, reshard_plan_blockwise_fp8, reshard_execute, reshard_execute_static, reshard_plan_stats, reshard_plan_regions,
     reshard_plan_group_members, reshard_plan_items, reshard_plan_slabs, reshard_plan_status,
     reshard_plan_destroy, reshard_last_error, make_spec,

@@ -6,6 +6,7 @@ the library. There is no fallback: if the library is missing, importing this mod
 from __future__ import annotations
 
 import ctypes
+import dataclasses
 import os
 from typing import Any, Dict, List, Optional, Sequence
 
@@ -109,6 +110,34 @@ def _check(rc: int) -> None:
 
 def reshard_last_error() -> str:
     return LIB.reshard_last_error().decode()
+
+
+# ------------------------------------------------------------------------ spec containers
+
+@dataclasses.dataclass
+class View:
+    """Where one rank's shard lives in its buffer: element offset and element strides of the
+    local shard (None: dense row-major)."""
+    offset: int = 0
+    strides: Optional[Sequence[int]] = None
+
+
+@dataclasses.dataclass
+class Spec:
+    """One tensor's reshard, as reshard_plan_create takes it: the global shape and dtype
+    ("bf16", "f16", "f32", "u8", "i32", "i64"), and on each side the mesh shape and one placement
+    per mesh dim ("S<d>" / "R", or torch.distributed.tensor Shard(d) / Replicate()). Optional:
+    per-rank views (one per pointer index) and rank permutations (mesh position -> pointer index)."""
+    global_shape: Sequence[int]
+    dtype: str
+    src_mesh: Sequence[int]
+    src_placements: Sequence[Any]
+    dst_mesh: Sequence[int]
+    dst_placements: Sequence[Any]
+    src_views: Optional[Sequence[View]] = None
+    dst_views: Optional[Sequence[View]] = None
+    src_ranks: Optional[Sequence[int]] = None
+    dst_ranks: Optional[Sequence[int]] = None
 
 
 # ------------------------------------------------------------------------- spec marshalling

@@ -272,3 +272,15 @@ def test_torch_placement_objects_are_accepted():
     want = sorted(_planner_regions(R.reshard_plan_create(a)))
     assert sorted(_planner_regions(R.reshard_plan_create(b))) == want
     assert sorted(_planner_regions(R.reshard_plan_batch([b]))) == want
+
+
+def test_spec_containers_plan_like_workload_descriptions():
+    """R.Spec / R.View (the binding's own containers) plan exactly like the test descriptions."""
+    a = S.TensorDesc("w", (12, 10), "f32", (2,), ("S0",), (2, 2), ("R", "S1"),
+                     [S.View(0), S.View(1)], [S.View(0, 3, (8, 1)), S.View(1, 0, (8, 1)),
+                                              S.View(2, 0, (8, 1)), S.View(3, 0, (8, 1))])
+    b = R.Spec((12, 10), "f32", (2,), ["S0"], (2, 2), ["R", "S1"],
+               dst_views=[R.View(3, (8, 1)), R.View(0, (8, 1)), R.View(0, (8, 1)), R.View(0, (8, 1))])
+    assert sorted(_planner_regions(R.reshard_plan_create(b))) == sorted(_planner_regions(R.reshard_plan_create(a)))
+    st = R.reshard_plan_stats(R.reshard_plan_batch([b, b]))
+    assert st["n_tensors"] == 2 and st["bytes_written"] == 2 * 2 * 12 * 10 * 4

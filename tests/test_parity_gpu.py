@@ -372,9 +372,8 @@ def test_general_walker_build_follows_the_item_shapes():
 
 def test_readme_example():
     """The usage example of the README, verbatim in substance: 2 row shards -> 4 column shards."""
-    from synthetic import TensorDesc, View
-    spec = TensorDesc("w", (8, 8), "bf16", (2,), ("S0",), (4,), ("S1",),
-                      [View(0), View(1)], [View(i) for i in range(4)])
+    from torch.distributed.tensor import Shard
+    spec = R.Spec((8, 8), "bf16", (2,), [Shard(0)], (4,), [Shard(1)])
     src = [torch.randn(4, 8, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
     dst = [torch.empty(8, 2, dtype=torch.bfloat16, device="cuda") for _ in range(4)]
     plan = R.reshard_plan_create(spec)
