@@ -1547,6 +1547,9 @@ extern "C" int reshard_plan_destroy(reshard_plan_t *p) {
     int cur = 0;
     cudaGetDevice(&cur);
     cudaSetDevice(p->device);
+    // executes of this plan may still be queued on any stream (a garbage-collected handle, for
+    // instance): let the device finish before its tables and workspace go
+    cudaDeviceSynchronize();
     free_device(p);
     cudaSetDevice(cur);
   }

@@ -293,7 +293,9 @@ int reshard_plan_slabs(const reshard_plan_t *plan, int64_t cap, int64_t *out, in
 int reshard_plan_status(reshard_plan_t *plan, int32_t *status, int reset);
 
 /* reshard_plan_destroy -- free the plan's host tables, device tables and workspace.
- * Safe on NULL. The caller must make sure no enqueued execute of the plan is still running. */
+ * Safe on NULL. A plan that has executed first synchronizes its device (executes may still be
+ * queued on any stream), so it is safe to destroy while work is in flight; it blocks until the
+ * device is idle. A plan that never executed frees host memory only. */
 int reshard_plan_destroy(reshard_plan_t *plan);
 
 /* reshard_last_error -- text of this thread's last error ("" if none). Valid until the next

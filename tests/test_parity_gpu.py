@@ -381,3 +381,18 @@ def test_readme_example():
                       mode="direct", quant="none", stream=torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     assert torch.equal(torch.cat(dst, 1), torch.cat(src, 0))
+
+
+def test_plan_released_right_after_execute():
+    """A plan handle dropped while its execute is still queued (garbage-collected at once):
+    destroy waits for the device, so the result is complete and correct."""
+    import gc
+    wl = S.dense_ffn(layers=1, hidden=256, ffn=1000)
+    lay = S.allocate(wl, "cuda")
+    S.fill_sources(wl, lay)
+    S.fill_canary(lay)
+    sp, dp = R.workload_pointers(wl, lay)
+    R.reshard_execute(R.plan_workload(wl), sp, dp, stream=torch.cuda.current_stream().cuda_stream)
+    gc.collect()
+    torch.cuda.synchronize()
+    assert_matches_oracle(wl, lay)
