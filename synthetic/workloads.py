@@ -554,6 +554,8 @@ WORKLOAD_NAMES = {
     # a generation side that keeps every FFN weight transposed (local shards column-major)
     "transpose_32x14336x4096_tp8_to_dp2tp2_dst_colmajor": lambda: transposed(tensors=32),
     "transpose_2x14336x4096_tp8_to_dp2tp2_dst_colmajor": lambda: transposed(tensors=2),
+    # a training side that keeps every weight transposed (source shards column-major)
+    "transpose_32x14336x4096_tp8_to_dp2tp2_src_colmajor": lambda: transposed(tensors=32, side="src"),
     "moe_1x128x1536x4096_ep16_to_ep8": lambda: moe_experts(layers=1, dst="ep8"),
     "moe_1x128x1536x4096_ep16_to_tp4_mxfp8": lambda: moe_experts(layers=1, dst="tp4"),
     # buffers of more than 2^31 elements (64-bit element offsets)

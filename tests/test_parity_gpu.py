@@ -257,9 +257,10 @@ def test_full_many_small_sampled():
     _full(S.many_small, "direct", sampled_check, per_tensor=4)
 
 
+@pytest.mark.parametrize("side", ["dst", "src"])
 @pytest.mark.parametrize("mode", ["direct", "packed"])
-def test_full_transposed_destination_sampled(mode):
-    wl, lay, plan = _full(lambda: S.workload_by_name("transpose_32x14336x4096_tp8_to_dp2tp2_dst_colmajor"), mode,
+def test_full_transposed_destination_sampled(mode, side):
+    wl, lay, plan = _full(lambda: S.workload_by_name(f"transpose_32x14336x4096_tp8_to_dp2tp2_{side}_colmajor"), mode,
                           sampled_check, per_tensor=64, corners=True)
     assert R.reshard_plan_status(plan) == 0
 
