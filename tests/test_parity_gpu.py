@@ -55,8 +55,27 @@ SMALL = {
     "nearly_empty_1x1": lambda: _one((1, 1), (2,), ("S0",), (3,), ("S1",)),
     "replicated_source_to_2d": lambda: _one((257, 130), (3, 2), ("R", "S1"), (2, 2), ("S0", "S1")),
     "aligned_rows_with_byte_tails": lambda: _padded((64, 1000), 1024, 504),
+    "transpose_mixed_bf16_f32_one_plan": lambda: _merge(
+        S.transposed(shape=(300, 200), src_mesh=(4,), src_pl=("S0",)),
+        S.transposed(shape=(130, 257), src_mesh=(3,), src_pl=("S1",), dst_mesh=(2,), dst_pl=("S0",),
+                     dtype="f32", seed=7)),
     "run_shorter_than_a_word": lambda: _one((1, 3), (1,), ("R",), (2,), ("R",)),
 }
+
+
+def _merge(a, b):
+    """One workload holding both workloads' tensors (b's buffers renumbered after a's)."""
+    import dataclasses
+    ns, nd = len(a.src_buffer_numel), len(a.dst_buffer_numel)
+    tb = []
+    for t in b.tensors:
+        tb.append(dataclasses.replace(
+            t, src_views=[dataclasses.replace(v, buffer=v.buffer + ns) for v in t.src_views],
+            dst_views=[dataclasses.replace(v, buffer=v.buffer + nd) for v in t.dst_views]))
+    return S.Workload(a.name + "+" + b.name, a.tensors + tb, src_buffer_numel=a.src_buffer_numel + b.src_buffer_numel,
+                      src_buffer_dtype=a.src_buffer_dtype + b.src_buffer_dtype,
+                      dst_buffer_numel=a.dst_buffer_numel + b.dst_buffer_numel,
+                      dst_buffer_dtype=a.dst_buffer_dtype + b.dst_buffer_dtype)
 
 
 def _padded(shape, src_pitch, dst_pitch):
@@ -396,4 +415,12 @@ def test_plan_released_right_after_execute():
     R.reshard_execute(R.plan_workload(wl), sp, dp, stream=torch.cuda.current_stream().cuda_stream)
     gc.collect()
     torch.cuda.synchronize()
+    assert_matches_oracle(wl, lay)
+
+
+def test_transposing_items_of_two_element_sizes_take_two_launches():
+    wl = SMALL["transpose_mixed_bf16_f32_one_plan"]()
+    lay, plan = run_gpu(wl)
+    st = R.reshard_plan_stats(plan)
+    assert st["last_launches"] == 2 and st["last_aligned_items"] + st["last_general_items"] == 0
     assert_matches_oracle(wl, lay)
