@@ -373,13 +373,23 @@ def reshard_plan_blockwise_fp8(descs: Sequence[Any], block=(128, 128), src_capac
     return Plan(h.value, 2 * sum(_n_ranks(d.src_mesh) for d in descs), 2 * sum(_n_ranks(d.dst_mesh) for d in descs))
 
 
-def pointer_array(ptrs: Sequence[int]):
-    """Device pointers as a contiguous uint64 numpy array, passed to the C calls without copying.
+def _address(p) -> int:
+    """A pointer given as an int (0 / None for an empty shard) or as a tensor (its data_ptr())."""
+    if p is None:
+        return 0
+    if hasattr(p, "data_ptr"):
+        return int(p.data_ptr())
+    return int(p)
+
+
+def pointer_array(ptrs: Sequence[Any]):
+    """Pointers (ints or tensors) as a contiguous uint64 numpy array, passed to the C calls
+    without copying.
 
     Build it once per set of buffers: re-marshalling tens of thousands of pointers per call
     costs milliseconds of host time."""
     import numpy as np
-    return np.ascontiguousarray(np.asarray([int(p) if p else 0 for p in ptrs], dtype=np.uint64))
+    return np.ascontiguousarray(np.asarray([_address(p) for p in ptrs], dtype=np.uint64))
 
 
 def _ptrs_arg(ptrs):
@@ -388,15 +398,15 @@ def _ptrs_arg(ptrs):
         if ptrs.dtype not in (np.uint64, np.int64) or not ptrs.flags["C_CONTIGUOUS"]:
             raise TypeError("pointer arrays must be contiguous uint64/int64")
         return ptrs.ctypes.data_as(ctypes.POINTER(ctypes.c_void_p)), ptrs
-    arr = (ctypes.c_void_p * max(1, len(ptrs)))(*[int(p) if p else None for p in ptrs])
+    arr = (ctypes.c_void_p * max(1, len(ptrs)))(*[_address(p) or None for p in ptrs])
     return arr, arr
 
 
 def reshard_execute(plan: Plan, src_ptrs, dst_ptrs, mode="direct", quant="none", stream: int = 0) -> None:
     """Enqueue the reshard on ``stream`` (a cudaStream_t as int; 0 = legacy default stream).
 
-    ``src_ptrs`` / ``dst_ptrs``: sequences of device pointers, or uint64 arrays from
-    ``pointer_array`` (no per-call marshalling)."""
+    ``src_ptrs`` / ``dst_ptrs``: sequences of pointers (ints, or tensors whose data_ptr() is
+    used), or uint64 arrays from ``pointer_array`` (no per-call marshalling)."""
     mode = MODES[mode] if isinstance(mode, str) else int(mode)
     quant = QUANTS[quant] if isinstance(quant, str) else int(quant)
     sp, _ks = _ptrs_arg(src_ptrs)

@@ -397,8 +397,8 @@ def test_readme_example():
     src = [torch.randn(4, 8, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
     dst = [torch.empty(8, 2, dtype=torch.bfloat16, device="cuda") for _ in range(4)]
     plan = R.reshard_plan_create(spec)
-    R.reshard_execute(plan, [t.data_ptr() for t in src], [t.data_ptr() for t in dst],
-                      mode="direct", quant="none", stream=torch.cuda.current_stream().cuda_stream)
+    R.reshard_execute(plan, src, dst, mode="direct", quant="none",
+                      stream=torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     assert torch.equal(torch.cat(dst, 1), torch.cat(src, 0))
 
