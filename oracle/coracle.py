@@ -31,28 +31,34 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def load(path: str):
+    """The oracle library at ``path`` with its argument types declared (tests load planted-mistake
+    builds of oracle.c this way)."""
+    L = ctypes.CDLL(path)
+    p64 = ctypes.POINTER(ctypes.c_int64)
+    p32 = ctypes.POINTER(ctypes.c_int32)
+    pp = ctypes.POINTER(ctypes.c_void_p)
+    L.oracle_reshard_tensor.argtypes = [
+        ctypes.c_int, p64, ctypes.c_int,
+        ctypes.c_int, p64, p32, pp, p64, p64,
+        ctypes.c_int, p64, p32, pp, p64, p64,
+        ctypes.c_int, pp]
+    L.oracle_reshard_tensor.restype = ctypes.c_int
+    L.oracle_e4m3.argtypes = [ctypes.c_uint16, ctypes.c_int]
+    L.oracle_e4m3.restype = ctypes.c_uint8
+    L.oracle_block_exponent.argtypes = [ctypes.POINTER(ctypes.c_uint16)]
+    L.oracle_block_exponent.restype = ctypes.c_int
+    L.oracle_mxfp8_block.argtypes = [ctypes.POINTER(ctypes.c_uint16), ctypes.POINTER(ctypes.c_uint8),
+                                     ctypes.POINTER(ctypes.c_uint8)]
+    L.oracle_mxfp8_block.restype = None
+    return L
+
+
 def lib():
     global _lib
     if _lib is None:
         build()
-        L = ctypes.CDLL(_LIB_PATH)
-        p64 = ctypes.POINTER(ctypes.c_int64)
-        p32 = ctypes.POINTER(ctypes.c_int32)
-        pp = ctypes.POINTER(ctypes.c_void_p)
-        L.oracle_reshard_tensor.argtypes = [
-            ctypes.c_int, p64, ctypes.c_int,
-            ctypes.c_int, p64, p32, pp, p64, p64,
-            ctypes.c_int, p64, p32, pp, p64, p64,
-            ctypes.c_int, pp]
-        L.oracle_reshard_tensor.restype = ctypes.c_int
-        L.oracle_e4m3.argtypes = [ctypes.c_uint16, ctypes.c_int]
-        L.oracle_e4m3.restype = ctypes.c_uint8
-        L.oracle_block_exponent.argtypes = [ctypes.POINTER(ctypes.c_uint16)]
-        L.oracle_block_exponent.restype = ctypes.c_int
-        L.oracle_mxfp8_block.argtypes = [ctypes.POINTER(ctypes.c_uint16), ctypes.POINTER(ctypes.c_uint8),
-                                         ctypes.POINTER(ctypes.c_uint8)]
-        L.oracle_mxfp8_block.restype = None
-        _lib = L
+        _lib = load(_LIB_PATH)
     return _lib
 
 
@@ -69,9 +75,9 @@ def _ptrs(arrs):
 
 
 def reshard_tensor(desc, src_bufs: Sequence[np.ndarray], dst_bufs: Sequence[np.ndarray],
-                   quant: str = "none", scale_bufs: Optional[Sequence[np.ndarray]] = None) -> None:
+                   quant: str = "none", scale_bufs: Optional[Sequence[np.ndarray]] = None, L=None) -> None:
     """Golden reshard of one tensor through the C oracle, in place into byte buffers."""
-    L = lib()
+    L = L or lib()
     nd = len(desc.global_shape)
 
     def strides(views, mesh, pls):
@@ -100,7 +106,7 @@ def reshard_tensor(desc, src_bufs: Sequence[np.ndarray], dst_bufs: Sequence[np.n
 
 
 def run_workload(wl, src_slab: np.ndarray, src_off, dst_slab: np.ndarray, dst_off,
-                 scale_slab: Optional[np.ndarray] = None, scale_off=None, tensors=None) -> None:
+                 scale_slab: Optional[np.ndarray] = None, scale_off=None, tensors=None, L=None) -> None:
     """Golden reshard of (a subset of) a workload's tensors, in place on host slabs."""
     for ti in (range(len(wl.tensors)) if tensors is None else tensors):
         t = wl.tensors[ti]
@@ -116,7 +122,7 @@ def run_workload(wl, src_slab: np.ndarray, src_off, dst_slab: np.ndarray, dst_of
             db = [dst_slab[dst_off[v.buffer]: dst_off[v.buffer] + wl.dst_buffer_numel[v.buffer] * es]
                   for v in t.dst_views]
             cb = None
-        reshard_tensor(t, sb, db, wl.quant, cb)
+        reshard_tensor(t, sb, db, wl.quant, cb, L)
 
 
 def e4m3(bits: int, x: int) -> int:

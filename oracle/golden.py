@@ -27,7 +27,8 @@ Readings of points the pages leave open (each also listed in the design notes):
 
 Parity: pinned by the 8x8 worked example (golden fixture), brute force over small meshes with
 element-id payloads, torch.chunk as the library definition of the split, the byte invariants
-and the A->B->A round trip (tests).
+and the A->B->A round trip; the MXFP8 placement (``store_mxfp8``) by a hand-derived fixture of
+where every code and scale byte lands, and against the C oracle (tests).
 """
 from __future__ import annotations
 
@@ -145,9 +146,19 @@ def golden_reshard(desc, src_bufs: Sequence[np.ndarray], dst_bufs: Sequence[np.n
             raise OracleError(f"{desc.name}: mxfp8 needs bf16, dense views and K % 32 == 0")
         rows = part.reshape(-1, shp[-1])
         codes, scales = _mx.quantize_rows([[int(b) for b in row] for row in rows])
-        n = rows.size
-        dst_bufs[r][v.offset: v.offset + n] = np.asarray(codes, np.uint8).reshape(-1)
-        scale_bufs[r][v.offset // 32: v.offset // 32 + n // 32] = np.asarray(scales, np.uint8).reshape(-1)
+        store_mxfp8(dst_bufs[r], scale_bufs[r], v.offset, codes, scales)
+
+
+def store_mxfp8(data_buf: np.ndarray, scale_buf: np.ndarray, offset: int, codes, scales) -> None:
+    """Place one quantized shard: its E4M3 codes (one byte per element, row-major rows of the
+    local shard) from byte ``offset`` of the data buffer, and its E8M0 scales (one byte per
+    32-element block, row-major [..., K_local / 32]) from byte ``offset // 32`` of the scale
+    buffer. The layout is the plainest reading of "quantize each received shard" ("Enabling
+    It") under the OCP MX v1.0 block rule; ``offset`` is a multiple of 32."""
+    c = np.asarray(codes, np.uint8).reshape(-1)
+    s = np.asarray(scales, np.uint8).reshape(-1)
+    data_buf[offset: offset + c.size] = c
+    scale_buf[offset // 32: offset // 32 + s.size] = s
 
 
 def run_workload(wl, src_slab: np.ndarray, src_off, dst_slab: np.ndarray, dst_off,

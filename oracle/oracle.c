@@ -15,7 +15,10 @@
  *
  * Parity: cross-checked against the Python oracle (which is pinned by the 8x8 worked example,
  * brute force and torch.chunk) and, for MXFP8, against brute-force nearest-code enumeration
- * over every BF16 pattern (tests). Single-threaded; one tensor per call.
+ * over every BF16 pattern; the placement of a quantized shard (E4M3 bytes row-major from the
+ * shard's element offset, E8M0 scales row-major [..., K_local / 32] from offset / 32) against a
+ * hand-derived fixture whose every scale byte and code block names its block, and against the
+ * Python oracle's independent placement (tests). Single-threaded; one tensor per call.
  */
 #include <stdint.h>
 #include <stdlib.h>
