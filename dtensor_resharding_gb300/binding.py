@@ -31,7 +31,13 @@ RESHARD_MAX_DIMS = 4
 DTYPE_CODES = {"u8": 0, "bf16": 1, "f16": 2, "f32": 3, "i32": 4, "i64": 5}
 MODES = {"direct": RESHARD_DIRECT, "packed": RESHARD_PACKED}
 QUANTS = {"none": RESHARD_QUANT_NONE, "mxfp8": RESHARD_QUANT_MXFP8}
+RESHARD_STRIPED = 1
+RESHARD_SEND = 0
+RESHARD_RECV = 1
+RESHARD_SEND_BUF = 0
+RESHARD_RECV_BUF = 1
 EXPORTED = ("reshard_plan_create", "reshard_plan_batch", "reshard_plan_blockwise_fp8", "reshard_execute",
+            "reshard_execute_pack", "reshard_execute_unpack", "reshard_plan_partition", "reshard_plan_transfers",
             "reshard_execute_static",
             "reshard_plan_stats",
             "reshard_plan_regions", "reshard_plan_group_members", "reshard_plan_items", "reshard_plan_slabs",
@@ -61,11 +67,17 @@ class TensorSpecT(ctypes.Structure):
 
 STATS_FIELDS = ("n_tensors", "regions", "items", "dst_groups", "messages", "bytes_read", "bytes_written",
                 "wire_bytes", "message_bytes", "gather_bcast_bytes", "global_bytes", "last_launches",
-                "last_aligned_items", "last_general_items", "last_rows_kernel")
+                "last_aligned_items", "last_general_items", "last_rows_kernel", "recv_bytes", "rank", "world",
+                "transfers", "sent_bytes", "forwarded_bytes", "local_bytes", "last_staged_items")
 
 
 class StatsT(ctypes.Structure):
     _fields_ = [(f, ctypes.c_int64) for f in STATS_FIELDS]
+
+
+class TransferT(ctypes.Structure):
+    _fields_ = [("peer", ctypes.c_int32), ("dir", ctypes.c_int32), ("buf", ctypes.c_int32), ("phase", ctypes.c_int32),
+                ("offset", ctypes.c_int64), ("bytes", ctypes.c_int64)]
 
 
 class ReshardError(RuntimeError):
@@ -85,6 +97,11 @@ def _load(path: str = LIB_PATH):
                                                ctypes.c_int64, ctypes.POINTER(vp)]
     lib.reshard_execute.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.c_int, ctypes.c_int, vp]
     lib.reshard_execute_static.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp]
+    lib.reshard_execute_pack.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp, ctypes.c_int, vp]
+    lib.reshard_execute_unpack.argtypes = [vp, vp, ctypes.POINTER(vp), ctypes.c_int, vp]
+    lib.reshard_plan_partition.argtypes = [vp, _i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.POINTER(vp)]
+    lib.reshard_plan_transfers.argtypes = [vp, ctypes.c_int, ctypes.c_int64, ctypes.POINTER(TransferT), _i64p]
     lib.reshard_plan_stats.argtypes = [vp, ctypes.POINTER(StatsT)]
     lib.reshard_plan_regions.argtypes = [vp, ctypes.c_int64, _i32p, _i32p, _i32p, _i64p, _i64p, _i64p]
     lib.reshard_plan_group_members.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, _i32p, _i64p]
@@ -412,6 +429,48 @@ def reshard_execute(plan: Plan, src_ptrs, dst_ptrs, mode="direct", quant="none",
     sp, _ks = _ptrs_arg(src_ptrs)
     dp, _kd = _ptrs_arg(dst_ptrs)
     _check(LIB.reshard_execute(plan.handle, sp, dp, mode, quant, ctypes.c_void_p(int(stream) or None)))
+
+
+def reshard_execute_pack(plan: Plan, src_ptrs, dst_ptrs, send_buf, quant="none", stream: int = 0) -> None:
+    """Pack pass with a caller-owned send buffer (``send_buf``: pointer or tensor,
+    ``reshard_plan_stats(plan)["message_bytes"]`` bytes). On a partitioned plan it also makes the
+    copies whose source and destination are both local; ``dst_ptrs`` may be None otherwise."""
+    quant = QUANTS[quant] if isinstance(quant, str) else int(quant)
+    sp, _ks = _ptrs_arg(src_ptrs)
+    dp, _kd = _ptrs_arg(dst_ptrs) if dst_ptrs is not None else (None, None)
+    _check(LIB.reshard_execute_pack(plan.handle, sp, dp, ctypes.c_void_p(_address(send_buf) or None), quant,
+                                    ctypes.c_void_p(int(stream) or None)))
+
+
+def reshard_execute_unpack(plan: Plan, recv_buf, dst_ptrs, quant="none", stream: int = 0) -> None:
+    """Unpack pass from a caller-owned receive buffer (``reshard_plan_stats(plan)["recv_bytes"]``)."""
+    quant = QUANTS[quant] if isinstance(quant, str) else int(quant)
+    dp, _kd = _ptrs_arg(dst_ptrs)
+    _check(LIB.reshard_execute_unpack(plan.handle, ctypes.c_void_p(_address(recv_buf) or None), dp, quant,
+                                      ctypes.c_void_p(int(stream) or None)))
+
+
+def reshard_plan_partition(plan: Plan, src_owner: Sequence[int], dst_owner: Sequence[int], world: int, rank: int,
+                           striped: bool = True) -> Plan:
+    """The share of ``plan`` that process ``rank`` of ``world`` runs; owners map every flat source /
+    destination pointer index to the process holding it."""
+    so = np.ascontiguousarray(np.asarray(src_owner, dtype=np.int32))
+    do = np.ascontiguousarray(np.asarray(dst_owner, dtype=np.int32))
+    if so.size != plan.n_src_ptrs or do.size != plan.n_dst_ptrs:
+        raise ValueError("one owner per source pointer and per destination pointer")
+    h = ctypes.c_void_p()
+    _check(LIB.reshard_plan_partition(plan.handle, so.ctypes.data_as(_i32p), do.ctypes.data_as(_i32p), int(world),
+                                      int(rank), RESHARD_STRIPED if striped else 0, ctypes.byref(h)))
+    return Plan(h.value, plan.n_src_ptrs, plan.n_dst_ptrs)
+
+
+def reshard_plan_transfers(plan: Plan, phase: int) -> List[Dict[str, int]]:
+    """Point-to-point transfers of a partitioned plan's rank in one phase, in posting order."""
+    n = ctypes.c_int64()
+    _check(LIB.reshard_plan_transfers(plan.handle, int(phase), 0, None, ctypes.byref(n)))
+    out = (TransferT * max(1, n.value))()
+    _check(LIB.reshard_plan_transfers(plan.handle, int(phase), n.value, out, ctypes.byref(n)))
+    return [{f: int(getattr(out[i], f)) for f, _ in TransferT._fields_} for i in range(n.value)]
 
 
 def reshard_execute_static(plan: Plan, src_ptrs: Sequence[int], dst_ptrs: Sequence[int], stream: int = 0) -> None:

@@ -508,6 +508,202 @@ __global__ void __launch_bounds__(kBlock, RESHARD_MIN_BLOCKS) reshard_copy_align
   }
 }
 
+// ------------------------------------------------- shared memory and bounded waits --
+
+constexpr unsigned long long kWaitLimitNs = 200ull * 1000 * 1000;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, unsigned long long deadline) {
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (global_ns() > deadline) return false;
+  }
+}
+
+// ------------------------------------------------------- bulk-staged misaligned rows --
+//
+// reshard_copy_staged_kernel copies items of many short rows whose destination rows are not all
+// 16-byte aligned (a column split whose row pitch is not a multiple of 16 bytes, for instance).
+// Source rows are staged in shared memory by the TMA bulk-copy unit: warp 0 issues one
+// cp.async.bulk per row (the row's span rounded out to 16-byte boundaries, so both ends stay in
+// blocks that hold bytes of the row) into a ring of stages, completion counted in bytes on an
+// mbarrier; loads run up to kSStages chunks ahead and hold no registers while in flight. Every
+// warp then drains rows from the stage: lane l writes destination words l, l + 32, ... of the
+// row, each assembled from at most two aligned 16-byte shared-memory reads by a funnel shift and
+// stored whole (or, at the row's two ends, in naturally aligned pieces), once per replica.
+// Waits are bounded like the transposing kernel's: on expiry bit 0 of the status word is set and
+// the CTA returns after waiting (bounded) for its copies in flight.
+
+#ifndef RESHARD_STAGED
+#define RESHARD_STAGED 1
+#endif
+#ifndef RESHARD_STAGED_STAGES
+#define RESHARD_STAGED_STAGES 4
+#endif
+#ifndef RESHARD_STAGED_BYTES
+#define RESHARD_STAGED_BYTES 12288
+#endif
+#ifndef RESHARD_STAGED_MIN_BLOCKS
+#define RESHARD_STAGED_MIN_BLOCKS 3
+#endif
+constexpr int kSStages = RESHARD_STAGED_STAGES;
+constexpr int kSBytes = RESHARD_STAGED_BYTES;  // bytes per stage (multiple of 16)
+constexpr size_t kStagedSmem = (size_t)kSStages * kSBytes;
+static_assert(kSBytes % 16 == 0 && kSStages >= 2 && kSStages <= 8, "stage ring shape");
+// rows up to this many bytes go through the staged kernel (one row must fit a stage)
+constexpr int64_t kStagedMaxRun = RESHARD_ROWS_MAX_RUN;
+static_assert(kStagedMaxRun + 32 <= kSBytes, "a staged row and its rounding fit one stage");
+
+struct StagedChunk {
+  int32_t item;   // position in the launch's item list
+  int32_t r0;     // first row
+  int32_t nrows;
+  int32_t slot;   // bytes per row slot in the stage
+};
+
+__device__ __forceinline__ int staged_slot(int64_t run_b) { return (int)((run_b + 15) / 16 * 16 + 16); }
+
+__device__ __forceinline__ uint4 lds16(const uint8_t *p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(smem_u32(p)));
+  return v;
+}
+
+__global__ void __launch_bounds__(kBlock, RESHARD_STAGED_MIN_BLOCKS) reshard_copy_staged_kernel(
+    const Item *__restrict__ items, const int32_t *__restrict__ idx, int n_items, const uint64_t *__restrict__ ptrs,
+    const int32_t *__restrict__ gstart, const int32_t *__restrict__ mptr, const int64_t *__restrict__ moff,
+    int32_t *status, int wait_last) {
+  if (!wait_last) pdl_enter();
+  extern __shared__ __align__(128) uint8_t sring[];
+  __shared__ __align__(8) uint64_t bar[kSStages];
+  __shared__ StagedChunk desc[kSStages];
+  __shared__ int s_total;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    int tot = 0;
+    for (int k = blockIdx.x; k < n_items; k += gridDim.x) {
+      const Item &it = items[item_index(idx, k)];
+      const int rpc = kSBytes / staged_slot((int64_t)it.run * it.esize);
+      tot += (it.rows + rpc - 1) / rpc;
+    }
+    s_total = tot;
+    for (int st = 0; st < kSStages; ++st) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar[st])));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const int total = s_total;
+
+  // chunk cursor of warp 0 (uniform across its lanes): item k, next row r
+  int ck = blockIdx.x, cr = 0;
+  auto issue = [&](int stage) {
+    Item it = items[item_index(idx, ck)];
+    while (cr >= it.rows) {
+      ck += gridDim.x;
+      cr = 0;
+      it = items[item_index(idx, ck)];
+    }
+    const int64_t es = it.esize, run_b = (int64_t)it.run * es, sp_b = it.src_pitch * es;
+    const int slot = staged_slot(run_b);
+    const int n = min(kSBytes / slot, it.rows - cr);
+    const uintptr_t src0 = (uintptr_t)ptrs[it.src] + (uintptr_t)(it.src_off * es);
+    uint32_t tx = 0;
+    for (int j = lane; j < n; j += 32) {
+      const uintptr_t a = src0 + (uintptr_t)((cr + j) * sp_b);
+      tx += (uint32_t)(((a + run_b + 15) & ~(uintptr_t)15) - (a & ~(uintptr_t)15));
+    }
+    tx = __reduce_add_sync(0xffffffffu, tx);
+    const uint32_t b = smem_u32(&bar[stage]);
+    if (lane == 0) {
+      desc[stage] = StagedChunk{ck, cr, n, slot};
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(tx) : "memory");
+    }
+    __syncwarp();
+    uint8_t *dst0 = sring + (size_t)stage * kSBytes;
+    for (int j = lane; j < n; j += 32) {
+      const uintptr_t a = src0 + (uintptr_t)((cr + j) * sp_b);
+      const uintptr_t lo = a & ~(uintptr_t)15, hi = (a + run_b + 15) & ~(uintptr_t)15;
+      asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                       smem_u32(dst0 + (size_t)j * slot)),
+                   "l"(lo), "r"((uint32_t)(hi - lo)), "r"(b)
+                   : "memory");
+    }
+    cr += n;
+  };
+  if (warp == 0)
+    for (int st = 0; st < kSStages && st < total; ++st) issue(st);
+
+  uint32_t phases = 0;
+  for (int t = 0; t < total; ++t) {
+#if RESHARD_PDL
+    if (t + 1 == total) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+    const int stage = t % kSStages;
+    const bool ok = bar_wait(smem_u32(&bar[stage]), (phases >> stage) & 1, global_ns() + kWaitLimitNs);
+    if (__syncthreads_or(!ok)) {
+      // a bulk load never completed: report, give every load in flight one more bounded wait, stop
+      if (threadIdx.x == 0) atomicOr(status, 1);
+      for (int u = t; u < total && u < t + kSStages; ++u) {
+        const int su = u % kSStages;
+        bar_wait(smem_u32(&bar[su]), (phases >> su) & 1, global_ns() + kWaitLimitNs);
+      }
+      if (wait_last) pdl_enter();
+      return;
+    }
+    phases ^= 1u << stage;
+    const StagedChunk c = desc[stage];
+    const Item it = items[item_index(idx, c.item)];
+    const int64_t es = it.esize, run_b = (int64_t)it.run * es, sp_b = it.src_pitch * es, dp_b = it.dst_pitch * es;
+    const uintptr_t src0 = (uintptr_t)ptrs[it.src] + (uintptr_t)(it.src_off * es);
+    const int g0 = gstart[it.group], g1 = gstart[it.group + 1];
+    const uint8_t *stg = sring + (size_t)stage * kSBytes;
+    for (int j = warp; j < c.nrows; j += kBlock / 32) {
+      const int row = c.r0 + j;
+      const uint8_t *srow = stg + (size_t)j * c.slot;              // holds the row from its 16-byte block
+      const int sh0 = (int)((src0 + (uintptr_t)(row * sp_b)) & 15);  // row byte 0 sits at srow + sh0
+      for (int m = g0; m < g1; ++m) {
+        uint8_t *drow = reinterpret_cast<uint8_t *>(ptrs[mptr[m]]) + (moff[m] + it.dst_off) * es + row * dp_b;
+        const int a = (int)(reinterpret_cast<uintptr_t>(drow) & 15);
+        const int nw = (int)((a + run_b + 15) >> 4);
+        const int s = (sh0 - a) & 15;  // byte phase of each destination word in the stage
+        uint8_t *dword0 = drow - a;
+        for (int w = lane; w < nw; w += 32) {
+          const int64_t start = 16 * (int64_t)w - a;  // row byte of the word's first byte
+          const int kmin = w == 0 ? a : 0;
+          const int kmax = run_b - start < 16 ? (int)(run_b - start) : 16;
+          const int base = sh0 + (int)start;           // stage offset of the word's first byte
+          const int q0 = base - s;                      // 16-byte aligned
+          uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+          if (kmin < 16 - s) lo = lds16(srow + q0);
+          if (s && kmax > 16 - s) hi = lds16(srow + q0 + 16);
+          const uint4 o = s ? shift_bytes(lo, hi, s) : lo;
+          if (kmin == 0 && kmax == 16)
+            store_stream(dword0 + 16 * (int64_t)w, o);
+          else
+            store_partial(dword0 + 16 * (int64_t)w, o, kmin, kmax);
+        }
+      }
+    }
+    __syncthreads();  // the stage is drained: warp 0 may refill it
+    if (warp == 0 && t + kSStages < total) issue(stage);
+  }
+  if (wait_last) pdl_enter();
+}
+
 // ------------------------------------------------------------------------ MXFP8 epilogue --
 
 // Shared E8M0 exponent X of a block from its largest BF16 magnitude (15-bit pattern, finite):
@@ -730,31 +926,6 @@ __global__ void __launch_bounds__(kQBlock, RESHARD_MXFP8_MIN_BLOCKS) reshard_mxf
 constexpr int kTBlock = 256;                          // threads per CTA (one unit per tile per thread)
 constexpr int kTStages = 2;
 constexpr int kTileBytes = kTileRows * kTileRowBytes;  // 16 KiB per stage
-constexpr unsigned long long kWaitLimitNs = 200ull * 1000 * 1000;
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, unsigned long long deadline) {
-  for (;;) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (ok) return true;
-    if (global_ns() > deadline) return false;
-  }
-}
-
 // Byte offset in a 128-byte-swizzled tile of (row, byte within the row).
 __device__ __forceinline__ int swz(int row, int byte) { return row * kTileRowBytes + ((((byte >> 4) ^ (row & 7))) << 4) + (byte & 15); }
 
@@ -1121,6 +1292,7 @@ struct LaunchCaps {
   int aligned_grid = 0;
   int copy_grid = 0;
   int rows_grid = 0;
+  int staged_grid = 0;
   int mxfp8_grid = 0;
   int transpose_grid[4] = {0, 0, 0, 0};  // per element size 1, 2, 4, 8 bytes
 };
@@ -1141,6 +1313,9 @@ int launch_caps(int device, LaunchCaps &c) {
   }
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, reshard_copy_kernel, kBlock, 0));
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b4, reshard_copy_rows_kernel, kBlock, 0));
+  int bs = 0;
+  RS_CUDA(cudaFuncSetAttribute(reshard_copy_staged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStagedSmem));
+  RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bs, reshard_copy_staged_kernel, kBlock, kStagedSmem));
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b2, reshard_mxfp8_kernel, kQBlock, 0));
   int bt[4] = {0, 0, 0, 0};
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bt[0], reshard_transpose_kernel<1>, kTBlock, 0));
@@ -1152,6 +1327,7 @@ int launch_caps(int device, LaunchCaps &c) {
   g_caps.bulk_grid = sms * std::max(1, bb);
   g_caps.copy_grid = sms * std::max(1, b1);
   g_caps.rows_grid = sms * std::max(1, b4);
+  g_caps.staged_grid = sms * std::max(1, bs);
   g_caps.mxfp8_grid = sms * std::max(1, b2);
   for (int k = 0; k < 4; ++k) g_caps.transpose_grid[k] = sms * std::max(1, bt[k]);
   c = g_caps;
@@ -1201,47 +1377,34 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // managed memory, or page-locked host memory mapped into the device's address space
 // (cudaHostAlloc, cudaMallocHost, cudaHostRegister). The kernels then read and write host memory
 // in place over the host link. A host pointer whose device alias differs from it is replaced by
-// the alias in `table`; `host[i]` marks host memory, over which no TMA tensor map is encoded.
-// Pageable host memory and other devices' memory are refused, naming up to eight entries.
-int check_pointers(const reshard_plan_t *p, std::vector<uint64_t> &table, std::vector<uint8_t> &host) {
-  const int64_t Ns = p->n_src_ptrs, Nd = p->n_dst_ptrs;
-  host.assign(table.size(), 0);
-  std::string bad;
-  int n_bad = 0;
-  for (int64_t i = 0; i < Ns + 2 * Nd; ++i) {
-    const uint64_t v = table[(size_t)i];
-    if (!v) continue;
-    cudaPointerAttributes a{};
-    if (cudaPointerGetAttributes(&a, reinterpret_cast<const void *>(v)) != cudaSuccess) {
-      (void)cudaGetLastError();
-      a.type = cudaMemoryTypeUnregistered;
-    }
-    const char *why = nullptr;
-    if (a.type == cudaMemoryTypeDevice) {
-      if (a.device != p->device) why = "is memory of another device";
-    } else if (a.type == cudaMemoryTypeHost) {
-      if (!a.devicePointer) {
-        why = "is page-locked host memory without a device mapping";
-      } else {
-        table[(size_t)i] = reinterpret_cast<uint64_t>(a.devicePointer);
-        host[(size_t)i] = 1;
-      }
-    } else if (a.type != cudaMemoryTypeManaged) {
-      why = "is pageable host memory (page-lock it with cudaHostRegister or use device memory)";
-    }
-    if (why && n_bad++ < 8) {
-      const std::string which = i < Ns        ? "source pointer " + std::to_string(i)
-                                : i < Ns + Nd ? "destination pointer " + std::to_string(i - Ns)
-                                              : "scale pointer " + std::to_string(i - Ns - Nd);
-      char addr[32];
-      std::snprintf(addr, sizeof addr, "0x%llx", (unsigned long long)v);
-      bad += "\n  " + which + " (" + addr + ") " + why;
-    }
+// the alias in `*dev`; `*host` marks host memory, over which no TMA tensor map is encoded.
+// Returns why the entry is refused, or nullptr (NULL entries are never dereferenced and pass).
+const char *check_entry(int device, uint64_t v, uint64_t *dev, uint8_t *host) {
+  *dev = v;
+  *host = 0;
+  if (!v) return nullptr;
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, reinterpret_cast<const void *>(v)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    a.type = cudaMemoryTypeUnregistered;
   }
-  if (n_bad)
-    return fail(RESHARD_ERR_INVALID_ARG,
-                std::to_string(n_bad) + " pointer(s) the device cannot dereference:" + bad);
-  return RESHARD_OK;
+  if (a.type == cudaMemoryTypeDevice) return a.device != device ? "is memory of another device" : nullptr;
+  if (a.type == cudaMemoryTypeHost) {
+    if (!a.devicePointer) return "is page-locked host memory without a device mapping";
+    *dev = reinterpret_cast<uint64_t>(a.devicePointer);
+    *host = 1;
+    return nullptr;
+  }
+  if (a.type == cudaMemoryTypeManaged) return nullptr;
+  return "is pageable host memory (page-lock it with cudaHostRegister or use device memory)";
+}
+
+std::string entry_name(int64_t i, int64_t Ns, int64_t Nd) {
+  return i < Ns            ? "source pointer " + std::to_string(i)
+         : i < Ns + Nd     ? "destination pointer " + std::to_string(i - Ns)
+         : i < Ns + 2 * Nd ? "scale pointer " + std::to_string(i - Ns - Nd)
+         : i == Ns + 2 * Nd ? std::string("send buffer")
+                            : std::string("receive buffer");
 }
 
 // One 2-D tensor map per source slab of the transposing items, for the current pointers. A slab
@@ -1342,8 +1505,10 @@ int classify(reshard_plan_t *p, int set, cudaStream_t stream) {
   std::vector<int32_t> &idx = p->cls_idx[set];
   idx.clear();
   idx.reserve(items.size());
-  std::vector<int32_t> general;
+  std::vector<int32_t> staged, general;
   int64_t gen_bytes = 0, row_bytes = 0;
+  // bulk copies read device memory only (page-locked host memory goes through the walkers)
+  const bool stage_ok = RESHARD_STAGED && !p->any_host;
   for (size_t i = 0; i < items.size(); ++i) {
     const Item &it = items[i];
     const uint64_t es = (uint64_t)it.esize;
@@ -1352,18 +1517,23 @@ int classify(reshard_plan_t *p, int set, cudaStream_t stream) {
     if (it.rows > 1) m |= (uint64_t)it.src_pitch * es | (uint64_t)it.dst_pitch * es;
     for (int32_t k = p->grp_start[(size_t)it.group]; k < p->grp_start[(size_t)it.group + 1]; ++k)
       m |= tab[(size_t)p->mem_ptr[(size_t)k]] + (uint64_t)(p->mem_off[(size_t)k] + it.dst_off) * es;
+    const int64_t run_b = (int64_t)it.run * (int64_t)es;
     if ((m & 15) == 0) {
       idx.push_back((int32_t)i);
+    } else if (stage_ok && it.rows > 1 && run_b <= kStagedMaxRun) {
+      staged.push_back((int32_t)i);
     } else {
       general.push_back((int32_t)i);
-      const int64_t b = (int64_t)it.rows * it.run * (int64_t)es;
+      const int64_t b = (int64_t)it.rows * run_b;
       gen_bytes += b;
-      if (it.rows > 1 && (int64_t)it.run * (int64_t)es < RESHARD_ROWS_MAX_RUN) row_bytes += b;
+      if (it.rows > 1 && run_b < RESHARD_ROWS_MAX_RUN) row_bytes += b;
     }
   }
   p->n_aligned[set] = (int32_t)idx.size();
+  p->n_staged[set] = (int32_t)staged.size();
   // the general items run in the many-rows build when most of their bytes are short rows
   p->gen_rows[set] = 2 * row_bytes > gen_bytes;
+  idx.insert(idx.end(), staged.begin(), staged.end());
   idx.insert(idx.end(), general.begin(), general.end());
   if (!p->d_cls_idx[set] && !idx.empty())
     RS_CUDA(cudaMalloc(reinterpret_cast<void **>(&p->d_cls_idx[set]), idx.size() * sizeof(int32_t)));
@@ -1389,9 +1559,10 @@ int launch(reshard_plan_t *p, int set, bool quant, cudaStream_t stream, const La
     ++p->last_launches;
   } else {
     if ((rc = classify(p, set, stream))) return rc;
-    const int na = p->n_aligned[set], ng = n - na;
+    const int na = p->n_aligned[set], ns = p->n_staged[set], ng = n - na - ns;
     const int32_t *idx = p->d_cls_idx[set];
     p->last_aligned = na;
+    p->last_staged = ns;
     p->last_general = ng;
     if (na > 0 && RESHARD_BULK && !p->any_host) {  // bulk copies over device memory only
       RS_CUDA(launch_kernel(true, reshard_bulk_kernel, std::min(na, caps.bulk_grid), 32, kBulkSmem, stream, items, idx, na,
@@ -1403,14 +1574,23 @@ int launch(reshard_plan_t *p, int set, bool quant, cudaStream_t stream, const La
       ++p->last_launches;
     }
     p->last_rows_kernel = ng > 0 && p->gen_rows[set];
-    const int wait_last = RESHARD_GEN_OVERLAP && na > 0 ? 1 : 0;  // an aligned walker of this pass precedes
+    // a later launch of the pass starts while the earlier ones drain (their items touch other
+    // bytes) and takes its dependency wait just before it exits
+    if (ns > 0) {
+      const int wait_last = RESHARD_GEN_OVERLAP && na > 0 ? 1 : 0;
+      RS_CUDA(launch_kernel(true, reshard_copy_staged_kernel, std::min(ns, caps.staged_grid), kBlock, kStagedSmem, stream,
+                            items, idx + na, ns, p->d_ptrs, p->d_grp_start, p->d_mem_ptr, p->d_mem_off, p->d_status,
+                            wait_last));
+      ++p->last_launches;
+    }
+    const int wait_last = RESHARD_GEN_OVERLAP && na + ns > 0 ? 1 : 0;
     if (ng > 0 && p->gen_rows[set]) {
-      RS_CUDA(launch_kernel(true, reshard_copy_rows_kernel, std::min(ng, caps.rows_grid), kBlock, 0, stream, items, idx + na,
-                            ng, p->d_ptrs, p->d_grp_start, p->d_mem_ptr, p->d_mem_off, wait_last));
+      RS_CUDA(launch_kernel(true, reshard_copy_rows_kernel, std::min(ng, caps.rows_grid), kBlock, 0, stream, items,
+                            idx + na + ns, ng, p->d_ptrs, p->d_grp_start, p->d_mem_ptr, p->d_mem_off, wait_last));
       ++p->last_launches;
     } else if (ng > 0) {
-      RS_CUDA(launch_kernel(true, reshard_copy_kernel, std::min(ng, caps.copy_grid), kBlock, 0, stream, items, idx + na, ng,
-                            p->d_ptrs, p->d_grp_start, p->d_mem_ptr, p->d_mem_off, wait_last));
+      RS_CUDA(launch_kernel(true, reshard_copy_kernel, std::min(ng, caps.copy_grid), kBlock, 0, stream, items,
+                            idx + na + ns, ng, p->d_ptrs, p->d_grp_start, p->d_mem_ptr, p->d_mem_off, wait_last));
       ++p->last_launches;
     }
   }
@@ -1454,76 +1634,240 @@ void free_device(reshard_plan_t *p) {
 
 using namespace reshard;
 
+namespace reshard {
+namespace {
+
+// Entries of the pointer table that one call provides: (index, caller's value).
+typedef std::vector<std::pair<int64_t, uint64_t>> PtrUpdate;
+
+void provide_sources(const reshard_plan_t *p, void *const *src_ptrs, PtrUpdate &u) {
+  for (int64_t i = 0; i < p->n_src_ptrs; ++i) u.emplace_back(i, reinterpret_cast<uint64_t>(src_ptrs[i]));
+}
+
+void provide_destinations(const reshard_plan_t *p, void *const *dst_ptrs, bool quant, PtrUpdate &u) {
+  const int64_t Ns = p->n_src_ptrs, Nd = p->n_dst_ptrs;
+  for (int64_t i = 0; i < Nd; ++i) {
+    u.emplace_back(Ns + i, reinterpret_cast<uint64_t>(quant ? dst_ptrs[2 * i] : dst_ptrs[i]));
+    u.emplace_back(Ns + Nd + i, quant ? reinterpret_cast<uint64_t>(dst_ptrs[2 * i + 1]) : 0);
+  }
+}
+
+// Every entry the passes `sets` dereference is non-NULL in `u` (scales too under quant).
+int check_used(const reshard_plan_t *p, const PtrUpdate &u, std::initializer_list<int> sets, bool quant) {
+  const int64_t Ns = p->n_src_ptrs, Nd = p->n_dst_ptrs;
+  std::vector<uint64_t> val((size_t)pointer_table_size(p), 0);
+  std::vector<char> given((size_t)pointer_table_size(p), 0);
+  for (const auto &e : u) {
+    val[(size_t)e.first] = e.second;
+    given[(size_t)e.first] = 1;
+  }
+  std::string missing;
+  int n = 0;
+  auto need = [&](int64_t i) {
+    if ((!given[(size_t)i] || !val[(size_t)i]) && n++ < 8) missing += "\n  " + entry_name(i, Ns, Nd) + " is NULL";
+  };
+  for (int set : sets) {
+    for (int32_t i : p->used_src[set]) need(i);
+    for (int32_t i : p->used_dst[set]) {
+      need(i);
+      if (quant && set != kPack) need(i + Nd);
+    }
+  }
+  if (n) return fail(RESHARD_ERR_INVALID_ARG, std::to_string(n) + " NULL pointer(s) the kernels need:" + missing);
+  return RESHARD_OK;
+}
+
+// Bring the device pointer table up to date with the entries this call provides (entries it
+// does not provide keep their values; the passes it runs do not read them). Changed entries are
+// checked first, so a refused pointer leaves the table as it was.
+int stage_pointers(reshard_plan_t *p, const PtrUpdate &u, cudaStream_t stream) {
+  const size_t n = (size_t)pointer_table_size(p);
+  if (p->ptr_cache.size() != n) {
+    p->ptr_cache.assign(n, 0);
+    p->dev_ptrs.assign(n, 0);
+    p->ptr_host.assign(n, 0);
+    p->ptr_cache_valid = false;
+  }
+  const int64_t Ns = p->n_src_ptrs, Nd = p->n_dst_ptrs;
+  std::vector<std::pair<int64_t, std::pair<uint64_t, uint8_t>>> changed;
+  std::string bad;
+  int n_bad = 0;
+  for (const auto &e : u) {
+    if (p->ptr_cache_valid && p->ptr_cache[(size_t)e.first] == e.second) continue;
+    uint64_t dv;
+    uint8_t host;
+    const char *why = check_entry(p->device, e.second, &dv, &host);
+    if (why) {
+      if (n_bad++ < 8) {
+        char addr[32];
+        std::snprintf(addr, sizeof addr, "0x%llx", (unsigned long long)e.second);
+        bad += "\n  " + entry_name(e.first, Ns, Nd) + " (" + addr + ") " + why;
+      }
+      continue;
+    }
+    changed.emplace_back(e.first, std::make_pair(dv, host));
+  }
+  if (n_bad) return fail(RESHARD_ERR_INVALID_ARG, std::to_string(n_bad) + " pointer(s) the device cannot dereference:" + bad);
+  if (changed.empty() && p->ptr_cache_valid) return RESHARD_OK;
+  for (const auto &e : u) p->ptr_cache[(size_t)e.first] = e.second;
+  for (const auto &c : changed) {
+    p->dev_ptrs[(size_t)c.first] = c.second.first;
+    p->ptr_host[(size_t)c.first] = c.second.second;
+  }
+  // pageable source: the runtime stages the bytes before returning, so the table may change
+  RS_CUDA(cudaMemcpyAsync(p->d_ptrs, p->dev_ptrs.data(), n * sizeof(uint64_t), cudaMemcpyHostToDevice, stream));
+  int rc = encode_maps(p, p->dev_ptrs, p->ptr_host, stream);
+  if (rc) return rc;
+  p->any_host = std::find(p->ptr_host.begin(), p->ptr_host.end(), 1) != p->ptr_host.end();
+  ++p->ptr_version;
+  p->ptr_cache_valid = true;
+  return RESHARD_OK;
+}
+
+// Completion of this call's work on `stream`, for destroy to wait on (not under stream capture:
+// a captured execute runs when its graph is replayed, and the plan must outlive the graph).
+void record_done(reshard_plan_t *p, cudaStream_t stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return;
+  }
+  if (cs != cudaStreamCaptureStatusNone) return;
+  for (auto &e : p->done_events)
+    if (e.first == static_cast<void *>(stream)) {
+      cudaEventRecord(static_cast<cudaEvent_t>(e.second), stream);
+      return;
+    }
+  // forget streams whose last execute has finished, then track this one
+  for (size_t i = 0; i < p->done_events.size();) {
+    cudaEvent_t ev = static_cast<cudaEvent_t>(p->done_events[i].second);
+    if (cudaEventQuery(ev) == cudaSuccess) {
+      cudaEventDestroy(ev);
+      p->done_events.erase(p->done_events.begin() + (long)i);
+    } else {
+      (void)cudaGetLastError();
+      ++i;
+    }
+  }
+  cudaEvent_t ev = nullptr;
+  if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return;
+  }
+  cudaEventRecord(ev, stream);
+  p->done_events.emplace_back(static_cast<void *>(stream), static_cast<void *>(ev));
+}
+
+int check_mode_quant(const reshard_plan_t *p, int quant) {
+  if (quant != RESHARD_QUANT_NONE && quant != RESHARD_QUANT_MXFP8) return fail(RESHARD_ERR_INVALID_ARG, "unknown quant");
+  if (quant == RESHARD_QUANT_MXFP8 && !p->quant_ok) return fail(RESHARD_ERR_UNSUPPORTED, p->quant_why);
+  return RESHARD_OK;
+}
+
+int check_message_buffer(const reshard_plan_t *p, const void *buf, int64_t bytes, const char *what) {
+  if (bytes <= 0) return RESHARD_OK;
+  if (!buf) return fail(RESHARD_ERR_INVALID_ARG, std::string(what) + " is NULL");
+  if (reinterpret_cast<uintptr_t>(buf) & 15) return fail(RESHARD_ERR_INVALID_ARG, std::string(what) + " is not 16-byte aligned");
+  (void)p;
+  return RESHARD_OK;
+}
+
+}  // namespace
+}  // namespace reshard
+
 extern "C" int reshard_execute(reshard_plan_t *p, void *const *src_ptrs, void *const *dst_ptrs, int mode, int quant,
                                reshard_stream_t stream_) {
   if (!p) return fail(RESHARD_ERR_INVALID_ARG, "plan is NULL");
+  if (p->rank >= 0)
+    return fail(RESHARD_ERR_INVALID_ARG, "a partitioned plan runs through reshard_execute_pack and reshard_execute_unpack");
   if (mode != RESHARD_DIRECT && mode != RESHARD_PACKED) return fail(RESHARD_ERR_INVALID_ARG, "unknown mode");
-  if (quant != RESHARD_QUANT_NONE && quant != RESHARD_QUANT_MXFP8) return fail(RESHARD_ERR_INVALID_ARG, "unknown quant");
-  if (quant == RESHARD_QUANT_MXFP8 && !p->quant_ok) return fail(RESHARD_ERR_UNSUPPORTED, p->quant_why);
+  int rc = check_mode_quant(p, quant);
+  if (rc) return rc;
   if (p->regions.empty()) return RESHARD_OK;
   if ((p->n_src_ptrs && !src_ptrs) || (p->n_dst_ptrs && !dst_ptrs))
     return fail(RESHARD_ERR_INVALID_ARG, "src_ptrs or dst_ptrs is NULL");
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-
-  // pointer table: [sources | destination data | destination scales | workspace]
-  const int64_t Ns = p->n_src_ptrs, Nd = p->n_dst_ptrs;
-  std::vector<uint64_t> table((size_t)pointer_table_size(p), 0);
-  std::string missing;
-  int n_missing = 0;
-  for (size_t ti = 0; ti < p->tensors.size(); ++ti) {
-    const TensorInfo &t = p->tensors[ti];
-    for (int64_t r = 0; r < t.n_src; ++r) {
-      void *ptr = src_ptrs[t.src_base + r];
-      table[(size_t)(t.src_base + r)] = reinterpret_cast<uint64_t>(ptr);
-      const Box &b = t.src_box[(size_t)r];
-      bool empty = false;
-      for (int d = 0; d < t.ndim; ++d) empty = empty || b.hi[d] <= b.lo[d];
-      if (!ptr && !empty && n_missing++ < 8)
-        missing += "\n  tensor " + std::to_string(ti) + ": source pointer " + std::to_string(r) + " is NULL";
-    }
-    for (int64_t r = 0; r < t.n_dst; ++r) {
-      const int64_t flat = t.dst_base + r;
-      void *data = quant ? dst_ptrs[2 * flat] : dst_ptrs[flat];
-      void *scale = quant ? dst_ptrs[2 * flat + 1] : nullptr;
-      table[(size_t)(Ns + flat)] = reinterpret_cast<uint64_t>(data);
-      table[(size_t)(Ns + Nd + flat)] = reinterpret_cast<uint64_t>(scale);
-      const Box &b = t.dst_box[(size_t)r];
-      bool empty = false;
-      for (int d = 0; d < t.ndim; ++d) empty = empty || b.hi[d] <= b.lo[d];
-      if (!empty && (!data || (quant && !scale)) && n_missing++ < 8)
-        missing += "\n  tensor " + std::to_string(ti) + ": destination pointer " + std::to_string(r) + " is NULL";
-    }
+  const bool q = quant == RESHARD_QUANT_MXFP8;
+  PtrUpdate u;
+  provide_sources(p, src_ptrs, u);
+  provide_destinations(p, dst_ptrs, q, u);
+  if (mode == RESHARD_DIRECT) {
+    if ((rc = check_used(p, u, {kDirect}, q))) return rc;
+  } else if ((rc = check_used(p, u, {kPack, kUnpack}, q))) {
+    return rc;
   }
-  if (n_missing) return fail(RESHARD_ERR_INVALID_ARG, std::to_string(n_missing) + " NULL pointer(s):" + missing);
-
-  int rc = bind_device(p);
-  if (rc) return rc;
+  if ((rc = bind_device(p))) return rc;
   LaunchCaps caps;
   if ((rc = launch_caps(p->device, caps))) return rc;
-  if (mode == RESHARD_PACKED && !p->d_workspace && p->stats.message_bytes > 0)
-    RS_CUDA(cudaMalloc(&p->d_workspace, (size_t)p->stats.message_bytes));
-  table[(size_t)p->workspace_ptr] = reinterpret_cast<uint64_t>(p->d_workspace);
-
-  if (!p->ptr_cache_valid || p->ptr_cache != table) {
-    p->ptr_cache_valid = false;
-    std::vector<uint64_t> dev_table = table;
-    std::vector<uint8_t> host;
-    if ((rc = check_pointers(p, dev_table, host))) return rc;
-    // pageable source: the runtime stages the bytes before returning, so `dev_table` may die
-    RS_CUDA(cudaMemcpyAsync(p->d_ptrs, dev_table.data(), dev_table.size() * sizeof(uint64_t), cudaMemcpyHostToDevice,
-                            stream));
-    if ((rc = encode_maps(p, dev_table, host, stream))) return rc;
-    p->any_host = std::find(host.begin(), host.end(), 1) != host.end();
-    p->dev_ptrs = std::move(dev_table);
-    p->ptr_cache = std::move(table);
-    ++p->ptr_version;
-    p->ptr_cache_valid = true;
+  if (mode == RESHARD_PACKED) {
+    if (!p->d_workspace && p->stats.message_bytes > 0) RS_CUDA(cudaMalloc(&p->d_workspace, (size_t)p->stats.message_bytes));
+    u.emplace_back(p->workspace_ptr, reinterpret_cast<uint64_t>(p->d_workspace));
+    u.emplace_back(p->workspace_ptr + 1, reinterpret_cast<uint64_t>(p->d_workspace));
   }
-  const bool q = quant == RESHARD_QUANT_MXFP8;
+  if ((rc = stage_pointers(p, u, stream))) return rc;
   p->last_launches = 0;
-  if (mode == RESHARD_DIRECT) return launch(p, kDirect, q, stream, caps);
-  if ((rc = launch(p, kPack, false, stream, caps))) return rc;
-  return launch(p, kUnpack, q, stream, caps);
+  if (mode == RESHARD_DIRECT) {
+    rc = launch(p, kDirect, q, stream, caps);
+  } else if (!(rc = launch(p, kPack, false, stream, caps))) {
+    rc = launch(p, kUnpack, q, stream, caps);
+  }
+  if (!rc) record_done(p, stream);
+  return rc;
+}
+
+extern "C" int reshard_execute_pack(reshard_plan_t *p, void *const *src_ptrs, void *const *dst_ptrs, void *send_buf,
+                                    int quant, reshard_stream_t stream_) {
+  if (!p) return fail(RESHARD_ERR_INVALID_ARG, "plan is NULL");
+  int rc = check_mode_quant(p, quant);
+  if (rc) return rc;
+  const bool q = quant == RESHARD_QUANT_MXFP8;
+  if (p->rank < 0 && q) return fail(RESHARD_ERR_INVALID_ARG, "packing an unpartitioned plan does not quantize");
+  // an unpartitioned plan's direct table is reshard_execute's; only a partition's is local copies
+  const bool direct = p->rank >= 0 && (!p->items[kDirect].empty() || !p->titems[kDirect].empty());
+  const bool pack = !p->items[kPack].empty() || !p->titems[kPack].empty();
+  if (!direct && !pack) return RESHARD_OK;
+  if (p->n_src_ptrs && !src_ptrs) return fail(RESHARD_ERR_INVALID_ARG, "src_ptrs is NULL");
+  if (direct && p->n_dst_ptrs && !dst_ptrs) return fail(RESHARD_ERR_INVALID_ARG, "dst_ptrs is NULL");
+  if (pack && (rc = check_message_buffer(p, send_buf, p->stats.message_bytes, "send_buf"))) return rc;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  PtrUpdate u;
+  provide_sources(p, src_ptrs, u);
+  if (dst_ptrs) provide_destinations(p, dst_ptrs, q, u);
+  if ((rc = direct ? check_used(p, u, {kDirect, kPack}, q) : check_used(p, u, {kPack}, q))) return rc;
+  if ((rc = bind_device(p))) return rc;
+  LaunchCaps caps;
+  if ((rc = launch_caps(p->device, caps))) return rc;
+  u.emplace_back(p->workspace_ptr, reinterpret_cast<uint64_t>(send_buf));
+  if ((rc = stage_pointers(p, u, stream))) return rc;
+  p->last_launches = 0;
+  if (direct && (rc = launch(p, kDirect, q, stream, caps))) return rc;
+  if (pack && (rc = launch(p, kPack, false, stream, caps))) return rc;
+  record_done(p, stream);
+  return RESHARD_OK;
+}
+
+extern "C" int reshard_execute_unpack(reshard_plan_t *p, const void *recv_buf, void *const *dst_ptrs, int quant,
+                                      reshard_stream_t stream_) {
+  if (!p) return fail(RESHARD_ERR_INVALID_ARG, "plan is NULL");
+  int rc = check_mode_quant(p, quant);
+  if (rc) return rc;
+  if (p->items[kUnpack].empty() && p->titems[kUnpack].empty()) return RESHARD_OK;
+  if (p->n_dst_ptrs && !dst_ptrs) return fail(RESHARD_ERR_INVALID_ARG, "dst_ptrs is NULL");
+  if ((rc = check_message_buffer(p, recv_buf, p->stats.recv_bytes, "recv_buf"))) return rc;
+  const bool q = quant == RESHARD_QUANT_MXFP8;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  PtrUpdate u;
+  provide_destinations(p, dst_ptrs, q, u);
+  if ((rc = check_used(p, u, {kUnpack}, q))) return rc;
+  if ((rc = bind_device(p))) return rc;
+  LaunchCaps caps;
+  if ((rc = launch_caps(p->device, caps))) return rc;
+  u.emplace_back(p->workspace_ptr + 1, reinterpret_cast<uint64_t>(recv_buf));
+  if ((rc = stage_pointers(p, u, stream))) return rc;
+  p->last_launches = 0;
+  if ((rc = launch(p, kUnpack, q, stream, caps))) return rc;
+  record_done(p, stream);
+  return RESHARD_OK;
 }
 
 extern "C" int reshard_plan_status(reshard_plan_t *p, int32_t *status, int reset) {
@@ -1547,10 +1891,20 @@ extern "C" int reshard_plan_destroy(reshard_plan_t *p) {
     int cur = 0;
     cudaGetDevice(&cur);
     cudaSetDevice(p->device);
-    // executes of this plan may still be queued on any stream (a garbage-collected handle, for
-    // instance): let the device finish before its tables and workspace go
-    cudaDeviceSynchronize();
+    // Executes of this plan may still be queued (a garbage-collected handle, for instance): wait
+    // for the last one on every stream it used, not for the whole device. Relaxed capture mode
+    // keeps these waits and frees from invalidating a stream capture another thread runs.
+    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+    const bool swapped = cudaThreadExchangeStreamCaptureMode(&mode) == cudaSuccess;
+    for (auto &e : p->done_events) {
+      cudaEvent_t ev = static_cast<cudaEvent_t>(e.second);
+      cudaEventSynchronize(ev);
+      cudaEventDestroy(ev);
+    }
+    p->done_events.clear();
     free_device(p);
+    if (swapped) cudaThreadExchangeStreamCaptureMode(&mode);
+    (void)cudaGetLastError();
     cudaSetDevice(cur);
   }
   delete p;
@@ -1578,6 +1932,11 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_static_mu;
 uint8_t *g_static_addr[kMaxDevices] = {};
+// the pointers of the last call on each device that passed the reachability check (host memory)
+struct StaticCheck {
+  std::vector<uint64_t> given, dev;
+};
+StaticCheck g_static_check[kMaxDevices];
 
 // Device address of the scratch array on device `dev` (which must be current). The host-side
 // name of a __device__ array is not a device address, so it is looked up once per device with
@@ -1604,23 +1963,10 @@ extern "C" int reshard_execute_static(const reshard_plan_t *p, void *const *src_
                                       reshard_stream_t stream_) {
   using namespace reshard;
   if (!p) return fail(RESHARD_ERR_INVALID_ARG, "plan is NULL");
-  if (p->regions.empty()) return RESHARD_OK;
-  if ((p->n_src_ptrs && !src_ptrs) || (p->n_dst_ptrs && !dst_ptrs))
-    return fail(RESHARD_ERR_INVALID_ARG, "src_ptrs or dst_ptrs is NULL");
+  if (p->rank >= 0)
+    return fail(RESHARD_ERR_INVALID_ARG, "a partitioned plan runs through reshard_execute_pack and reshard_execute_unpack");
   if (!p->titems[kDirect].empty())
     return fail(RESHARD_ERR_UNSUPPORTED, "plans with transposing regions need reshard_execute (TMA tensor maps)");
-  for (const TensorInfo &t : p->tensors) {
-    for (int side = 0; side < 2; ++side) {
-      const int64_t n = side ? t.n_dst : t.n_src;
-      for (int64_t r = 0; r < n; ++r) {
-        const Box &b = side ? t.dst_box[(size_t)r] : t.src_box[(size_t)r];
-        bool empty = false;
-        for (int d = 0; d < t.ndim; ++d) empty = empty || b.hi[d] <= b.lo[d];
-        void *ptr = side ? dst_ptrs[t.dst_base + r] : src_ptrs[t.src_base + r];
-        if (!empty && !ptr) return fail(RESHARD_ERR_INVALID_ARG, "a pointer of a non-empty shard is NULL");
-      }
-    }
-  }
   // scratch layout: items | group starts | member pointers | member offsets | pointer table
   const std::vector<Item> &items = p->items[kDirect];
   const size_t b_items = items.size() * sizeof(Item);
@@ -1635,11 +1981,53 @@ extern "C" int reshard_execute_static(const reshard_plan_t *p, void *const *src_
                                              " bytes of descriptor scratch; reshard_execute_static holds at most " +
                                              std::to_string((size_t)RESHARD_STATIC_SCRATCH_BYTES) +
                                              " (split the batch or use reshard_execute)");
+  if (!p->regions.empty() && ((p->n_src_ptrs && !src_ptrs) || (p->n_dst_ptrs && !dst_ptrs)))
+    return fail(RESHARD_ERR_INVALID_ARG, "src_ptrs or dst_ptrs is NULL");
+  PtrUpdate u;
+  if (!p->regions.empty()) {
+    provide_sources(p, src_ptrs, u);
+    for (int64_t i = 0; i < p->n_dst_ptrs; ++i)
+      u.emplace_back(p->n_src_ptrs + i, reinterpret_cast<uint64_t>(dst_ptrs[i]));
+    int rc = check_used(p, u, {kDirect}, false);
+    if (rc) return rc;
+  }
+  // set-up on every call, an empty plan's too: the array's device address on this device (the
+  // lookup loads the library's device code here, which reserves the array)
   int dev = 0;
   RS_CUDA(cudaGetDevice(&dev));
   uint8_t *base = nullptr;
   int rc = static_scratch(dev, &base);
   if (rc) return rc;
+  if (p->regions.empty()) return RESHARD_OK;
+  // the pointers the kernel will dereference must be reachable from this device, as for
+  // reshard_execute; the last validated table (per device) is remembered, so repeated calls with
+  // the same pointers skip the per-pointer queries
+  std::vector<uint64_t> table((size_t)pointer_table_size(p), 0);
+  {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    std::vector<uint64_t> given((size_t)(p->n_src_ptrs + p->n_dst_ptrs));
+    for (size_t k = 0; k < given.size(); ++k) given[k] = u[k].second;
+    StaticCheck &c = g_static_check[dev];
+    if (c.given != given) {
+      std::string bad;
+      int n_bad = 0;
+      std::vector<uint64_t> devp(given.size());
+      for (size_t k = 0; k < given.size(); ++k) {
+        uint8_t host;
+        const char *why = check_entry(dev, given[k], &devp[k], &host);
+        if (why && n_bad++ < 8) {
+          char addr[32];
+          std::snprintf(addr, sizeof addr, "0x%llx", (unsigned long long)given[k]);
+          bad += "\n  " + entry_name((int64_t)k, p->n_src_ptrs, p->n_dst_ptrs) + " (" + addr + ") " + why;
+        }
+      }
+      if (n_bad)
+        return fail(RESHARD_ERR_INVALID_ARG, std::to_string(n_bad) + " pointer(s) the device cannot dereference:" + bad);
+      c.given = std::move(given);
+      c.dev = std::move(devp);
+    }
+    std::copy(c.dev.begin(), c.dev.end(), table.begin());
+  }
   LaunchCaps caps;
   if ((rc = launch_caps(dev, caps))) return rc;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -1649,12 +2037,8 @@ extern "C" int reshard_execute_static(const reshard_plan_t *p, void *const *src_
   RS_CUDA(cudaMemcpyAsync(base + o_mp, p->mem_ptr.data(), b_mp, cudaMemcpyHostToDevice, stream));
   RS_CUDA(cudaMemcpyAsync(base + o_mo, p->mem_off.data(), b_mo, cudaMemcpyHostToDevice, stream));
   // pointer table [sources | destinations | ...]: the direct copy reads only these two runs
-  if (p->n_src_ptrs)
-    RS_CUDA(cudaMemcpyAsync(base + o_pt, src_ptrs, (size_t)p->n_src_ptrs * sizeof(void *), cudaMemcpyHostToDevice,
-                            stream));
-  if (p->n_dst_ptrs)
-    RS_CUDA(cudaMemcpyAsync(base + o_pt + (size_t)p->n_src_ptrs * sizeof(uint64_t), dst_ptrs,
-                            (size_t)p->n_dst_ptrs * sizeof(void *), cudaMemcpyHostToDevice, stream));
+  RS_CUDA(cudaMemcpyAsync(base + o_pt, table.data(), (size_t)(p->n_src_ptrs + p->n_dst_ptrs) * sizeof(uint64_t),
+                          cudaMemcpyHostToDevice, stream));
   const int n = (int)items.size();
   const int grid = std::min(n, caps.copy_grid);
   reshard_copy_kernel<<<grid, kBlock, 0, stream>>>(

@@ -35,7 +35,7 @@ int fail(int code, const std::string &msg) {
   return code;
 }
 
-int64_t pointer_table_size(const reshard_plan *p) { return p->n_src_ptrs + 2 * p->n_dst_ptrs + 1; }
+int64_t pointer_table_size(const reshard_plan *p) { return p->n_src_ptrs + 2 * p->n_dst_ptrs + 2; }
 
 namespace {
 
@@ -399,13 +399,11 @@ void emit_region(int nd, const int64_t *ext, int64_t so, const int64_t *sa, cons
   emit_items(m, pe, so, pa, dof, pb, ra.ptr, group, esize, item_bytes, out);
 }
 
-int build(const reshard_tensor_spec_t *specs, int n, reshard_plan_t **out) {
-  if (!out) return fail(RESHARD_ERR_INVALID_ARG, "out is NULL");
-  *out = nullptr;
+// Steps 1 and 2: validation, every rank's box and view, replica groups, intersections and the
+// source of every region. Fills plan->tensors, regions, groups and the MXFP8 eligibility.
+int plan_regions(const reshard_tensor_spec_t *specs, int n, reshard_plan *plan) {
   if (n < 0 || (n > 0 && !specs)) return fail(RESHARD_ERR_INVALID_ARG, "specs is NULL or n_tensors < 0");
   Violations v;
-  std::unique_ptr<reshard_plan> owner(new reshard_plan());
-  reshard_plan *plan = owner.get();
   plan->tensors.resize((size_t)n);
 
   // 1. validate every tensor and compute every rank's box and view
@@ -468,10 +466,12 @@ int build(const reshard_tensor_spec_t *specs, int n, reshard_plan_t **out) {
     }
     // source groups: identical boxes hold identical data; the lowest pointer index supplies
     std::map<BoxKey, int32_t> src_rep;
+    t.src_rep.assign((size_t)t.n_src, -1);
     for (int64_t p = 0; p < t.n_src; ++p) {
       if (volume(t.src_box[(size_t)p], nd) == 0) continue;
       auto k = key_of(t.src_box[(size_t)p]);
       if (!src_rep.count(k)) src_rep[k] = (int32_t)p;
+      t.src_rep[(size_t)p] = src_rep[k];
     }
     std::vector<int32_t> reps;
     for (auto &kv : src_rep) reps.push_back(kv.second);
@@ -529,28 +529,28 @@ int build(const reshard_tensor_spec_t *specs, int n, reshard_plan_t **out) {
     }
   }
   if (n == 0) plan->quant_ok = true;
+  return RESHARD_OK;
+}
 
-  // 3. packed-mode message layout: one message per (source rank, destination group members),
-  //    regions in plan order inside a message, each starting on a 16-byte boundary
-  std::map<std::pair<int32_t, std::vector<int32_t>>, std::vector<size_t>> messages;
-  for (size_t i = 0; i < plan->regions.size(); ++i) {
-    const Region &r = plan->regions[i];
-    messages[std::make_pair(r.src, plan->groups[(size_t)r.group].members)].push_back(i);
-  }
-  int64_t msg_bytes = 0;
-  for (auto &kv : messages)
-    for (size_t i : kv.second) {
-      Region &r = plan->regions[i];
-      const TensorInfo &t = plan->tensors[(size_t)r.tensor];
-      r.msg_off_bytes = msg_bytes;
-      msg_bytes += (volume(r.box, t.ndim) * t.esize + 15) / 16 * 16;
-    }
+int64_t region_bytes(const reshard_plan &p, const Region &r) {
+  const TensorInfo &t = p.tensors[(size_t)r.tensor];
+  return volume(r.box, t.ndim) * t.esize;
+}
 
-  // 4. group table (device layout) and the workspace pseudo-group
+int64_t align16(int64_t x) { return (x + 15) / 16 * 16; }
+
+// Steps 4 and 5: the device group table (the given replica sets plus the send-buffer group) and
+// the work items of the three passes, each region as its role says. `dev_groups` are replica
+// sets of destination pointer indices within a tensor's run; a role's group indexes them.
+int emit_tables(reshard_plan *plan, const std::vector<Role> &roles, const std::vector<Group> &dev_groups) {
   const int64_t Ns = plan->n_src_ptrs, Nd = plan->n_dst_ptrs;
   plan->workspace_ptr = Ns + 2 * Nd;
-  plan->grp_start.push_back(0);
-  for (const Group &g : plan->groups) {
+  const int32_t recv_ptr = (int32_t)(plan->workspace_ptr + 1);
+  plan->grp_start.assign(1, 0);
+  plan->mem_ptr.clear();
+  plan->mem_off.clear();
+  plan->max_fanout = 0;
+  for (const Group &g : dev_groups) {
     const TensorInfo &t = plan->tensors[(size_t)g.tensor];
     for (int32_t m : g.members) {
       plan->mem_ptr.push_back((int32_t)(Ns + t.dst_base + m));
@@ -559,33 +559,29 @@ int build(const reshard_tensor_spec_t *specs, int n, reshard_plan_t **out) {
     plan->grp_start.push_back((int32_t)plan->mem_ptr.size());
     plan->max_fanout = std::max(plan->max_fanout, (int)g.members.size());
   }
-  plan->workspace_group = (int32_t)plan->groups.size();
+  plan->workspace_group = (int32_t)dev_groups.size();
   plan->mem_ptr.push_back((int32_t)plan->workspace_ptr);
   plan->mem_off.push_back(0);
   plan->grp_start.push_back((int32_t)plan->mem_ptr.size());
 
-  // 5. work items: direct (source -> destination replicas), pack (source -> message),
-  //    unpack (message -> destination replicas)
-  int64_t bytes_read = 0, bytes_written = 0, global_bytes = 0;
   int64_t plan_bytes = 0;
-  for (const Region &r : plan->regions)
-    plan_bytes += volume(r.box, plan->tensors[(size_t)r.tensor].ndim) * plan->tensors[(size_t)r.tensor].esize;
+  for (size_t i = 0; i < plan->regions.size(); ++i)
+    if (roles[i].direct >= 0 || roles[i].send_off >= 0 || roles[i].unpack >= 0) plan_bytes += region_bytes(*plan, plan->regions[i]);
   int64_t item_bytes = kMaxItemBytes;
   while (item_bytes > kMinItemBytes && plan_bytes / item_bytes < kItemsPerPlan) item_bytes /= 2;
   std::map<SlabSpec, int32_t> slab_ids;
-  for (const Region &r : plan->regions) {
+  for (size_t i = 0; i < plan->regions.size(); ++i) {
+    const Region &r = plan->regions[i];
+    const Role &role = roles[i];
     const TensorInfo &t = plan->tensors[(size_t)r.tensor];
     const int nd = t.ndim;
     const Box &sb = t.src_box[(size_t)r.src];
-    const Group &g = plan->groups[(size_t)r.group];
     const RankView &sv = t.src_view[(size_t)r.src];
-    const RankView &dv = t.dst_view[(size_t)g.members[0]];
     int64_t ext[kMaxDims], ms[kMaxDims];
-    int64_t so = sv.offset, dof = 0;
+    int64_t so = sv.offset;
     for (int d = 0; d < nd; ++d) {
       ext[d] = r.box.hi[d] - r.box.lo[d];
       so += (r.box.lo[d] - sb.lo[d]) * sv.strides[d];
-      dof += (r.box.lo[d] - g.box.lo[d]) * dv.strides[d];
     }
     int64_t dd = 1;
     for (int d = nd - 1; d >= 0; --d) {
@@ -593,23 +589,39 @@ int build(const reshard_tensor_spec_t *specs, int n, reshard_plan_t **out) {
       dd *= ext[d];
     }
     const int32_t sp = (int32_t)(t.src_base + r.src);
-    const int64_t mo = r.msg_off_bytes / t.esize;
     int64_t slo[kMaxDims], sext[kMaxDims], zero[kMaxDims] = {0, 0, 0, 0};
     for (int d = 0; d < nd; ++d) {
       slo[d] = r.box.lo[d] - sb.lo[d];
       sext[d] = sb.hi[d] - sb.lo[d];
     }
     const ReadSide from_src{sp, sv.offset, slo, sext};
-    const ReadSide from_msg{(int32_t)plan->workspace_ptr, mo, zero, ext};
-    emit_region(nd, ext, so, sv.strides, from_src, dof, dv.strides, r.group, t.esize, item_bytes,
-                plan->items[kDirect], plan->titems[kDirect], slab_ids, plan->slabs);
-    emit_region(nd, ext, so, sv.strides, from_src, mo, ms, plan->workspace_group, t.esize, item_bytes,
-                plan->items[kPack], plan->titems[kPack], slab_ids, plan->slabs);
-    emit_region(nd, ext, mo, ms, from_msg, dof, dv.strides, r.group, t.esize, item_bytes, plan->items[kUnpack],
-                plan->titems[kUnpack], slab_ids, plan->slabs);
-    const int64_t b = volume(r.box, nd) * t.esize;
-    bytes_read += b;
-    bytes_written += b * (int64_t)g.members.size();
+    // destination offset and strides of a device group (all members share the strides)
+    auto dst_side = [&](int32_t dg, int64_t &dof) -> const int64_t * {
+      const Group &g = dev_groups[(size_t)dg];
+      const RankView &dv = t.dst_view[(size_t)g.members[0]];
+      dof = 0;
+      for (int d = 0; d < nd; ++d) dof += (r.box.lo[d] - g.box.lo[d]) * dv.strides[d];
+      return dv.strides;
+    };
+    if (role.direct >= 0) {
+      int64_t dof;
+      const int64_t *ds = dst_side(role.direct, dof);
+      emit_region(nd, ext, so, sv.strides, from_src, dof, ds, role.direct, t.esize, item_bytes, plan->items[kDirect],
+                  plan->titems[kDirect], slab_ids, plan->slabs);
+    }
+    if (role.send_off >= 0) {
+      const int64_t mo = role.send_off / t.esize;
+      emit_region(nd, ext, so, sv.strides, from_src, mo, ms, plan->workspace_group, t.esize, item_bytes,
+                  plan->items[kPack], plan->titems[kPack], slab_ids, plan->slabs);
+    }
+    if (role.unpack >= 0) {
+      const int64_t mo = role.recv_off / t.esize;
+      const ReadSide from_msg{recv_ptr, mo, zero, ext};
+      int64_t dof;
+      const int64_t *ds = dst_side(role.unpack, dof);
+      emit_region(nd, ext, mo, ms, from_msg, dof, ds, role.unpack, t.esize, item_bytes, plan->items[kUnpack],
+                  plan->titems[kUnpack], slab_ids, plan->slabs);
+    }
   }
 #if RESHARD_SIZE_ORDER
   // largest items first: the persistent grid deals items round-robin, so CTAs finish together
@@ -622,28 +634,315 @@ int build(const reshard_tensor_spec_t *specs, int n, reshard_plan_t **out) {
   // transposing kernel per element size present, each over a contiguous run of the table
   for (auto &tv : plan->titems)
     std::stable_sort(tv.begin(), tv.end(), [](const TItem &a, const TItem &b) { return a.esize < b.esize; });
+
+  // pointer-table entries each pass reads (sources) and writes (destinations)
+  for (int set = 0; set < kNumSets; ++set) {
+    std::vector<char> s_used((size_t)Ns, 0), d_used((size_t)Nd, 0);
+    auto note = [&](int32_t src, int32_t group) {
+      if (src < Ns) s_used[(size_t)src] = 1;
+      for (int32_t k = plan->grp_start[(size_t)group]; k < plan->grp_start[(size_t)group + 1]; ++k) {
+        const int32_t q = plan->mem_ptr[(size_t)k];
+        if (q >= Ns && q < Ns + Nd) d_used[(size_t)(q - Ns)] = 1;
+      }
+    };
+    for (const Item &it : plan->items[set]) note(it.src, it.group);
+    for (const TItem &it : plan->titems[set]) note(it.src, it.group);
+    plan->used_src[set].clear();
+    plan->used_dst[set].clear();
+    for (int64_t i = 0; i < Ns; ++i)
+      if (s_used[(size_t)i]) plan->used_src[set].push_back((int32_t)i);
+    for (int64_t i = 0; i < Nd; ++i)
+      if (d_used[(size_t)i]) plan->used_dst[set].push_back((int32_t)(Ns + i));
+  }
+
+  int64_t global_bytes = 0;
   for (const TensorInfo &t : plan->tensors) {
     int64_t v2 = t.esize;
     for (int d = 0; d < t.ndim; ++d) v2 *= t.shape[d];
     global_bytes += v2;
   }
-
   reshard_stats_t &st = plan->stats;
-  st.n_tensors = n;
+  st.n_tensors = (int64_t)plan->tensors.size();
   st.regions = (int64_t)plan->regions.size();
   st.items = (int64_t)(plan->items[kDirect].size() + plan->titems[kDirect].size());
   st.dst_groups = (int64_t)plan->groups.size();
+  st.gather_bcast_bytes = 2 * global_bytes;
+  st.global_bytes = global_bytes;
+  st.rank = plan->rank;
+  st.world = plan->world;
+  if ((int64_t)(plan->items[kDirect].size() + plan->items[kPack].size() + plan->items[kUnpack].size() +
+                plan->titems[kDirect].size() + plan->titems[kPack].size() + plan->titems[kUnpack].size()) > INT32_MAX ||
+      (int64_t)plan->mem_ptr.size() > INT32_MAX || (int64_t)plan->slabs.size() > INT32_MAX ||
+      pointer_table_size(plan) > INT32_MAX) {
+    return fail(RESHARD_ERR_UNSUPPORTED, "plan too large (more than 2^31 items, members or pointers)");
+  }
+  return RESHARD_OK;
+}
+
+int build(const reshard_tensor_spec_t *specs, int n, reshard_plan_t **out) {
+  if (!out) return fail(RESHARD_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  std::unique_ptr<reshard_plan> owner(new reshard_plan());
+  reshard_plan *plan = owner.get();
+  int rc = plan_regions(specs, n, plan);
+  if (rc) return rc;
+
+  // 3. packed-mode message layout: one message per (source rank, destination group members),
+  //    regions in plan order inside a message, each starting on a 16-byte boundary
+  std::map<std::pair<int32_t, std::vector<int32_t>>, std::vector<size_t>> messages;
+  for (size_t i = 0; i < plan->regions.size(); ++i) {
+    const Region &r = plan->regions[i];
+    messages[std::make_pair(r.src, plan->groups[(size_t)r.group].members)].push_back(i);
+  }
+  int64_t msg_bytes = 0;
+  for (auto &kv : messages)
+    for (size_t i : kv.second) {
+      Region &r = plan->regions[i];
+      r.msg_off_bytes = msg_bytes;
+      msg_bytes += align16(region_bytes(*plan, r));
+    }
+
+  // every region: direct to its group, packed at its message offset, unpacked from the same
+  std::vector<Role> roles(plan->regions.size());
+  int64_t bytes_read = 0, bytes_written = 0;
+  for (size_t i = 0; i < plan->regions.size(); ++i) {
+    const Region &r = plan->regions[i];
+    roles[i] = Role{r.group, r.msg_off_bytes, r.group, r.msg_off_bytes};
+    const int64_t b = region_bytes(*plan, r);
+    bytes_read += b;
+    bytes_written += b * (int64_t)plan->groups[(size_t)r.group].members.size();
+  }
+  if ((rc = emit_tables(plan, roles, plan->groups))) return rc;
+  reshard_stats_t &st = plan->stats;
   st.messages = (int64_t)messages.size();
   st.bytes_read = bytes_read;
   st.bytes_written = bytes_written;
   st.wire_bytes = bytes_read;
   st.message_bytes = msg_bytes;
-  st.gather_bcast_bytes = 2 * global_bytes;
-  st.global_bytes = global_bytes;
-  if (st.items > INT32_MAX || (int64_t)plan->mem_ptr.size() > INT32_MAX || (int64_t)plan->slabs.size() > INT32_MAX ||
-      pointer_table_size(plan) > INT32_MAX) {
-    return fail(RESHARD_ERR_UNSUPPORTED, "plan too large (more than 2^31 items, members or pointers)");
+  st.recv_bytes = msg_bytes;
+  *out = owner.release();
+  set_error("");
+  return RESHARD_OK;
+}
+
+// The share of a plan that process `rank` runs when the shards are spread over `world`
+// processes (multi-GPU form of the method; see reshard_plan_partition in the header).
+int partition(const reshard_plan &g, const int32_t *src_owner, const int32_t *dst_owner, int world, int rank,
+              int flags, reshard_plan_t **out) {
+  *out = nullptr;
+  const int64_t Ns = g.n_src_ptrs, Nd = g.n_dst_ptrs;
+  {
+    Violations v;
+    if (g.rank >= 0) v.add(RESHARD_ERR_INVALID_ARG, "the plan is already partitioned");
+    if (world < 1) v.add(RESHARD_ERR_INVALID_ARG, "world must be >= 1");
+    if (rank < 0 || rank >= world) v.add(RESHARD_ERR_INVALID_ARG, "rank out of range 0..world-1");
+    if (flags & ~RESHARD_STRIPED) v.add(RESHARD_ERR_INVALID_ARG, "unknown flags");
+    if ((Ns && !src_owner) || (Nd && !dst_owner)) v.add(RESHARD_ERR_INVALID_ARG, "src_owner or dst_owner is NULL");
+    if (!v.lines.empty()) return v.report();
+    for (int64_t i = 0; i < Ns; ++i)
+      if (src_owner[i] < 0 || src_owner[i] >= world) {
+        v.add(RESHARD_ERR_INVALID_ARG, "src_owner[" + std::to_string(i) + "] is not a process of the group");
+        if (v.lines.size() >= 8) break;
+      }
+    for (int64_t i = 0; i < Nd; ++i)
+      if (dst_owner[i] < 0 || dst_owner[i] >= world) {
+        v.add(RESHARD_ERR_INVALID_ARG, "dst_owner[" + std::to_string(i) + "] is not a process of the group");
+        if (v.lines.size() >= 16) break;
+      }
+    if (!v.lines.empty()) return v.report();
   }
+  std::unique_ptr<reshard_plan> owner(new reshard_plan());
+  reshard_plan *plan = owner.get();
+  plan->tensors = g.tensors;
+  plan->groups = g.groups;
+  plan->n_src_ptrs = Ns;
+  plan->n_dst_ptrs = Nd;
+  plan->quant_ok = g.quant_ok;
+  plan->quant_why = g.quant_why;
+  plan->rank = rank;
+  plan->world = world;
+  const bool striped = (flags & RESHARD_STRIPED) != 0;
+
+  // source choice and message key of every region of the unpartitioned plan
+  typedef std::pair<int32_t, std::vector<int32_t>> MsgKey;  // (sender, other receivers, sorted)
+  struct Placed {
+    Region r;
+    int32_t sender;
+    std::vector<int32_t> recv;   // processes other than the sender holding a member
+    std::vector<int32_t> local;  // members held by `rank`
+  };
+  std::vector<Placed> placed;
+  placed.reserve(g.regions.size());
+  // holders of every source replica group, per tensor: rep pointer index -> holders (ascending)
+  std::vector<std::vector<std::vector<int32_t>>> holders(g.tensors.size());
+  for (size_t ti = 0; ti < g.tensors.size(); ++ti) {
+    const TensorInfo &t = g.tensors[ti];
+    holders[ti].resize((size_t)t.n_src);
+    for (int64_t p = 0; p < t.n_src; ++p)
+      if (t.src_rep[(size_t)p] >= 0) holders[ti][(size_t)t.src_rep[(size_t)p]].push_back((int32_t)p);
+  }
+  for (size_t i = 0; i < g.regions.size(); ++i) {
+    const Region &r = g.regions[i];
+    const TensorInfo &t = g.tensors[(size_t)r.tensor];
+    const Group &grp = g.groups[(size_t)r.group];
+    std::vector<int32_t> procs;
+    Placed pl;
+    for (int32_t m : grp.members) {
+      const int32_t q = dst_owner[t.dst_base + m];
+      procs.push_back(q);
+      if (q == rank) pl.local.push_back(m);
+    }
+    std::sort(procs.begin(), procs.end());
+    procs.erase(std::unique(procs.begin(), procs.end()), procs.end());
+    // holders of the region's source box: a holder on a receiving process keeps that copy local
+    const std::vector<int32_t> &hold = holders[(size_t)r.tensor][(size_t)r.src];
+    int32_t pick = -1;
+    for (int32_t h : hold)
+      if (std::binary_search(procs.begin(), procs.end(), src_owner[t.src_base + h])) {
+        pick = h;
+        break;
+      }
+    if (pick < 0) pick = hold[i % hold.size()];
+    pl.r = r;
+    pl.r.src = pick;
+    pl.sender = src_owner[t.src_base + pick];
+    for (int32_t q : procs)
+      if (q != pl.sender) pl.recv.push_back(q);
+    placed.push_back(std::move(pl));
+  }
+
+  // messages: (sender, receivers) -> regions in plan order, each 16-byte aligned
+  std::map<MsgKey, std::vector<size_t>> msgs;
+  for (size_t i = 0; i < placed.size(); ++i)
+    if (!placed[i].recv.empty()) msgs[MsgKey(placed[i].sender, placed[i].recv)].push_back(i);
+  std::vector<int64_t> in_msg(placed.size(), -1);
+  std::map<MsgKey, int64_t> msg_size;
+  for (auto &kv : msgs) {
+    int64_t off = 0;
+    for (size_t i : kv.second) {
+      in_msg[i] = off;
+      off += align16(region_bytes(g, placed[i].r));
+    }
+    msg_size[kv.first] = off;
+  }
+  // buffer layouts: every process's send and receive offsets of every message it takes part in
+  std::map<std::pair<int32_t, MsgKey>, int64_t> send_at, recv_at;
+  std::vector<int64_t> send_end((size_t)world, 0), recv_end((size_t)world, 0);
+  for (auto &kv : msg_size) {
+    const MsgKey &k = kv.first;
+    send_at[std::make_pair(k.first, k)] = send_end[(size_t)k.first];
+    send_end[(size_t)k.first] += kv.second;
+    for (int32_t q : k.second) {
+      recv_at[std::make_pair(q, k)] = recv_end[(size_t)q];
+      recv_end[(size_t)q] += kv.second;
+    }
+  }
+
+  // roles of this rank's regions; device groups are the members this rank holds
+  std::map<std::pair<int32_t, std::vector<int32_t>>, int32_t> dev_of;  // (semantic group, local members)
+  std::vector<Group> dev_groups;
+  auto dev_group = [&](const Placed &p) -> int32_t {
+    auto key = std::make_pair(p.r.group, p.local);
+    auto f = dev_of.find(key);
+    if (f != dev_of.end()) return f->second;
+    Group dg;
+    dg.tensor = p.r.tensor;
+    dg.box = g.groups[(size_t)p.r.group].box;
+    dg.members = p.local;
+    dev_groups.push_back(dg);
+    return dev_of[key] = (int32_t)dev_groups.size() - 1;
+  };
+  std::vector<Role> roles;
+  int64_t bytes_read = 0, bytes_written = 0, local_bytes = 0;
+  for (size_t i = 0; i < placed.size(); ++i) {
+    const Placed &p = placed[i];
+    Role role;
+    const int64_t b = region_bytes(g, p.r);
+    if (p.sender == rank && !p.local.empty()) {
+      role.direct = dev_group(p);
+      local_bytes += b;
+      bytes_read += b;
+      bytes_written += b * (int64_t)p.local.size();
+    }
+    if (!p.recv.empty()) {
+      const MsgKey k(p.sender, p.recv);
+      if (p.sender == rank) {
+        role.send_off = send_at[std::make_pair(rank, k)] + in_msg[i];
+        bytes_read += b;
+      }
+      if (std::binary_search(p.recv.begin(), p.recv.end(), rank)) {
+        role.unpack = dev_group(p);
+        role.recv_off = recv_at[std::make_pair(rank, k)] + in_msg[i];
+        bytes_written += b * (int64_t)p.local.size();
+      }
+    }
+    if (role.direct < 0 && role.send_off < 0 && role.unpack < 0) continue;
+    plan->regions.push_back(p.r);
+    roles.push_back(role);
+  }
+
+  // transfers, enumerated once for the whole group in message order, kept where `rank` takes part
+  int64_t sent = 0, forwarded = 0;
+  std::vector<Transfer> phase2;
+  for (auto &kv : msg_size) {
+    const MsgKey &k = kv.first;
+    const int64_t size = kv.second;
+    const int32_t s = k.first;
+    const std::vector<int32_t> &rv = k.second;
+    const int64_t R = (int64_t)rv.size();
+    const int64_t s_off = send_at[std::make_pair(s, k)];
+    if (!striped || R == 1) {
+      for (int32_t q : rv) {
+        const int64_t q_off = recv_at[std::make_pair(q, k)];
+        if (s == rank) {
+          plan->transfers.push_back(Transfer{q, RESHARD_SEND, RESHARD_SEND_BUF, 1, s_off, size});
+          sent += size;
+        }
+        if (q == rank) plan->transfers.push_back(Transfer{s, RESHARD_RECV, RESHARD_RECV_BUF, 1, q_off, size});
+      }
+      continue;
+    }
+    std::vector<int64_t> cut((size_t)R + 1);
+    for (int64_t j = 0; j <= R; ++j) cut[(size_t)j] = j == R ? size : (size * j / R) / 16 * 16;
+    for (int64_t j = 0; j < R; ++j) {
+      const int64_t lo = cut[(size_t)j], len = cut[(size_t)j + 1] - lo;
+      if (len <= 0) continue;
+      const int32_t qk = rv[(size_t)j];
+      const int64_t qk_off = recv_at[std::make_pair(qk, k)];
+      if (s == rank) {
+        plan->transfers.push_back(Transfer{qk, RESHARD_SEND, RESHARD_SEND_BUF, 1, s_off + lo, len});
+        sent += len;
+      }
+      if (qk == rank) plan->transfers.push_back(Transfer{s, RESHARD_RECV, RESHARD_RECV_BUF, 1, qk_off + lo, len});
+      for (int32_t qj : rv) {
+        if (qj == qk) continue;
+        const int64_t qj_off = recv_at[std::make_pair(qj, k)];
+        if (qk == rank) {
+          phase2.push_back(Transfer{qj, RESHARD_SEND, RESHARD_RECV_BUF, 2, qk_off + lo, len});
+          forwarded += len;
+        }
+        if (qj == rank) phase2.push_back(Transfer{qk, RESHARD_RECV, RESHARD_RECV_BUF, 2, qj_off + lo, len});
+      }
+    }
+  }
+  plan->transfers.insert(plan->transfers.end(), phase2.begin(), phase2.end());
+
+  int rc = emit_tables(plan, roles, dev_groups);
+  if (rc) return rc;
+  reshard_stats_t &st = plan->stats;
+  int64_t n_msgs = 0;
+  for (auto &kv : msg_size)
+    if (kv.first.first == rank || std::binary_search(kv.first.second.begin(), kv.first.second.end(), rank)) ++n_msgs;
+  st.messages = n_msgs;
+  st.bytes_read = bytes_read;
+  st.bytes_written = bytes_written;
+  st.wire_bytes = sent + forwarded;
+  st.message_bytes = send_end[(size_t)rank];
+  st.recv_bytes = recv_end[(size_t)rank];
+  st.transfers = (int64_t)plan->transfers.size();
+  st.sent_bytes = sent;
+  st.forwarded_bytes = forwarded;
+  st.local_bytes = local_bytes;
   *out = owner.release();
   set_error("");
   return RESHARD_OK;
@@ -739,6 +1038,32 @@ extern "C" int reshard_plan_blockwise_fp8(const reshard_tensor_spec_t *specs, in
   }
 }
 
+extern "C" int reshard_plan_partition(const reshard_plan_t *plan, const int32_t *src_owner, const int32_t *dst_owner,
+                                      int world, int rank, int flags, reshard_plan_t **out) {
+  if (!out) return fail(RESHARD_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!plan) return fail(RESHARD_ERR_INVALID_ARG, "plan is NULL");
+  try {
+    return partition(*plan, src_owner, dst_owner, world, rank, flags, out);
+  } catch (const std::bad_alloc &) {
+    return fail(RESHARD_ERR_OOM, "host allocation failed while partitioning");
+  }
+}
+
+extern "C" int reshard_plan_transfers(const reshard_plan_t *plan, int phase, int64_t cap, reshard_transfer_t *out,
+                                      int64_t *n_out) {
+  if (!plan) return fail(RESHARD_ERR_INVALID_ARG, "plan is NULL");
+  if (phase != 1 && phase != 2) return fail(RESHARD_ERR_INVALID_ARG, "phase must be 1 or 2");
+  int64_t n = 0;
+  for (const Transfer &t : plan->transfers) {
+    if (t.phase != phase) continue;
+    if (out && n < cap) out[n] = reshard_transfer_t{t.peer, t.dir, t.buf, t.phase, t.offset, t.bytes};
+    ++n;
+  }
+  if (n_out) *n_out = n;
+  return RESHARD_OK;
+}
+
 extern "C" int reshard_plan_stats(const reshard_plan_t *plan, reshard_stats_t *out) {
   if (!plan || !out) return fail(RESHARD_ERR_INVALID_ARG, "plan or out is NULL");
   *out = plan->stats;
@@ -746,6 +1071,7 @@ extern "C" int reshard_plan_stats(const reshard_plan_t *plan, reshard_stats_t *o
   out->last_aligned_items = plan->last_aligned;
   out->last_general_items = plan->last_general;
   out->last_rows_kernel = plan->last_rows_kernel;
+  out->last_staged_items = plan->last_staged;
   return RESHARD_OK;
 }
 

@@ -4,6 +4,7 @@
 
 #include <cstdint>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "../../include/reshard.h"
@@ -113,6 +114,9 @@ struct TensorInfo {
   int64_t src_base = 0, dst_base = 0;  // first pointer index of this tensor (flat, per side)
   std::vector<Box> src_box, dst_box;   // per pointer index
   std::vector<RankView> src_view, dst_view;
+  // per source pointer index: the lowest pointer index holding the same box (its replica
+  // group's representative), or -1 for an empty shard
+  std::vector<int32_t> src_rep;
 };
 
 struct Region {
@@ -121,6 +125,26 @@ struct Region {
   int32_t group;  // plan-wide destination group id
   Box box;        // global coordinates
   int64_t msg_off_bytes = 0;  // packed-mode workspace offset (16-byte aligned)
+};
+
+// How a plan executes one region: `direct` (device group index, or -1) copies the source to
+// that group's members; `send_off` (bytes, or -1) packs it into the send buffer; `unpack`
+// (device group index, or -1) copies it from the receive buffer at `recv_off` to the group.
+struct Role {
+  int32_t direct = -1;
+  int64_t send_off = -1;
+  int32_t unpack = -1;
+  int64_t recv_off = -1;
+};
+
+// One point-to-point transfer of a partitioned plan (mirrors reshard_transfer_t).
+struct Transfer {
+  int32_t peer;
+  int32_t dir;    // RESHARD_SEND / RESHARD_RECV
+  int32_t buf;    // RESHARD_SEND_BUF / RESHARD_RECV_BUF
+  int32_t phase;  // 1 or 2
+  int64_t offset;
+  int64_t bytes;
 };
 
 struct Group {
@@ -146,12 +170,19 @@ struct reshard_plan {
   std::vector<int32_t> grp_start;
   std::vector<int32_t> mem_ptr;   // pointer-table index of each member's data pointer
   std::vector<int64_t> mem_off;   // member's view offset (elements)
-  int32_t workspace_group = -1;
-  int64_t workspace_ptr = -1;     // pointer-table index of the workspace
+  int32_t workspace_group = -1;  // device group whose one member is the send buffer
+  int64_t workspace_ptr = -1;     // pointer-table index of the send buffer; the receive
+                                  // buffer follows it
   int max_fanout = 0;
   reshard_stats_t stats{};
   bool quant_ok = false;
   std::string quant_why;
+  // partitioned plans (reshard_plan_partition): the process this plan runs on, or -1
+  int rank = -1;
+  int world = 0;
+  std::vector<reshard::Transfer> transfers;  // phase 1 entries first, then phase 2
+  // pointer-table indices of the sources read and the destinations written by each pass
+  std::vector<int32_t> used_src[reshard::kNumSets], used_dst[reshard::kNumSets];
 
   // device state (bound at the first execute)
   int device = -1;
@@ -161,9 +192,11 @@ struct reshard_plan {
   int32_t *d_map_ok = nullptr; // 1 where the slab's map could be encoded
   int32_t *d_status = nullptr; // device-side status word (bit 0: a TMA wait timed out)
   // copy items split by alignment for the current pointers: cls_idx[set] lists the items that
-  // are 16-byte aligned everywhere first (n_aligned of them), then the rest
+  // are 16-byte aligned everywhere first (n_aligned of them), then the misaligned items of many
+  // short rows for the bulk-staged kernel (n_staged), then the rest
   std::vector<int32_t> cls_idx[reshard::kNumSets];
   int32_t n_aligned[reshard::kNumSets] = {0, 0, 0};
+  int32_t n_staged[reshard::kNumSets] = {0, 0, 0};  // next in cls_idx: the bulk-staged items
   int32_t *d_cls_idx[reshard::kNumSets] = {nullptr, nullptr, nullptr};
   uint64_t cls_version[reshard::kNumSets] = {0, 0, 0};
   uint64_t ptr_version = 0;  // bumped whenever the pointer table changes
@@ -171,20 +204,24 @@ struct reshard_plan {
   int64_t last_aligned = 0;  // copy items of the last pass that took the aligned walker
   int64_t last_general = 0;  // ... and the general walker
   int64_t last_rows_kernel = 0;  // 1 when those ran in the many-rows build of the general walker
+  int64_t last_staged = 0;       // copy items of the last pass run by the bulk-staged kernel
   bool gen_rows[reshard::kNumSets] = {false, false, false};  // general items mostly short rows
   int32_t *d_grp_start = nullptr;
   int32_t *d_mem_ptr = nullptr;
   int64_t *d_mem_off = nullptr;
   uint64_t *d_ptrs = nullptr;
   void *d_workspace = nullptr;
-  std::vector<uint64_t> ptr_cache;  // the caller's pointers of the last execute
+  std::vector<uint64_t> ptr_cache;  // the pointer table the kernels last saw, caller's values
   std::vector<uint64_t> dev_ptrs;   // ... as the kernels see them (host memory by its device alias)
+  std::vector<uint8_t> ptr_host;    // 1 where an entry is page-locked host memory
   bool any_host = false;            // some pointer is page-locked host memory
   bool ptr_cache_valid = false;
+  // completion of the last execute on each stream it used (waited for by destroy)
+  std::vector<std::pair<void *, void *>> done_events;  // (cudaStream_t, cudaEvent_t)
 };
 
 namespace reshard {
 void set_error(const std::string &msg);
 int fail(int code, const std::string &msg);
-int64_t pointer_table_size(const reshard_plan *p);  // Ns + 2 Nd + 1
+int64_t pointer_table_size(const reshard_plan *p);  // Ns + 2 Nd + 2
 }  // namespace reshard

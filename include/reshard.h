@@ -74,6 +74,13 @@ extern "C" {
 #define RESHARD_QUANT_NONE 0
 #define RESHARD_QUANT_MXFP8 1 /* BF16 -> E4M3 bytes + one E8M0 scale byte per 32 elements */
 
+/* partitioned plans (multi-process exchange) */
+#define RESHARD_STRIPED 1  /* reshard_plan_partition flag: striped two-phase receive */
+#define RESHARD_SEND 0     /* reshard_transfer_t.dir */
+#define RESHARD_RECV 1
+#define RESHARD_SEND_BUF 0 /* reshard_transfer_t.buf */
+#define RESHARD_RECV_BUF 1
+
 /* Opaque CUDA stream; pass a cudaStream_t (NULL = the legacy default stream). */
 struct CUstream_st;
 typedef struct CUstream_st *reshard_stream_t;
@@ -139,7 +146,28 @@ typedef struct {
   int64_t last_general_items; /* ... and by the general (unaligned-capable) walker */
   int64_t last_rows_kernel;   /* 1 if those ran in its many-short-rows build
                                  (reshard_copy_rows_kernel), 0 if in reshard_copy_kernel */
+  /* the message buffers of reshard_execute_pack / _unpack: message_bytes (above) is the send
+   * buffer's size, recv_bytes the receive buffer's (equal for an unpartitioned plan) */
+  int64_t recv_bytes;
+  int64_t rank;               /* the process a partitioned plan is for; -1 if unpartitioned */
+  int64_t world;              /* processes of the partition; 0 if unpartitioned */
+  int64_t transfers;          /* point-to-point operations of this rank, both phases */
+  int64_t sent_bytes;         /* bytes this rank sends in phase 1 (its own sources' messages) */
+  int64_t forwarded_bytes;    /* bytes this rank forwards in phase 2 (stripes it received) */
+  int64_t local_bytes;        /* source bytes this rank copies to its own destinations directly */
+  int64_t last_staged_items;  /* copy items of the last execute's last pass run by the bulk-staged
+                                 kernel (reshard_copy_staged_kernel: misaligned rows < 4 KiB) */
 } reshard_stats_t;
+
+/* One point-to-point transfer of a partitioned plan (see reshard_plan_transfers). */
+typedef struct {
+  int32_t peer;   /* the process at the other end */
+  int32_t dir;    /* RESHARD_SEND or RESHARD_RECV */
+  int32_t buf;    /* this rank's buffer: RESHARD_SEND_BUF or RESHARD_RECV_BUF */
+  int32_t phase;  /* 1 or 2 */
+  int64_t offset; /* byte offset in that buffer (a multiple of 16) */
+  int64_t bytes;  /* a multiple of 16, > 0 */
+} reshard_transfer_t;
 
 /*
  * reshard_plan_create -- plan one tensor's reshard (host only; touches no GPU).
@@ -205,6 +233,77 @@ int reshard_plan_blockwise_fp8(const reshard_tensor_spec_t *specs, int n_tensors
  */
 int reshard_execute(reshard_plan_t *plan, void *const *src_ptrs, void *const *dst_ptrs, int mode,
                     int quant, reshard_stream_t stream);
+
+/*
+ * reshard_execute_pack / reshard_execute_unpack -- the two passes of the packed mode with
+ * message buffers owned by the caller, so that a transport can move the messages in between
+ * ("NeMo-RL: Optimizing Non-Colocated Refit for Asynchronous RL", "Optimization #2": coalesce
+ * many tensors and pack them into contiguous buffers that move in few large transfers).
+ * pack reads the sources and writes send_buf (stats.message_bytes bytes). On a partitioned plan
+ *   (reshard_plan_partition) it also copies every region whose source and destination are both
+ *   on this rank straight into the destination (quantized under RESHARD_QUANT_MXFP8: dst_ptrs
+ *   then holds data/scale pairs as in reshard_execute); on an unpartitioned plan dst_ptrs may be
+ *   NULL and quant must be RESHARD_QUANT_NONE.
+ * unpack reads recv_buf (stats.recv_bytes bytes) and writes the destinations (quantizing under
+ *   RESHARD_QUANT_MXFP8, with the same constraints as reshard_execute).
+ * Message layout: regions in plan order, each starting on a 16-byte boundary; on an
+ *   unpartitioned plan it is the packed mode's (messages per (source rank, destination group),
+ *   both buffers the same size; they may be one buffer), so pack then unpack equals
+ *   reshard_execute(RESHARD_PACKED) with a caller-owned workspace.
+ * Buffers: device memory of the plan's device or page-locked host memory (as in
+ *   reshard_execute), 16-byte aligned, valid until the stream reaches the end of the work. Both
+ *   calls are asynchronous on `stream`; pointer arrays as in reshard_execute (on a partitioned
+ *   plan only this rank's entries are read; the others may be NULL).
+ * Errors as reshard_execute; INVALID_ARG also for a buffer that is NULL or not 16-byte aligned
+ *   while the plan has messages.
+ */
+int reshard_execute_pack(reshard_plan_t *plan, void *const *src_ptrs, void *const *dst_ptrs, void *send_buf,
+                         int quant, reshard_stream_t stream);
+int reshard_execute_unpack(reshard_plan_t *plan, const void *recv_buf, void *const *dst_ptrs, int quant,
+                           reshard_stream_t stream);
+
+/*
+ * reshard_plan_partition -- the share of `plan` that one process runs when the shards live on
+ * different processes (one GPU each) of a process group: the multi-GPU form of the Reshard
+ * collective (NeMo-RL design doc "NCCL Reshard Refit (Experimental)", "xferdtensor Transports":
+ * batched point-to-point transfers, receives striped across destination replicas, then spread
+ * inside each replica group; news article on NVIDIA's Reshard collective, "How NCCL M2N Reshard
+ * maximizes network bandwidth": each replica group pulls a byte over the network once and its
+ * members exchange their stripes over NVLink).
+ * src_owner[i], dst_owner[j]: the process (0 .. world-1) that holds source pointer i and
+ *   destination pointer j of `plan` (flat pointer-array order, as in reshard_execute).
+ * rank: the process to plan for. flags: 0 or RESHARD_STRIPED.
+ * Source choice: each region is sent by one holder of its source box; a holder on a process
+ *   that also holds a destination of the region is preferred (that copy stays local), otherwise
+ *   the holders take regions in turn. Messages: one per (sending process, set of other processes
+ *   receiving), holding the regions of every tensor it carries in plan order, 16-byte aligned;
+ *   the send buffer holds this rank's outgoing messages, the receive buffer its incoming ones,
+ *   each ordered by (sender, receivers).
+ * Transfers: without RESHARD_STRIPED each receiver gets every message whole from its sender
+ *   (phase 1). With it a message is cut into one 16-byte aligned stripe per receiver; the
+ *   sender sends stripe k to the k-th receiver (phase 1) and each receiver forwards its stripe to
+ *   the message's other receivers (phase 2), so each message byte leaves the sender once.
+ * Use: reshard_execute_pack (local copies, outgoing messages), then every transfer of phase 1,
+ *   then of phase 2 (reshard_plan_transfers), then reshard_execute_unpack. The result is a new
+ *   host-only plan; `plan` is not modified and may be destroyed. A partitioned plan cannot run
+ *   through reshard_execute or reshard_execute_static, and cannot be partitioned again.
+ * Errors: INVALID_ARG (NULL arguments, world < 1, rank or an owner out of range, a partitioned
+ *   plan, unknown flags); OOM.
+ */
+int reshard_plan_partition(const reshard_plan_t *plan, const int32_t *src_owner, const int32_t *dst_owner, int world,
+                           int rank, int flags, reshard_plan_t **out);
+
+/*
+ * reshard_plan_transfers -- the point-to-point transfers of a partitioned plan's rank in one
+ * phase (1 or 2), in posting order: for every pair of processes the sender's sends and the
+ * receiver's receives of a phase are listed in the same order with the same sizes, so that
+ * in-order matching (MPI, NCCL and gloo point-to-point semantics) pairs them correctly. All of
+ * phase 1 must complete before phase 2 starts (phase 2 sends read stripes received in phase
+ * 1). Up to cap entries go to `out` (may be NULL); *n_out gets the count. Empty for an
+ * unpartitioned plan.
+ */
+int reshard_plan_transfers(const reshard_plan_t *plan, int phase, int64_t cap, reshard_transfer_t *out,
+                           int64_t *n_out);
 
 /*
  * reshard_execute_static -- the direct-mode reshard (quant none) without any device allocation.

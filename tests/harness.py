@@ -2,6 +2,7 @@
 from __future__ import annotations
 
 import itertools
+import os
 
 import numpy as np
 import torch
@@ -44,6 +45,109 @@ def assert_matches_oracle(wl, lay):
         gs = lay.scale_slab.cpu().numpy()
         bad = np.nonzero(gs != wsc)[0]
         assert bad.size == 0, f"{wl.name}: {bad.size} scale bytes differ, first at {bad[:8]}"
+
+
+def _mem_available() -> int:
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 16 << 30
+
+
+def whole_check(wl, lay, workers=None):
+    """Whole-output parity at any size, streamed so that host memory stays bounded.
+
+    Tensors are grouped so that no destination buffer is shared between groups; for each group
+    the source buffers it reads are copied to the host, the C oracle writes the group's
+    destination (and scale) buffers into canary-filled host buffers, and every byte of those
+    buffers is compared with the device's (views and the gaps between them). Groups run on a
+    thread pool (the oracle and the copies release the GIL). Returns the bytes compared."""
+    import concurrent.futures as cf
+    es = {k: v[1] for k, v in S.DTYPES.items()}
+    quant = wl.quant == "mxfp8"
+    n_t = len(wl.tensors)
+    parent = list(range(n_t))
+
+    def find(x):
+        while parent[x] != x:
+            parent[x] = parent[parent[x]]
+            x = parent[x]
+        return x
+    first = {}
+    for ti, t in enumerate(wl.tensors):
+        for v in t.dst_views:
+            if v.buffer in first:
+                parent[find(ti)] = find(first[v.buffer])
+            else:
+                first[v.buffer] = ti
+    comps = {}
+    for ti in range(n_t):
+        comps.setdefault(find(ti), []).append(ti)
+    comps = list(comps.values())
+
+    def sbytes(b):
+        return wl.src_buffer_numel[b] * es[wl.src_buffer_dtype[b]]
+
+    def dbytes(b):
+        return wl.dst_buffer_numel[b] * (1 if quant else es[wl.dst_buffer_dtype[b]])
+
+    def need(tids):
+        sb = {v.buffer for ti in tids for v in wl.tensors[ti].src_views}
+        db = {v.buffer for ti in tids for v in wl.tensors[ti].dst_views}
+        glob = sum(int(np.prod(wl.tensors[ti].global_shape)) * es[wl.tensors[ti].dtype] for ti in tids)
+        return sum(sbytes(b) for b in sb) + 2 * sum(dbytes(b) for b in db) + 2 * glob
+    est = max(need(c) for c in comps) if comps else 1
+    cores = os.cpu_count() or 1
+    if workers is None:
+        workers = max(1, min(cores, int(0.5 * _mem_available() // max(est, 1))))
+
+    def compact(bufs, size_of):
+        off, cur = [0] * (max(bufs) + 1 if bufs else 1), 0
+        for b in bufs:
+            off[b] = cur
+            cur += (size_of(b) + 15) // 16 * 16
+        return off, cur
+
+    def one(tids):
+        sb = sorted({v.buffer for ti in tids for v in wl.tensors[ti].src_views})
+        db = sorted({v.buffer for ti in tids for v in wl.tensors[ti].dst_views})
+        s_off, s_n = compact(sb, sbytes)
+        d_off, d_n = compact(db, dbytes)
+        src = np.empty(max(1, s_n), np.uint8)
+        for b in sb:
+            torch.from_numpy(src[s_off[b]: s_off[b] + sbytes(b)]).copy_(lay.src_slab[lay.src_off[b]: lay.src_off[b] + sbytes(b)])
+        want = np.full(max(1, d_n), 0xA5, np.uint8)
+        got = np.empty(max(1, d_n), np.uint8)
+        wsc = gsc = c_off = None
+        if quant:
+            c_off, c_n = compact(db, lambda b: wl.dst_buffer_numel[b] // 32)
+            wsc = np.full(max(1, c_n), 0xA5, np.uint8)
+            gsc = np.empty(max(1, c_n), np.uint8)
+        coracle.run_workload(wl, src, s_off, want, d_off, wsc, c_off, tensors=tids)
+        n = 0
+        for b in db:
+            nb = dbytes(b)
+            torch.from_numpy(got[d_off[b]: d_off[b] + nb]).copy_(lay.dst_slab[lay.dst_off[b]: lay.dst_off[b] + nb])
+            bad = np.count_nonzero(got[d_off[b]: d_off[b] + nb] != want[d_off[b]: d_off[b] + nb])
+            assert bad == 0, f"{wl.name}: destination buffer {b}: {bad} bytes differ from the oracle"
+            n += nb
+            if quant:
+                nc = wl.dst_buffer_numel[b] // 32
+                torch.from_numpy(gsc[c_off[b]: c_off[b] + nc]).copy_(
+                    lay.scale_slab[lay.scale_off[b]: lay.scale_off[b] + nc])
+                bad = np.count_nonzero(gsc[c_off[b]: c_off[b] + nc] != wsc[c_off[b]: c_off[b] + nc])
+                assert bad == 0, f"{wl.name}: scale buffer {b}: {bad} bytes differ from the oracle"
+                n += nc
+        return n
+
+    if lay.dst_slab.is_cuda:
+        torch.cuda.synchronize()
+    with cf.ThreadPoolExecutor(workers) as ex:
+        return sum(ex.map(one, comps))
 
 
 def _gather(slab: torch.Tensor, offsets: np.ndarray, nbytes: int) -> np.ndarray:

@@ -190,6 +190,38 @@ def test_static_entry_rejects_transposing_plans_before_any_cuda_call():
     assert e.value.code == R.RESHARD_ERR_UNSUPPORTED and "transposing" in str(e.value)
 
 
+def test_static_entry_rejects_plans_beyond_its_array_before_any_cuda_call():
+    # 640 x 640 regions: 409,600 work items of 64 bytes, more than the fixed array holds; the
+    # size check comes first, so the (fabricated) pointers are never looked at
+    d = S.TensorDesc("w", (640, 1280), "i32", (640,), ("S0",), (640,), ("S1",),
+                     [S.View(i) for i in range(640)], [S.View(i) for i in range(640)])
+    plan = R.reshard_plan_create(d)
+    with pytest.raises(R.ReshardError) as e:
+        R.reshard_execute_static(plan, [1] * 640, [1] * 640)
+    assert e.value.code == R.RESHARD_ERR_UNSUPPORTED and "at most" in str(e.value)
+
+
+def test_pack_and_unpack_check_their_arguments_on_the_host():
+    wl = S.dense_ffn(layers=1, hidden=64, ffn=100)
+    plan = R.plan_workload(wl)
+    ns, nd = plan.n_src_ptrs, plan.n_dst_ptrs
+    for buf in (None, 8):   # missing, and not 16-byte aligned
+        with pytest.raises(R.ReshardError) as e:
+            R.reshard_execute_pack(plan, [1] * ns, None, buf)
+        assert e.value.code == R.RESHARD_ERR_INVALID_ARG and "send_buf" in str(e.value)
+        with pytest.raises(R.ReshardError) as e:
+            R.reshard_execute_unpack(plan, buf, [1] * nd)
+        assert e.value.code == R.RESHARD_ERR_INVALID_ARG and "recv_buf" in str(e.value)
+    with pytest.raises(R.ReshardError) as e:   # an unpartitioned plan's pack copies, never quantizes
+        R.reshard_execute_pack(plan, [1] * ns, None, 16, quant="mxfp8")
+    assert e.value.code in (R.RESHARD_ERR_INVALID_ARG, R.RESHARD_ERR_UNSUPPORTED)
+    with pytest.raises(R.ReshardError) as e:
+        R.reshard_execute_pack(plan, [0] * ns, None, 16)
+    assert e.value.code == R.RESHARD_ERR_INVALID_ARG and "NULL" in str(e.value)
+    st = R.reshard_plan_stats(plan)
+    assert st["recv_bytes"] == st["message_bytes"] > 0 and st["rank"] == -1 and st["world"] == 0
+
+
 def test_status_is_zero_before_any_execute():
     plan = R.plan_workload(S.example_8x8())
     assert R.reshard_plan_status(plan) == 0
@@ -249,6 +281,10 @@ def test_every_entry_point_refuses_null_and_out_of_range_arguments():
     assert L.reshard_plan_status(None, ctypes.byref(i32), 0) == inv
     assert L.reshard_execute(None, None, None, 0, 0, None) == inv
     assert L.reshard_execute_static(None, None, None, None) == inv
+    assert L.reshard_execute_pack(None, None, None, None, 0, None) == inv
+    assert L.reshard_execute_unpack(None, None, None, 0, None) == inv
+    assert L.reshard_plan_partition(None, None, None, 1, 0, 0, ctypes.byref(ctypes.c_void_p())) == inv
+    assert L.reshard_plan_transfers(None, 1, 0, None, ctypes.byref(n)) == inv
     assert L.reshard_plan_destroy(None) == R.RESHARD_OK
     plan = R.plan_workload(S.example_8x8())
     assert L.reshard_plan_stats(plan.handle, None) == inv
@@ -256,6 +292,8 @@ def test_every_entry_point_refuses_null_and_out_of_range_arguments():
     assert L.reshard_plan_group_members(plan.handle, -1, 0, None, ctypes.byref(n)) == inv
     assert L.reshard_plan_items(plan.handle, 6, 0, None, ctypes.byref(n), None, None, None, None, None) == inv
     assert L.reshard_plan_items(plan.handle, -1, 0, None, ctypes.byref(n), None, None, None, None, None) == inv
+    assert L.reshard_plan_transfers(plan.handle, 3, 0, None, ctypes.byref(n)) == inv
+    assert L.reshard_plan_partition(plan.handle, None, None, 1, 0, 0, None) == inv
     assert R.reshard_last_error()  # the last refusal left a message
     with pytest.raises(R.ReshardError):
         R.reshard_plan_group_members(plan, 10 ** 6)

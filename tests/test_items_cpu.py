@@ -12,6 +12,7 @@ import dtensor_resharding_gb300 as R
 import synthetic as S
 from oracle import coracle
 
+from emulator import run_items
 from test_parity_gpu import SMALL
 
 DIRECT, PACK, UNPACK = 0, 1, 2
@@ -33,7 +34,7 @@ def _ranges(wl, lay, plan):
             else:
                 sc.append(("none", 0, 0))
     ws = R.reshard_plan_stats(plan)["message_bytes"]
-    return src + dst + sc + [("ws", 0, ws)]
+    return src + dst + sc + [("ws", 0, ws), ("ws", 0, ws)]
 
 
 def check_bounds(wl, lay, plan, which, quant=False):
@@ -112,40 +113,8 @@ def emulate(wl, lay, plan, mode):
     ws = np.zeros(max(1, R.reshard_plan_stats(plan)["message_bytes"]), np.uint8)
     table = _ranges(wl, lay, plan)
     arrays = {"src": src, "dst": dst, "ws": ws}
-
-    def run_t(which):
-        items, gs, mp, mo = R.reshard_plan_items(plan, which + 3)
-        for it in items:
-            e = int(it["esize"])
-            kind, base, _ = table[it["src"]]
-            rr, cc = np.meshgrid(np.arange(int(it["rows"])), np.arange(int(it["cols"])), indexing="ij")
-            soff = base + (int(it["src_off"]) + rr * int(it["src_pitch"]) + cc) * e
-            vals = arrays[kind][(soff[..., None] + np.arange(e)).reshape(-1)]
-            for m in range(gs[it["group"]], gs[it["group"] + 1]):
-                dkind, dbase, _ = table[mp[m]]
-                doff = dbase + (int(mo[m]) + int(it["dst_off"]) + cc * int(it["dst_pitch"]) + rr) * e
-                arrays[dkind][(doff[..., None] + np.arange(e)).reshape(-1)] = vals
-
-    def run(which):
-        run_t(which)
-        items, gs, mp, mo = R.reshard_plan_items(plan, which)
-        for it in items:
-            e = int(it["esize"])
-            kind, base, _ = table[it["src"]]
-            sarr = arrays[kind]
-            for m in range(gs[it["group"]], gs[it["group"] + 1]):
-                dkind, dbase, _ = table[mp[m]]
-                darr = arrays[dkind]
-                for r in range(int(it["rows"])):
-                    s0 = base + (int(it["src_off"]) + r * int(it["src_pitch"])) * e
-                    d0 = dbase + (int(mo[m]) + int(it["dst_off"]) + r * int(it["dst_pitch"])) * e
-                    n = int(it["run"]) * e
-                    darr[d0: d0 + n] = sarr[s0: s0 + n]
-    if mode == "direct":
-        run(DIRECT)
-    else:
-        run(PACK)
-        run(UNPACK)
+    for which in ((DIRECT,) if mode == "direct" else (PACK, UNPACK)):
+        run_items(plan, which, table, arrays)
     return dst
 
 

@@ -2,8 +2,11 @@
 
 Small cases (whole slabs compared with the C oracle, canary bytes included) span several
 work items, ragged tails, uneven and empty chunks, misaligned buffers, both modes and MXFP8.
-Full-size workloads are checked on sampled outputs that the oracle computes one by one, and by
-the A -> B -> A round trip, which must give the sources back unchanged.
+The full-size workloads of the five headline configurations are compared whole as well
+(streamed tensor group by tensor group through the C oracle, every destination and scale byte,
+tolerance 0), after a fast sampled pre-check that the oracle computes element by element; the
+other full-size workloads are checked on samples and by the A -> B -> A round trip, which must
+give the sources back unchanged.
 """
 import numpy as np
 import pytest
@@ -16,7 +19,7 @@ pytestmark = pytest.mark.gpu
 if torch.cuda.is_available():
     import dtensor_resharding_gb300 as R
     from harness import (assert_matches_oracle, run_gpu, sampled_check, sampled_check_mxfp8,
-                         round_trip_desc)
+                         round_trip_desc, whole_check)
 
 SMALL = {
     "example_8x8": lambda: S.example_8x8(),
@@ -230,8 +233,9 @@ def _full(wl_fn, mode, sampler, **kw):
 
 
 @pytest.mark.parametrize("mode", ["direct", "packed"])
-def test_full_dense_ffn_sampled_and_round_trip(mode):
+def test_full_dense_ffn_whole_and_round_trip(mode):
     wl, lay, plan = _full(S.dense_ffn, mode, sampled_check, per_tensor=64, corners=True)
+    assert whole_check(wl, lay) == wl.dst_bytes()
     # A -> B -> A: the destinations resharded back reproduce the (fused) sources exactly
     back = S.Workload(wl.name + ".back", [round_trip_desc(t) for t in wl.tensors],
                       src_buffer_numel=wl.dst_buffer_numel, src_buffer_dtype=wl.dst_buffer_dtype,
@@ -249,13 +253,15 @@ def test_full_dense_ffn_sampled_and_round_trip(mode):
         assert torch.equal(lay.src_slab[off: off + nb], out[off: off + nb]), f"source buffer {b} changed"
 
 
-def test_full_moe_ep16_to_ep8_sampled():
-    _full(lambda: S.moe_experts(dst="ep8"), "direct", sampled_check, per_tensor=64, corners=True)
+def test_full_moe_ep16_to_ep8_whole():
+    wl, lay, _ = _full(lambda: S.moe_experts(dst="ep8"), "direct", sampled_check, per_tensor=64, corners=True)
+    assert whole_check(wl, lay) == wl.dst_bytes()
 
 
 @pytest.mark.parametrize("mode", ["direct", "packed"])
-def test_full_moe_tp4_mxfp8_sampled(mode):
-    _full(lambda: S.moe_experts(dst="tp4"), mode, sampled_check_mxfp8, per_tensor=6)
+def test_full_moe_tp4_mxfp8_whole(mode):
+    wl, lay, _ = _full(lambda: S.moe_experts(dst="tp4"), mode, sampled_check_mxfp8, per_tensor=6)
+    assert whole_check(wl, lay) == wl.dst_bytes()
 
 
 def test_full_edge_mix_bit_exact():
@@ -272,8 +278,9 @@ def test_full_next_rows_sampled(name):
     _full(lambda: S.workload_by_name(name), "direct", sampled_check, per_tensor=16, max_tensors=400, corners=True)
 
 
-def test_full_many_small_sampled():
-    _full(S.many_small, "direct", sampled_check, per_tensor=4)
+def test_full_many_small_whole():
+    wl, lay, _ = _full(S.many_small, "direct", sampled_check, per_tensor=4)
+    assert whole_check(wl, lay) == wl.dst_bytes()
 
 
 @pytest.mark.parametrize("side", ["dst", "src"])

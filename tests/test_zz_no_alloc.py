@@ -4,9 +4,9 @@ Such callers (an inference engine that keeps almost all device memory reserved f
 cache, a framework whose own allocator owns the device heap) cannot accept a cudaMalloc in the
 middle of a refit: it can fail for lack of memory, and it synchronizes the device. This entry
 point keeps its descriptor tables in a fixed array inside the library instead. Its output must
-be byte-identical (tolerance 0, as for every copy here) to reshard_execute's, on two calls in a
-row with different plans, so that stale tables left by the first call cannot leak into the
-second. Collected last, and independent of any other test's state.
+equal the oracle's byte for byte (tolerance 0, as for every copy here) and reshard_execute's, on
+two calls in a row with different plans, so that stale tables left by the first call cannot
+leak into the second. Collected last, and independent of any other test's state.
 """
 import pytest
 import torch
@@ -17,6 +17,7 @@ pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
     import dtensor_resharding_gb300 as R
+    from harness import assert_matches_oracle
 
 
 def _prepared(wl, misalign=0):
@@ -26,7 +27,7 @@ def _prepared(wl, misalign=0):
     return lay
 
 
-def test_static_entry_matches_execute_on_two_calls_in_a_row():
+def test_static_entry_matches_oracle_and_execute_on_two_calls_in_a_row():
     workloads = [S.dense_ffn(layers=2, hidden=256, ffn=1000),
                  S.mesh2d_to_1d(rows=143, cols=409, variant="2d")]
     plans = [R.plan_workload(wl) for wl in workloads]
@@ -47,6 +48,7 @@ def test_static_entry_matches_execute_on_two_calls_in_a_row():
         got.append(lay)
     torch.cuda.synchronize()
     for wl, a, b in zip(workloads, want, got):
+        assert_matches_oracle(wl, b)
         for t in range(len(wl.tensors)):
             es = S.DTYPES[wl.tensors[t].dtype][1]
             for v in wl.tensors[t].dst_views:
@@ -56,11 +58,19 @@ def test_static_entry_matches_execute_on_two_calls_in_a_row():
                 assert torch.equal(x, y), (wl.name, t, v.buffer)
 
 
-def test_static_entry_rejects_plans_beyond_its_array():
-    # 640 x 640 regions: 409,600 work items of 64 bytes, more than the fixed array holds
-    d = S.TensorDesc("w", (640, 1280), "i32", (640,), ("S0",), (640,), ("S1",),
-                     [S.View(i) for i in range(640)], [S.View(i) for i in range(640)])
-    plan = R.reshard_plan_create(d)
+def test_static_entry_refuses_pageable_memory_before_any_launch():
+    """The pointers are checked like reshard_execute's: pageable host memory is refused on the
+    host instead of reaching a kernel."""
+    import dataclasses
+    wl = S.dense_ffn(layers=1, hidden=256, ffn=1000)
+    lay = _prepared(wl)
+    plan = R.plan_workload(wl)
+    pageable = torch.empty(lay.src_slab.numel(), dtype=torch.uint8)
+    sp, dp = R.workload_pointers(wl, dataclasses.replace(lay, src_slab=pageable))
     with pytest.raises(R.ReshardError) as e:
-        R.reshard_execute_static(plan, [1] * 640, [1] * 640)
-    assert e.value.code == R.RESHARD_ERR_UNSUPPORTED and "at most" in str(e.value)
+        R.reshard_execute_static(plan, sp, dp)
+    assert e.value.code == R.RESHARD_ERR_INVALID_ARG and "pageable" in str(e.value)
+    sp, dp = R.workload_pointers(wl, lay)
+    R.reshard_execute_static(plan, sp, dp, stream=torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert_matches_oracle(wl, lay)
