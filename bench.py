@@ -286,9 +286,10 @@ def dominant_kernel(R, plan, mode: str, quant: str) -> str:
     if quant == "mxfp8":
         return "reshard_mxfp8_kernel"
     st = R.reshard_plan_stats(plan)
-    if st["last_aligned_items"] >= st["last_general_items"]:
-        return "reshard_copy_aligned_kernel"
-    return "reshard_copy_rows_kernel" if st["last_rows_kernel"] else "reshard_copy_kernel"
+    counts = {"reshard_copy_aligned_kernel": st["last_aligned_items"],
+              "reshard_copy_staged_kernel": st["last_staged_items"],
+              ("reshard_copy_rows_kernel" if st["last_rows_kernel"] else "reshard_copy_kernel"): st["last_general_items"]}
+    return max(counts, key=counts.get)
 
 
 def e2e_run(R, wl, plan, sp, dp, lay, args, quant, world, dev, dst_bytes, barrier, st):
@@ -537,9 +538,9 @@ def our_arm(args, rank: int, world: int, local_rank: int) -> None:
     if args.mode == "packed":
         roofline["note"] = "packed mode: the step is the pack and unpack launches; achieved counts both passes' bytes"
     elif launches > 1:
-        roofline["note"] = (f"the step is {launches} launches (aligned walker, general walker and/or "
-                            "transposing kernel, back to back on one stream): achieved and frac cover "
-                            "the whole step; the kernel named is the one with the most items")
+        roofline["note"] = (f"the step is {launches} launches (aligned walker, bulk-staged kernel, general "
+                            "walker and/or transposing kernel, back to back on one stream): achieved and "
+                            "frac cover the whole step; the kernel named is the one with the most items")
     same = copy_rate_same_run(dev)
     roofline["copy_rate_same_run"] = round(same, 1)
     roofline["frac_of_same_run_copy"] = round(achieved / same, 4)

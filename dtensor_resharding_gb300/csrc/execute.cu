@@ -539,41 +539,53 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, unsigned
 //
 // reshard_copy_staged_kernel copies items of many short rows whose destination rows are not all
 // 16-byte aligned (a column split whose row pitch is not a multiple of 16 bytes, for instance).
-// Source rows are staged in shared memory by the TMA bulk-copy unit: warp 0 issues one
-// cp.async.bulk per row (the row's span rounded out to 16-byte boundaries, so both ends stay in
-// blocks that hold bytes of the row) into a ring of stages, completion counted in bytes on an
-// mbarrier; loads run up to kSStages chunks ahead and hold no registers while in flight. Every
-// warp then drains rows from the stage: lane l writes destination words l, l + 32, ... of the
-// row, each assembled from at most two aligned 16-byte shared-memory reads by a funnel shift and
-// stored whole (or, at the row's two ends, in naturally aligned pieces), once per replica.
-// Waits are bounded like the transposing kernel's: on expiry bit 0 of the status word is set and
-// the CTA returns after waiting (bounded) for its copies in flight.
+// Source rows are staged in shared memory by the TMA bulk-copy unit, and every warp runs its own
+// pipeline, with no CTA-wide barrier: the rows of the CTA's items are dealt to its warps in
+// chunks (as many rows as fit one stage); a warp issues one cp.async.bulk per row of a chunk
+// (the row's span rounded out to 16-byte boundaries, so both ends stay in blocks that hold bytes
+// of the row) into one of its stages, completion counted in bytes on that stage's mbarrier, and
+// records in the stage's descriptor the row addresses it needs (source phase, every replica's
+// destination row), so draining a stage reads no descriptor from global memory. Loads run up to
+// kSStages - 1 chunks ahead and hold no registers while in flight. Draining: lane l writes
+// destination words l, l + 32, ... of a row, each assembled from at most two aligned 16-byte
+// shared-memory reads by a funnel shift, and stored whole (or, at the row's two ends, in
+// naturally aligned pieces) to every replica. Waits are bounded like the transposing kernel's:
+// on expiry bit 0 of the status word is set and the warp stops after waiting (bounded) for its
+// copies in flight.
 
 #ifndef RESHARD_STAGED
 #define RESHARD_STAGED 1
 #endif
 #ifndef RESHARD_STAGED_STAGES
-#define RESHARD_STAGED_STAGES 4
+#define RESHARD_STAGED_STAGES 3
+#endif
+#ifndef RESHARD_STAGED_MAX_RUN
+#define RESHARD_STAGED_MAX_RUN 4096
 #endif
 #ifndef RESHARD_STAGED_BYTES
-#define RESHARD_STAGED_BYTES 12288
+#define RESHARD_STAGED_BYTES (RESHARD_STAGED_MAX_RUN + 64)
 #endif
 #ifndef RESHARD_STAGED_MIN_BLOCKS
-#define RESHARD_STAGED_MIN_BLOCKS 3
+#define RESHARD_STAGED_MIN_BLOCKS 2
 #endif
-constexpr int kSStages = RESHARD_STAGED_STAGES;
-constexpr int kSBytes = RESHARD_STAGED_BYTES;  // bytes per stage (multiple of 16)
-constexpr size_t kStagedSmem = (size_t)kSStages * kSBytes;
+constexpr int kSStages = RESHARD_STAGED_STAGES;   // stages per warp
+constexpr int kSBytes = RESHARD_STAGED_BYTES;     // bytes per stage (multiple of 16)
+constexpr int kSWarps = kBlock / 32;
+constexpr size_t kStagedSmem = (size_t)kSWarps * kSStages * kSBytes;
 static_assert(kSBytes % 16 == 0 && kSStages >= 2 && kSStages <= 8, "stage ring shape");
-// rows up to this many bytes go through the staged kernel (one row must fit a stage)
-constexpr int64_t kStagedMaxRun = RESHARD_ROWS_MAX_RUN;
-static_assert(kStagedMaxRun + 32 <= kSBytes, "a staged row and its rounding fit one stage");
+// rows up to this many bytes go through the staged kernel (one row and its rounding fit a stage)
+constexpr int64_t kStagedMaxRun = RESHARD_STAGED_MAX_RUN;
+static_assert(kStagedMaxRun + 32 <= kSBytes + 16, "a staged row and its rounding fit one stage");
+constexpr int kStagedFan = kMaxFan;  // replicas an item may have to be staged
 
-struct StagedChunk {
-  int32_t item;   // position in the launch's item list
-  int32_t r0;     // first row
+struct StagedStage {
+  uint64_t src;             // address of the chunk's first source row
+  uint64_t dst[kStagedFan]; // every replica's destination row of the chunk's first row
+  int64_t sp_b, dp_b;       // row pitches (bytes)
+  int32_t run_b;            // bytes per row
   int32_t nrows;
-  int32_t slot;   // bytes per row slot in the stage
+  int32_t slot;             // bytes per row slot in the stage
+  int32_t nrep;
 };
 
 __device__ __forceinline__ int staged_slot(int64_t run_b) { return (int)((run_b + 15) / 16 * 16 + 16); }
@@ -584,122 +596,224 @@ __device__ __forceinline__ uint4 lds16(const uint8_t *p) {
   return v;
 }
 
+// Bytes [S, S + 16) of the 32-byte concatenation lo:hi, S a compile-time constant in [1, 16).
+template <int S>
+__device__ __forceinline__ uint4 shift_const(uint4 lo, uint4 hi) {
+  const uint32_t v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  constexpr int q = S / 4, r = (S % 4) * 8;
+  uint4 o;
+  if constexpr (r == 0) {
+    o = make_uint4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+  } else {
+    o.x = __funnelshift_r(v[q], v[q + 1], r);
+    o.y = __funnelshift_r(v[q + 1], v[q + 2], r);
+    o.z = __funnelshift_r(v[q + 2], v[q + 3], r);
+    o.w = __funnelshift_r(v[q + 3], v[q + 4], r);
+  }
+  return o;
+}
+
+// Whole destination words [w0, w1) of a staged row at byte phase S: word w is bytes
+// [16 w + S, 16 w + S + 16) of the stage from sw0 (one aligned read when S == 0, two otherwise).
+#ifndef RESHARD_STAGED_UNROLL
+#define RESHARD_STAGED_UNROLL 4
+#endif
+template <int S, int NF>
+__device__ __forceinline__ void drain_words(const uint8_t *sw0, uint8_t *d0, uint8_t *d1, int w0, int w1, int lane) {
+  constexpr int U = RESHARD_STAGED_UNROLL;  // words per lane whose shared reads are in flight together
+  for (int w = w0 + lane; w < w1; w += 32 * U) {
+    uint4 lo[U], hi[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int x = w + 32 * u;
+      lo[u] = make_uint4(0, 0, 0, 0);
+      hi[u] = make_uint4(0, 0, 0, 0);
+      if (x < w1) {
+        lo[u] = lds16(sw0 + 16 * x);
+        if constexpr (S != 0) hi[u] = lds16(sw0 + 16 * x + 16);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int x = w + 32 * u;
+      if (x < w1) {
+        uint4 o;
+        if constexpr (S == 0)
+          o = lo[u];
+        else
+          o = shift_const<S>(lo[u], hi[u]);
+        store_stream(d0 + 16 * x, o);
+        if constexpr (NF == 2) store_stream(d1 + 16 * x, o);
+      }
+    }
+  }
+}
+
+// Whole words of a row to one destination (d1 == nullptr) or to two at the same byte phase.
+__device__ __forceinline__ void drain_words_at(int s, const uint8_t *sw0, uint8_t *d0, uint8_t *d1, int w0, int w1,
+                                               int lane) {
+#define RESHARD_DRAIN_CASE(S_)                                       \
+  case S_:                                                           \
+    if (d1)                                                          \
+      drain_words<S_, 2>(sw0, d0, d1, w0, w1, lane);                 \
+    else                                                             \
+      drain_words<S_, 1>(sw0, d0, nullptr, w0, w1, lane);            \
+    break;
+  switch (s) {
+    RESHARD_DRAIN_CASE(0) RESHARD_DRAIN_CASE(1) RESHARD_DRAIN_CASE(2) RESHARD_DRAIN_CASE(3)
+    RESHARD_DRAIN_CASE(4) RESHARD_DRAIN_CASE(5) RESHARD_DRAIN_CASE(6) RESHARD_DRAIN_CASE(7)
+    RESHARD_DRAIN_CASE(8) RESHARD_DRAIN_CASE(9) RESHARD_DRAIN_CASE(10) RESHARD_DRAIN_CASE(11)
+    RESHARD_DRAIN_CASE(12) RESHARD_DRAIN_CASE(13) RESHARD_DRAIN_CASE(14) default:
+    RESHARD_DRAIN_CASE(15)
+  }
+#undef RESHARD_DRAIN_CASE
+}
+
 __global__ void __launch_bounds__(kBlock, RESHARD_STAGED_MIN_BLOCKS) reshard_copy_staged_kernel(
     const Item *__restrict__ items, const int32_t *__restrict__ idx, int n_items, const uint64_t *__restrict__ ptrs,
     const int32_t *__restrict__ gstart, const int32_t *__restrict__ mptr, const int64_t *__restrict__ moff,
     int32_t *status, int wait_last) {
   if (!wait_last) pdl_enter();
   extern __shared__ __align__(128) uint8_t sring[];
-  __shared__ __align__(8) uint64_t bar[kSStages];
-  __shared__ StagedChunk desc[kSStages];
-  __shared__ int s_total;
+  __shared__ __align__(8) uint64_t bar[kSWarps][kSStages];
+  __shared__ StagedStage desc[kSWarps][kSStages];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (threadIdx.x == 0) {
-    int tot = 0;
-    for (int k = blockIdx.x; k < n_items; k += gridDim.x) {
-      const Item &it = items[item_index(idx, k)];
-      const int rpc = kSBytes / staged_slot((int64_t)it.run * it.esize);
-      tot += (it.rows + rpc - 1) / rpc;
-    }
-    s_total = tot;
-    for (int st = 0; st < kSStages; ++st) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar[st])));
+  uint8_t *ring = sring + (size_t)warp * kSStages * kSBytes;
+  if (lane == 0) {
+    for (int st = 0; st < kSStages; ++st) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar[warp][st])));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncthreads();
-  const int total = s_total;
+  __syncwarp();
 
-  // chunk cursor of warp 0 (uniform across its lanes): item k, next row r
-  int ck = blockIdx.x, cr = 0;
-  auto issue = [&](int stage) {
-    Item it = items[item_index(idx, ck)];
-    while (cr >= it.rows) {
-      ck += gridDim.x;
-      cr = 0;
-      it = items[item_index(idx, ck)];
+  // issue cursor of this warp: item k (position in the launch's list), chunk j of that item;
+  // chunks of rows are dealt to the warps in turn, chunk j to warp j % kSWarps
+  int ik = blockIdx.x, ij = warp;
+  Item it{};
+  int rpc = 1, nch = 0;  // rows per chunk and chunks of the current item
+  auto load_item = [&]() {
+    while (ik < n_items) {
+      it = items[item_index(idx, ik)];
+      rpc = kSBytes / staged_slot((int64_t)it.run * it.esize);
+      nch = (it.rows + rpc - 1) / rpc;
+      if (ij < nch) return;
+      ij -= nch;  // keep the deal going across items: chunk numbering continues
+      ik += gridDim.x;
     }
+  };
+  load_item();
+  auto issue = [&](int st) -> bool {
+    if (ik >= n_items) return false;
     const int64_t es = it.esize, run_b = (int64_t)it.run * es, sp_b = it.src_pitch * es;
     const int slot = staged_slot(run_b);
-    const int n = min(kSBytes / slot, it.rows - cr);
-    const uintptr_t src0 = (uintptr_t)ptrs[it.src] + (uintptr_t)(it.src_off * es);
+    const int r0 = ij * rpc, n = min(rpc, it.rows - r0);
+    const uintptr_t src0 = (uintptr_t)ptrs[it.src] + (uintptr_t)((it.src_off + (int64_t)r0 * it.src_pitch) * es);
+    const int g0 = gstart[it.group], nrep = gstart[it.group + 1] - g0;
+    StagedStage &d = desc[warp][st];
+    if (lane < nrep)
+      d.dst[lane] = (uint64_t)ptrs[mptr[g0 + lane]] + (uint64_t)((moff[g0 + lane] + it.dst_off + (int64_t)r0 * it.dst_pitch) * es);
     uint32_t tx = 0;
-    for (int j = lane; j < n; j += 32) {
-      const uintptr_t a = src0 + (uintptr_t)((cr + j) * sp_b);
+    for (int r = lane; r < n; r += 32) {
+      const uintptr_t a = src0 + (uintptr_t)(r * sp_b);
       tx += (uint32_t)(((a + run_b + 15) & ~(uintptr_t)15) - (a & ~(uintptr_t)15));
     }
     tx = __reduce_add_sync(0xffffffffu, tx);
-    const uint32_t b = smem_u32(&bar[stage]);
+    const uint32_t b = smem_u32(&bar[warp][st]);
     if (lane == 0) {
-      desc[stage] = StagedChunk{ck, cr, n, slot};
+      d.src = src0;
+      d.sp_b = sp_b;
+      d.dp_b = it.dst_pitch * es;
+      d.run_b = (int32_t)run_b;
+      d.nrows = n;
+      d.slot = slot;
+      d.nrep = nrep;
       asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(tx) : "memory");
     }
     __syncwarp();
-    uint8_t *dst0 = sring + (size_t)stage * kSBytes;
-    for (int j = lane; j < n; j += 32) {
-      const uintptr_t a = src0 + (uintptr_t)((cr + j) * sp_b);
+    uint8_t *dst0 = ring + (size_t)st * kSBytes;
+    for (int r = lane; r < n; r += 32) {
+      const uintptr_t a = src0 + (uintptr_t)(r * sp_b);
       const uintptr_t lo = a & ~(uintptr_t)15, hi = (a + run_b + 15) & ~(uintptr_t)15;
       asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                       smem_u32(dst0 + (size_t)j * slot)),
+                       smem_u32(dst0 + (size_t)r * slot)),
                    "l"(lo), "r"((uint32_t)(hi - lo)), "r"(b)
                    : "memory");
     }
-    cr += n;
+    // next chunk of this warp
+    ij += kSWarps;
+    if (ij >= nch) {
+      ij -= nch;
+      ik += gridDim.x;
+      load_item();
+    }
+    return true;
   };
-  if (warp == 0)
-    for (int st = 0; st < kSStages && st < total; ++st) issue(st);
 
+  int issued = 0;
+  for (int st = 0; st < kSStages; ++st)
+    if (issue(st)) ++issued;
   uint32_t phases = 0;
-  for (int t = 0; t < total; ++t) {
+  for (int t = 0; t < issued; ++t) {
+    const int st = t % kSStages;
 #if RESHARD_PDL
-    if (t + 1 == total) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (t + 1 == issued && ik >= n_items) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 #endif
-    const int stage = t % kSStages;
-    const bool ok = bar_wait(smem_u32(&bar[stage]), (phases >> stage) & 1, global_ns() + kWaitLimitNs);
-    if (__syncthreads_or(!ok)) {
-      // a bulk load never completed: report, give every load in flight one more bounded wait, stop
-      if (threadIdx.x == 0) atomicOr(status, 1);
-      for (int u = t; u < total && u < t + kSStages; ++u) {
+    if (!bar_wait(smem_u32(&bar[warp][st]), (phases >> st) & 1, global_ns() + kWaitLimitNs)) {
+      // a bulk load never completed: report, give this warp's loads in flight one more bounded
+      // wait, and stop (the launch's output is incomplete)
+      if (lane == 0) atomicOr(status, 1);
+      for (int u = t; u < issued; ++u) {
         const int su = u % kSStages;
-        bar_wait(smem_u32(&bar[su]), (phases >> su) & 1, global_ns() + kWaitLimitNs);
+        bar_wait(smem_u32(&bar[warp][su]), (phases >> su) & 1, global_ns() + kWaitLimitNs);
       }
-      if (wait_last) pdl_enter();
-      return;
+      break;
     }
-    phases ^= 1u << stage;
-    const StagedChunk c = desc[stage];
-    const Item it = items[item_index(idx, c.item)];
-    const int64_t es = it.esize, run_b = (int64_t)it.run * es, sp_b = it.src_pitch * es, dp_b = it.dst_pitch * es;
-    const uintptr_t src0 = (uintptr_t)ptrs[it.src] + (uintptr_t)(it.src_off * es);
-    const int g0 = gstart[it.group], g1 = gstart[it.group + 1];
-    const uint8_t *stg = sring + (size_t)stage * kSBytes;
-    for (int j = warp; j < c.nrows; j += kBlock / 32) {
-      const int row = c.r0 + j;
-      const uint8_t *srow = stg + (size_t)j * c.slot;              // holds the row from its 16-byte block
-      const int sh0 = (int)((src0 + (uintptr_t)(row * sp_b)) & 15);  // row byte 0 sits at srow + sh0
-      for (int m = g0; m < g1; ++m) {
-        uint8_t *drow = reinterpret_cast<uint8_t *>(ptrs[mptr[m]]) + (moff[m] + it.dst_off) * es + row * dp_b;
+    phases ^= 1u << st;
+    const StagedStage &d = desc[warp][st];
+    const uintptr_t src0 = (uintptr_t)d.src;
+    const int64_t sp_b = d.sp_b, dp_b = d.dp_b;
+    const int run_b = d.run_b, nrows = d.nrows, slot = d.slot, nrep = d.nrep;
+    const uint8_t *stg = ring + (size_t)st * kSBytes;
+    for (int r = 0; r < nrows; ++r) {
+      const uint8_t *srow = stg + (size_t)r * slot;                   // the row from its 16-byte block
+      const int sh0 = (int)((src0 + (uintptr_t)(r * sp_b)) & 15);     // row byte 0 sits at srow + sh0
+      for (int f = 0; f < nrep; ++f) {
+        uint8_t *drow = reinterpret_cast<uint8_t *>(d.dst[f]) + r * dp_b;
         const int a = (int)(reinterpret_cast<uintptr_t>(drow) & 15);
-        const int nw = (int)((a + run_b + 15) >> 4);
-        const int s = (sh0 - a) & 15;  // byte phase of each destination word in the stage
+        const int nw = (a + run_b + 15) >> 4;
+        const int s = (sh0 - a) & 15;  // byte phase of every destination word in the stage
         uint8_t *dword0 = drow - a;
-        for (int w = lane; w < nw; w += 32) {
-          const int64_t start = 16 * (int64_t)w - a;  // row byte of the word's first byte
-          const int kmin = w == 0 ? a : 0;
-          const int kmax = run_b - start < 16 ? (int)(run_b - start) : 16;
-          const int base = sh0 + (int)start;           // stage offset of the word's first byte
-          const int q0 = base - s;                      // 16-byte aligned
-          uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-          if (kmin < 16 - s) lo = lds16(srow + q0);
-          if (s && kmax > 16 - s) hi = lds16(srow + q0 + 16);
-          const uint4 o = s ? shift_bytes(lo, hi, s) : lo;
-          if (kmin == 0 && kmax == 16)
-            store_stream(dword0 + 16 * (int64_t)w, o);
-          else
-            store_partial(dword0 + 16 * (int64_t)w, o, kmin, kmax);
+        const uint8_t *sw0 = srow + (sh0 - a - s);  // stage bytes of word 0 start here (or 16 before srow)
+        // whole words [wf, wl): the first word is whole when the row starts aligned, the last
+        // when the row ends on a word boundary; the next replica's words too when it has the same
+        // byte phase (each word is then read and shifted once for both)
+        const int wf = a ? 1 : 0, wl = (a + run_b) >> 4;
+        uint8_t *pair = nullptr;
+        if (f + 1 < nrep) {
+          uint8_t *drow1 = reinterpret_cast<uint8_t *>(d.dst[f + 1]) + r * dp_b;
+          if ((reinterpret_cast<uintptr_t>(drow1) & 15) == (uintptr_t)a) pair = drow1 - a;
         }
+        if (wl > wf) drain_words_at(s, sw0, dword0, pair, wf, wl, lane);
+        // the row's first and last word when partial (one lane each): only bytes [kmin, kmax)
+        // belong to the row, and only aligned stage blocks that hold some of them are read
+        int w = -1;
+        if (lane == 0 && a) w = 0;
+        if (lane == 1 && wl < nw && (wl > 0 || !a)) w = wl;
+        if (w >= 0) {
+          const int start = 16 * w - a;
+          const int kmin = w == 0 ? a : 0;
+          const int kmax = run_b - start < 16 ? run_b - start : 16;
+          uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+          if (kmin < 16 - s) lo = lds16(sw0 + 16 * w);
+          if (s && kmax > 16 - s) hi = lds16(sw0 + 16 * w + 16);
+          const uint4 o = s ? shift_bytes(lo, hi, s) : lo;
+          store_partial(dword0 + 16 * w, o, kmin, kmax);
+          if (pair) store_partial(pair + 16 * w, o, kmin, kmax);
+        }
+        if (pair) ++f;  // that replica is written too
       }
     }
-    __syncthreads();  // the stage is drained: warp 0 may refill it
-    if (warp == 0 && t + kSStages < total) issue(stage);
+    __syncwarp();  // the stage is drained: refill it
+    if (issue(st)) ++issued;
   }
   if (wait_last) pdl_enter();
 }
@@ -1520,7 +1634,8 @@ int classify(reshard_plan_t *p, int set, cudaStream_t stream) {
     const int64_t run_b = (int64_t)it.run * (int64_t)es;
     if ((m & 15) == 0) {
       idx.push_back((int32_t)i);
-    } else if (stage_ok && it.rows > 1 && run_b <= kStagedMaxRun) {
+    } else if (stage_ok && it.rows > 1 && run_b <= kStagedMaxRun &&
+               p->grp_start[(size_t)it.group + 1] - p->grp_start[(size_t)it.group] <= kStagedFan) {
       staged.push_back((int32_t)i);
     } else {
       general.push_back((int32_t)i);

@@ -16,9 +16,12 @@
  *  - "NeMo-RL: Optimizing Non-Colocated Refit for Asynchronous RL", "Optimization #2"
  *    (coalesce many tensors into one call; pack into contiguous messages).
  *
- * In this library all M source and N destination shards are separate buffers on ONE GPU,
- * so "sending" a region is a device copy. The work is split into a host-side plan (built once,
- * cached: "descriptor caching" in the ModelExpress reshard PR) and an asynchronous execute.
+ * In the single-process calls all M source and N destination shards are buffers reachable from
+ * ONE GPU, so "sending" a region is a device copy. The work is split into a host-side plan
+ * (built once, cached: "descriptor caching" in the ModelExpress reshard PR) and an asynchronous
+ * execute. When the shards are spread over several processes (one GPU each), every process runs
+ * its share of the plan (reshard_plan_partition): local copies and packing of outgoing messages,
+ * the listed point-to-point transfers (moved by the caller's communication library), unpacking.
  *
  * Conventions
  *  - All sizes, offsets and strides are in ELEMENTS of the tensor's dtype unless named _bytes.
@@ -221,14 +224,16 @@ int reshard_plan_blockwise_fp8(const reshard_tensor_spec_t *specs, int n_tensors
  * The first execute binds the plan to the current device and uploads its descriptor tables
  * (synchronous device allocations: do it outside stream capture); RESHARD_PACKED also
  * allocates the message workspace (stats.message_bytes) on first use. When the pointers differ
- * from the previous call's, the pointer table is re-uploaded on `stream`, the TMA tensor maps of
- * transposing regions are re-encoded, and the copy items are re-sorted on the host into those
- * 16-byte aligned everywhere (run by the aligned walker) and the rest (run by the general
- * walker): host work proportional to the plan's items, none when the pointers repeat.
+ * from the previous call's, the changed ones are checked, the pointer table is re-uploaded on
+ * `stream`, the TMA tensor maps of transposing regions are re-encoded, and the copy items are
+ * re-sorted on the host into those 16-byte aligned everywhere (run by the aligned walker),
+ * misaligned items of rows shorter than 4 KiB in device memory (run by the bulk-staged kernel)
+ * and the rest (run by the general walker): host work proportional to the plan's items, none
+ * when the pointers repeat.
  * Buffers must stay valid until the stream reaches the end of the work. Executes of one plan
  * on different streams that overlap in time race on its tables and workspace.
- * Errors: INVALID_ARG (NULL pointer for a non-empty shard, a pointer the device cannot
- *   dereference, plan bound to another device), UNSUPPORTED,
+ * Errors: INVALID_ARG (NULL pointer of a shard the plan reads or writes, a pointer the device
+ *   cannot dereference, plan bound to another device, a partitioned plan), UNSUPPORTED,
  *   CUDA (launch or copy failure), OOM. After an error the destinations are undefined.
  */
 int reshard_execute(reshard_plan_t *plan, void *const *src_ptrs, void *const *dst_ptrs, int mode,
@@ -312,22 +317,28 @@ int reshard_plan_transfers(const reshard_plan_t *plan, int phase, int64_t cap, r
  * the GPU for its KV cache, or a framework whose own caching allocator owns the device heap,
  * where cudaMalloc could fail for lack of memory and cudaMalloc/cudaFree would synchronize the
  * device and stall work already running.
- * The plan's descriptor tables and the pointer arrays are copied (cudaMemcpyAsync on `stream`,
+ * The plan's descriptor tables and the pointer table are copied (cudaMemcpyAsync on `stream`,
  * from pageable memory, staged before the call returns) into one file-scope device array of
- * RESHARD_STATIC_SCRATCH_BYTES bytes that the library image reserves on every GPU that loads it,
- * until the process exits; then the same copy kernel as reshard_execute runs from there. The
- * first call on a device looks the array's device address up (cudaGetSymbolAddress) with that
- * device current; make that first call before any stream capture. Calls on one device share the
- * array and it keeps the last call's contents (nothing in it needs to start at zero): calls that
- * overlap on the GPU race, so serialise them (for example, all on one stream).
- * Arguments as in reshard_execute (one destination pointer per rank), except that the pointers
- * reach the kernel as given, unchecked: device memory of the current device, managed memory, or
- * page-locked host memory whose device address equals its host address (cudaHostAlloc and
- * cudaMallocHost memory under unified addressing). The plan is only read and is not bound to a
- * device; plans with transposing regions are UNSUPPORTED here (their tensor
- * maps live with the plan). Errors: INVALID_ARG (NULL plan or pointer of a non-empty shard);
+ * RESHARD_STATIC_SCRATCH_BYTES bytes that the library image holds on every GPU that loads it,
+ * until the process exits; then the same copy kernel as reshard_execute runs from there.
+ * Set-up: every call, an empty plan's included, looks the array's device address up on the
+ * current device (cudaGetSymbolAddress, once per device; it also loads the library's device code
+ * there, which is when the array is reserved under lazy module loading, the CUDA default). So the
+ * first call on a device does that set-up: make it before any stream capture, and early (an empty
+ * plan will do) if the rest of device memory is about to be reserved by the caller.
+ * Calls on one device share the array and it keeps the last call's contents (nothing in it needs
+ * to start at zero): calls that overlap on the GPU race, so serialise them (for example, all on
+ * one stream).
+ * Arguments as in reshard_execute (one destination pointer per rank). The pointers are checked
+ * as reshard_execute checks them (cudaPointerGetAttributes, a host-side query that allocates
+ * nothing): pageable host memory and other devices' memory are refused with INVALID_ARG; the last
+ * accepted pointer set of each device is remembered, so repeating it skips the queries. The plan is
+ * only read and is not bound to a device; plans with transposing regions are UNSUPPORTED here
+ * (their tensor maps live with the plan), and partitioned plans INVALID_ARG.
+ * Errors: INVALID_ARG (NULL plan, a NULL or unreachable pointer of a shard the plan copies);
  * UNSUPPORTED when the tables need more than RESHARD_STATIC_SCRATCH_BYTES (the message gives the
- * size; split the batch or use reshard_execute); CUDA. Calls no cudaMalloc or cudaFree.
+ * size; split the batch or use reshard_execute; checked before any CUDA call); CUDA. Calls no
+ * cudaMalloc or cudaFree.
  */
 #define RESHARD_STATIC_SCRATCH_BYTES (16u << 20)
 int reshard_execute_static(const reshard_plan_t *plan, void *const *src_ptrs, void *const *dst_ptrs,
@@ -363,7 +374,8 @@ int reshard_plan_group_members(const reshard_plan_t *plan, int64_t g, int64_t ca
  * Transposing item: int64 src_off, dst_off, src_pitch, dst_pitch; int32 rows, cols, src, group,
  * esize, slab, x, y. Element (r, c) moves from src_off + r * src_pitch + c to
  * member_offset + dst_off + c * dst_pitch + r; (x, y) are (c = 0, r = 0) in slab coordinates.
- * Pointer table: [sources | destination data | destination scales | packed workspace]. Up to
+ * Pointer table: [sources | destination data | destination scales | send buffer | receive
+ * buffer] (pack items write the send buffer's group, unpack items read the receive buffer). Up to
  * cap items go to `items` (may be NULL); *n_out gets the count. Copy items are ordered largest
  * first (the walkers deal them round-robin to a persistent grid); transposing items are grouped
  * by element size (one launch per size).
@@ -392,9 +404,14 @@ int reshard_plan_slabs(const reshard_plan_t *plan, int64_t cap, int64_t *out, in
 int reshard_plan_status(reshard_plan_t *plan, int32_t *status, int reset);
 
 /* reshard_plan_destroy -- free the plan's host tables, device tables and workspace.
- * Safe on NULL. A plan that has executed first synchronizes its device (executes may still be
- * queued on any stream), so it is safe to destroy while work is in flight; it blocks until the
- * device is idle. A plan that never executed frees host memory only. */
+ * Safe on NULL. A plan that has executed first waits for the last execute it enqueued on each
+ * stream (an event per stream, not a device-wide synchronize), so it is safe to destroy while its
+ * work is in flight; it blocks until that work is done (cudaFree may also wait for the device).
+ * Its waits and frees run in relaxed stream-capture mode, so a destroy (a garbage-collected
+ * handle, say) does not invalidate a capture that another thread is recording. Executes captured
+ * into a CUDA graph are not waited for: a plan must outlive every graph that captured its
+ * executes, and the graph's launches must be complete before the plan is destroyed.
+ * A plan that never executed frees host memory only. */
 int reshard_plan_destroy(reshard_plan_t *plan);
 
 /* reshard_last_error -- text of this thread's last error ("" if none). Valid until the next

@@ -557,6 +557,10 @@ WORKLOAD_NAMES = {
     # a training side that keeps every weight transposed (source shards column-major)
     "transpose_32x14336x4096_tp8_to_dp2tp2_src_colmajor": lambda: transposed(tensors=32, side="src"),
     "moe_1x128x1536x4096_ep16_to_ep8": lambda: moe_experts(layers=1, dst="ep8"),
+    "moe_1x32x1536x4096_ep16_to_ep8": lambda: moe_experts(layers=1, experts=32, dst="ep8"),
+    # the (2,4) -> (3,) mesh reshard at 4x the rows (470 MB each way, above the 129 MB L2)
+    "mesh2x4_to_3_57344x4096": lambda: mesh2d_to_1d(rows=57344, variant="1d"),
+    "mesh2x4_to_3x2_57344x4096": lambda: mesh2d_to_1d(rows=57344, variant="2d"),
     "moe_1x128x1536x4096_ep16_to_tp4_mxfp8": lambda: moe_experts(layers=1, dst="tp4"),
     # buffers of more than 2^31 elements (64-bit element offsets)
     "large_offsets_65536x49152": lambda: large_offsets(),

@@ -382,19 +382,56 @@ def test_pageable_host_memory_is_refused_before_any_launch():
     assert_matches_oracle(wl, lay)
 
 
-def test_general_walker_build_follows_the_item_shapes():
-    """Misaligned items of many short rows run in reshard_copy_rows_kernel; misaligned single
-    long rows in reshard_copy_kernel. Both are bit-exact."""
+def test_misaligned_items_take_the_staged_kernel_or_the_general_walker():
+    """Misaligned items of many short rows in device memory run in the bulk-staged kernel; the
+    same items over page-locked host memory (no bulk copies there) in reshard_copy_rows_kernel;
+    misaligned single long rows in reshard_copy_kernel; more replicas than a staged descriptor
+    holds in the general walker too. All bit-exact."""
+    import dataclasses
     wl = S.mesh2d_to_1d(rows=512, cols=4096, variant="1d")      # destination pitch 2732 bytes
     lay, plan = run_gpu(wl)
     st = R.reshard_plan_stats(plan)
-    assert st["last_general_items"] > 0 and st["last_rows_kernel"] == 1
+    assert st["last_staged_items"] > 0 and st["last_general_items"] == 0
     assert_matches_oracle(wl, lay)
+    hl = dataclasses.replace(lay, dst_slab=torch.empty(lay.dst_slab.numel(), dtype=torch.uint8, pin_memory=True))
+    hl.dst_slab.fill_(0xA5)
+    sp, dp = R.workload_pointers(wl, hl)
+    R.reshard_execute(plan, sp, dp, stream=torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    st = R.reshard_plan_stats(plan)
+    assert st["last_staged_items"] == 0 and st["last_general_items"] > 0 and st["last_rows_kernel"] == 1
+    assert_matches_oracle(wl, hl)
     wl = S.dense_ffn(layers=1, hidden=256, ffn=1000)               # contiguous runs, shifted by 2
     lay, plan = run_gpu(wl, misalign=2)
     st = R.reshard_plan_stats(plan)
     assert st["last_general_items"] > 0 and st["last_rows_kernel"] == 0
     assert_matches_oracle(wl, lay)
+    wl = _one((96, 333), (2,), ("S1",), (12,), ("R",))            # 12 replicas of odd-width rows
+    lay, plan = run_gpu(wl)
+    st = R.reshard_plan_stats(plan)
+    assert st["last_staged_items"] == 0 and st["last_general_items"] > 0
+    assert_matches_oracle(wl, lay)
+
+
+def test_staged_kernel_row_shapes():
+    """The staged kernel over rows of every phase pair: source and destination offsets and
+    pitches that are not multiples of 16 bytes, runs from 1 to 4096 bytes, several replicas
+    with different phases, many rows per stage and one row per stage."""
+    cases = [
+        _one((300, 2048), (2,), ("S1",), (3,), ("S1",)),              # 683/682-column rows, 2-byte elements
+        _one((64, 4096), (1,), ("R",), (3,), ("S1",)),                # rows close to the 4 KiB limit
+        _one((500, 9), (1,), ("R",), (2, 2), ("S1", "R")),            # 4-5 element rows, 2 replicas
+        _one((200, 1000), (3,), ("S0",), (2, 3), ("R", "S1"), dtype="u8"),
+        _one((77, 700), (2,), ("S1",), (5,), ("S1",), dtype="f32"),
+        _one((40, 130), (1,), ("R",), (8, 2), ("R", "S1")),           # 8 replicas: the staged maximum
+    ]
+    for wl in cases:
+        for mis in (0, 2, 6):
+            if mis % S.DTYPES[wl.tensors[0].dtype][1]:
+                continue
+            lay, plan = run_gpu(wl, misalign=mis)
+            assert R.reshard_plan_stats(plan)["last_staged_items"] > 0 or mis == 0
+            assert_matches_oracle(wl, lay)
 
 
 def test_readme_example():
