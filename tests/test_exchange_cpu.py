@@ -249,3 +249,37 @@ def test_single_process_partition_is_all_local():
     st, g = R.reshard_plan_stats(rp), R.reshard_plan_stats(plan)
     assert st["message_bytes"] == st["recv_bytes"] == st["transfers"] == 0
     assert st["local_bytes"] == g["bytes_read"] and st["bytes_written"] == g["bytes_written"]
+
+
+FULL = ["dense_ffn_32x14336x4096_tp8_to_dp2tp2", "moe_8x128x1536x4096_ep16_to_ep8",
+        "moe_8x128x1536x4096_ep16_to_tp4_mxfp8", "mesh2x4_to_3x2_14336x4096",
+        "transpose_32x14336x4096_tp8_to_dp2tp2_dst_colmajor", "moe_fp8_8x128x768x2048_dp2ep8_to_dp8tp2_b128x128"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_partitioned_tables_stay_in_bounds_at_full_size(name):
+    """Every item of every pass of every rank's partitioned plan, at full size, reads and writes
+    inside its buffers (the send and receive buffers sized by the rank's stats), and the ranks'
+    receive buffers together hold every message the senders pack."""
+    import dtensor_resharding_gb300 as R
+    from test_items_cpu import check_bounds, check_transpose_bounds
+    wl = S.workload_by_name(name)
+    lay = S.allocate(wl, "meta")
+    plan = R.plan_workload(wl)
+    quant = wl.quant == "mxfp8"
+    for world, layout in ((4, "colocated"), (8, "colocated"), (4, "disjoint")):
+        so, do = owners(wl, layout, world)
+        sent = recv = 0
+        for rank in range(world):
+            rp = R.reshard_plan_partition(plan, so, do, world, rank, True)
+            st = R.reshard_plan_stats(rp)
+            for which in (0, 1, 2):
+                check_bounds(wl, lay, rp, which, quant=quant, ws=(st["message_bytes"], st["recv_bytes"]))
+                check_transpose_bounds(wl, lay, rp, which, ws=(st["message_bytes"], st["recv_bytes"]))
+            ts = R.reshard_plan_transfers(rp, 1) + R.reshard_plan_transfers(rp, 2)
+            for t in ts:
+                cap = st["message_bytes"] if t["buf"] == R.RESHARD_SEND_BUF else st["recv_bytes"]
+                assert t["offset"] % 16 == 0 and t["bytes"] % 16 == 0 and t["offset"] + t["bytes"] <= cap
+            sent += sum(t["bytes"] for t in ts if t["dir"] == R.RESHARD_SEND)
+            recv += sum(t["bytes"] for t in ts if t["dir"] == R.RESHARD_RECV)
+        assert sent == recv

@@ -18,8 +18,9 @@ from test_parity_gpu import SMALL
 DIRECT, PACK, UNPACK = 0, 1, 2
 
 
-def _ranges(wl, lay, plan):
-    """Byte range [lo, hi) in the host slabs of every pointer-table entry (workspace: own array)."""
+def _ranges(wl, lay, plan, ws=None):
+    """Byte range [lo, hi) in the host slabs of every pointer-table entry (send and receive
+    buffers: arrays of their own, `ws` = their sizes; the plan's message bytes by default)."""
     es = {"u8": 1, "bf16": 2, "f16": 2, "f32": 4, "i32": 4, "i64": 8}
     src, dst, sc = [], [], []
     for t in wl.tensors:
@@ -33,15 +34,17 @@ def _ranges(wl, lay, plan):
                 sc.append(("scale", lay.scale_off[v.buffer], lay.scale_off[v.buffer] + wl.dst_buffer_numel[v.buffer] // 32))
             else:
                 sc.append(("none", 0, 0))
-    ws = R.reshard_plan_stats(plan)["message_bytes"]
-    return src + dst + sc + [("ws", 0, ws), ("ws", 0, ws)]
+    if ws is None:
+        n = R.reshard_plan_stats(plan)["message_bytes"]
+        ws = (n, n)
+    return src + dst + sc + [("ws", 0, ws[0]), ("ws", 0, ws[1])]
 
 
-def check_bounds(wl, lay, plan, which, quant=False):
+def check_bounds(wl, lay, plan, which, quant=False, ws=None):
     items, gs, mp, mo = R.reshard_plan_items(plan, which)
     if len(items) == 0:
         return
-    table = _ranges(wl, lay, plan)
+    table = _ranges(wl, lay, plan, ws)
     n_dst = plan.n_dst_ptrs
     lo = np.array([r[1] for r in table], np.int64)
     hi = np.array([r[2] for r in table], np.int64)
@@ -72,14 +75,14 @@ def check_bounds(wl, lay, plan, which, quant=False):
             assert (lo[sp] + e0 // 32 >= lo[sp]).all() and (c1 <= hi[sp]).all(), "scale write out of bounds"
 
 
-def check_transpose_bounds(wl, lay, plan, which):
+def check_transpose_bounds(wl, lay, plan, which, ws=None):
     """Transposing items: every element read and written stays in its buffer, and every item's
     TMA slab coordinates name exactly the element its plain-load offset names, inside a slab that
     lies inside the source buffer."""
     items, gs, mp, mo = R.reshard_plan_items(plan, which + 3)
     if len(items) == 0:
         return
-    table = _ranges(wl, lay, plan)
+    table = _ranges(wl, lay, plan, ws)
     lo = np.array([r[1] for r in table], np.int64)
     hi = np.array([r[2] for r in table], np.int64)
     es = items["esize"].astype(np.int64)
