@@ -40,13 +40,23 @@ def _flat(buf):
     return buf.view(-1).view(torch.uint8)
 
 
+_started = set()  # process groups that have run a collective with every rank
+
+
 def run_transfers(plan, send_buf, recv_buf, group=None) -> None:
     """Post this rank's transfers of phase 1, wait for them, then those of phase 2.
 
     ``send_buf`` / ``recv_buf``: contiguous tensors (uint8 views are taken) on the device the
-    process group communicates from. Peers are ranks of ``group`` (the default group if None)."""
+    process group communicates from. Peers are ranks of ``group`` (the default group if None).
+    A rank with nothing to send or receive in a phase posts nothing; since a batched
+    point-to-point call that is a group's first collective must include every rank (NCCL), the
+    first call on a group starts with a barrier of the whole group."""
     import torch.distributed as dist
     _bufs(plan, send_buf, recv_buf)
+    key = id(group) if group is not None else None
+    if key not in _started:
+        dist.barrier(group=group)
+        _started.add(key)
     sb = _flat(send_buf) if send_buf is not None else None
     rb = _flat(recv_buf) if recv_buf is not None else None
     for phase in (1, 2):

@@ -37,6 +37,8 @@ def _one(shape, sm, sp, dm, dp, dtype="bf16"):
     return S.workloads._size_buffers(S.Workload("one", [t]), ns, nd)
 
 
+FUZZ = {f"fuzz_{i}": (lambda i=i: S.fuzz_cases(24, seed=29)[i]) for i in range(24)}
+
 WORKLOADS = {
     "dense_tp8_to_dp2tp2": lambda: S.dense_ffn(layers=1, hidden=128, ffn=520),
     "moe_ep4_to_ep2": lambda: S.moe_experts(layers=1, experts=8, hidden=64, ffn=48, ep_src=4, dst="ep2"),
@@ -45,11 +47,16 @@ WORKLOADS = {
     "transposed_dst": lambda: S.transposed(shape=(96, 80), src_mesh=(2,), src_pl=("S0",), dst_mesh=(2, 2),
                                            dst_pl=("R", "S0")),
     "mesh2x4_to_3x2": lambda: S.mesh2d_to_1d(rows=40, cols=77, variant="2d", dtype="u8"),
+    **FUZZ,
 }
 
 
 def owners(wl, layout, world):
-    """Process of every flat source and destination pointer index."""
+    """Process of every flat source and destination pointer index (``random``: seeded draws)."""
+    if layout == "random":
+        rng = np.random.Generator(np.random.PCG64(len(wl.tensors) * 7919 + world))
+        ns, nd = sum(t.n_src for t in wl.tensors), sum(t.n_dst for t in wl.tensors)
+        return [int(x) for x in rng.integers(0, world, ns)], [int(x) for x in rng.integers(0, world, nd)]
     so, do = [], []
     for t in wl.tensors:
         for i in range(t.n_src):
@@ -196,8 +203,9 @@ def _check(world, res, combos):
             assert all(x["stats"]["forwarded_bytes"] == 0 for x in per)
 
 
-COMBOS = [(c, lay, st) for c in sorted(WORKLOADS) for lay in ("colocated", "disjoint", "one_sender")
+COMBOS = [(c, lay, st) for c in sorted(WORKLOADS) if not c.startswith("fuzz") for lay in ("colocated", "disjoint", "one_sender")
           for st in (True, False)]
+FUZZ_COMBOS = [(c, "random", i % 2 == 0) for i, c in enumerate(sorted(FUZZ))]
 
 
 def test_two_gloo_ranks_exchange():
@@ -209,7 +217,7 @@ def test_four_gloo_ranks_exchange():
     res = _run(4, COMBOS)
     _check(4, res, COMBOS)
     # striping: the same bytes reach every receiver, but each leaves its sender once
-    for c in sorted(WORKLOADS):
+    for c in sorted(w for w in WORKLOADS if not w.startswith("fuzz")):
         for lay in ("colocated", "disjoint", "one_sender"):
             s = sum(res[r][(c, lay, True)]["stats"]["sent_bytes"] for r in range(4))
             f = sum(res[r][(c, lay, True)]["stats"]["forwarded_bytes"] for r in range(4))
@@ -218,6 +226,13 @@ def test_four_gloo_ranks_exchange():
     # a workload with destination replicas on several processes does forward stripes
     assert sum(res[r][("broadcast_to_4_replicas", "one_sender", True)]["stats"]["forwarded_bytes"]
                for r in range(4)) > 0
+
+
+def test_three_gloo_ranks_fuzzed_layouts_random_owners():
+    """Random shapes, meshes, dtypes and per-rank layouts (padded, column-major, offset views)
+    with every pointer on a random one of three processes."""
+    res = _run(3, FUZZ_COMBOS)
+    _check(3, res, FUZZ_COMBOS)
 
 
 def test_partition_rejects_bad_owners():
@@ -283,3 +298,48 @@ def test_partitioned_tables_stay_in_bounds_at_full_size(name):
             sent += sum(t["bytes"] for t in ts if t["dir"] == R.RESHARD_SEND)
             recv += sum(t["bytes"] for t in ts if t["dir"] == R.RESHARD_RECV)
         assert sent == recv
+
+
+def test_brute_force_partitions_through_the_loopback_transport():
+    """120 brute-force problems (every placement kind, nested meshes, uneven and empty chunks,
+    element-id payloads), each partitioned over 1-5 processes with random owners, striped or
+    not: every rank's emulated pack, the loopback transport and every rank's emulated unpack give
+    the oracle's destinations, each rank touching only its own buffers."""
+    import dtensor_resharding_gb300 as R
+    from dtensor_resharding_gb300 import exchange
+    from emulator import run_items
+    rng = np.random.Generator(np.random.PCG64(77))
+    for i, wl in enumerate(S.brute_force_cases(120, seed=43)):
+        world = int(rng.integers(1, 6))
+        ns, nd = sum(t.n_src for t in wl.tensors), sum(t.n_dst for t in wl.tensors)
+        so = [int(x) for x in rng.integers(0, world, ns)]
+        do = [int(x) for x in rng.integers(0, world, nd)]
+        lay = S.allocate(wl, "cpu")
+        S.fill_sources(wl, lay)
+        plan = R.plan_workload(wl)
+        want = np.full(lay.dst_slab.numel(), CANARY, np.uint8)
+        coracle.run_workload(wl, lay.src_slab.numpy(), lay.src_off, want, lay.dst_off)
+        dst = np.full(lay.dst_slab.numel(), CANARY, np.uint8)
+        parts, sends, recvs, arrays = [], [], [], []
+        for r in range(world):
+            rp = R.reshard_plan_partition(plan, so, do, world, r, bool(i % 2))
+            st = R.reshard_plan_stats(rp)
+            src = lay.src_slab.numpy().copy()
+            for k, v in enumerate(wl.tensors[0].src_views):     # one tensor per brute-force case
+                if so[k] != r:
+                    o = lay.src_off[v.buffer]
+                    src[o: o + wl.src_buffer_numel[v.buffer] * S.DTYPES[wl.tensors[0].dtype][1]] = POISON
+            send = np.zeros(max(16, st["message_bytes"]), np.uint8)
+            recv = np.zeros(max(16, st["recv_bytes"]), np.uint8)
+            a = {"src": src, "dst": dst, "send": send, "recv": recv}
+            table = table_for(wl, lay, st["message_bytes"], st["recv_bytes"])
+            run_items(rp, 0, table, a)
+            run_items(rp, 1, table, a)
+            parts.append((rp, table))
+            sends.append(torch.from_numpy(send))
+            recvs.append(torch.from_numpy(recv))
+            arrays.append(a)
+        exchange.loopback_transfers([p for p, _ in parts], sends, recvs)
+        for (rp, table), a in zip(parts, arrays):
+            run_items(rp, 2, table, a)
+        assert np.array_equal(dst, want), (i, wl.tensors[0], world, so, do)

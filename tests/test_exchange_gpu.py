@@ -78,6 +78,10 @@ def test_pack_unpack_with_caller_buffers(name, two_buffers):
 
 
 def _owners(wl, layout, world):
+    if layout == "random":
+        rng = np.random.Generator(np.random.PCG64(len(wl.tensors) * 7919 + world))
+        ns, nd = sum(t.n_src for t in wl.tensors), sum(t.n_dst for t in wl.tensors)
+        return [int(x) for x in rng.integers(0, world, ns)], [int(x) for x in rng.integers(0, world, nd)]
     so, do = [], []
     for t in wl.tensors:
         so += [i % world if layout == "colocated" else i % max(1, world // 2) for i in range(t.n_src)]
@@ -93,13 +97,8 @@ def _local(ptrs, owner, rank, per=1):
     return out
 
 
-@pytest.mark.parametrize("striped", [True, False])
-@pytest.mark.parametrize("layout", ["colocated", "disjoint"])
-@pytest.mark.parametrize("world", [2, 4])
-@pytest.mark.parametrize("name", sorted(CASES))
-def test_ranks_emulated_on_one_gpu(name, world, layout, striped):
-    wl = CASES[name]()
-    lay = _prepared(wl)
+def _emulate(wl, world, layout, striped, misalign=0):
+    lay = _prepared(wl, misalign)
     plan = R.plan_workload(wl)
     so, do = _owners(wl, layout, world)
     sp, dp = R.workload_pointers(wl, lay)
@@ -121,3 +120,18 @@ def test_ranks_emulated_on_one_gpu(name, world, layout, striped):
     assert_matches_oracle(wl, lay)
     sent = sum(R.reshard_plan_stats(p)["sent_bytes"] + R.reshard_plan_stats(p)["forwarded_bytes"] for p in plans)
     assert moved == sent
+
+
+@pytest.mark.parametrize("striped", [True, False])
+@pytest.mark.parametrize("layout", ["colocated", "disjoint"])
+@pytest.mark.parametrize("world", [2, 4])
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_ranks_emulated_on_one_gpu(name, world, layout, striped):
+    _emulate(CASES[name](), world, layout, striped)
+
+
+def test_fuzzed_layouts_random_owners_three_ranks():
+    """Random shapes, meshes, dtypes and per-rank layouts with every pointer on a random one of
+    three emulated ranks; buffers shifted by 8 bytes for every other case."""
+    for i, wl in enumerate(S.fuzz_cases(40, seed=31)):
+        _emulate(wl, 3, "random", i % 2 == 0, misalign=8 * (i % 2))
