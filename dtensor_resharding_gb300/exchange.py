@@ -40,7 +40,7 @@ def _flat(buf):
     return buf.view(-1).view(torch.uint8)
 
 
-_started = set()  # process groups that have run a collective with every rank
+_started = {}  # process groups that have run a collective with every rank (id -> the group)
 
 
 def run_transfers(plan, send_buf, recv_buf, group=None) -> None:
@@ -53,10 +53,10 @@ def run_transfers(plan, send_buf, recv_buf, group=None) -> None:
     first call on a group starts with a barrier of the whole group."""
     import torch.distributed as dist
     _bufs(plan, send_buf, recv_buf)
-    key = id(group) if group is not None else None
-    if key not in _started:
+    g = group if group is not None else dist.distributed_c10d._get_default_group()
+    if _started.get(id(g)) is not g:
         dist.barrier(group=group)
-        _started.add(key)
+        _started[id(g)] = g  # held, so that its id is not reused by a later group
     sb = _flat(send_buf) if send_buf is not None else None
     rb = _flat(recv_buf) if recv_buf is not None else None
     for phase in (1, 2):

@@ -135,3 +135,36 @@ def test_fuzzed_layouts_random_owners_three_ranks():
     three emulated ranks; buffers shifted by 8 bytes for every other case."""
     for i, wl in enumerate(S.fuzz_cases(40, seed=31)):
         _emulate(wl, 3, "random", i % 2 == 0, misalign=8 * (i % 2))
+
+
+def test_exchange_through_a_one_rank_nccl_group():
+    """exchange.reshard_exchange through a real NCCL process group of one rank (the one GPU):
+    every region is a local copy made by the pack call, the group's first-exchange barrier goes
+    through NCCL, and the result equals the oracle's. A second partition with the same plan and
+    owners reuses the group without a barrier."""
+    import os
+    import socket
+    import torch.distributed as dist
+    if dist.is_initialized():
+        pytest.skip("a process group already exists in this process")
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("nccl", rank=0, world_size=1, device_id=torch.device("cuda", 0))
+    try:
+        for wl in (CASES["dense_ragged"](), CASES["moe_tp4_mxfp8"]()):
+            lay = _prepared(wl)
+            plan = R.plan_workload(wl)
+            part = R.reshard_plan_partition(plan, [0] * plan.n_src_ptrs, [0] * plan.n_dst_ptrs, 1, 0, True)
+            st = R.reshard_plan_stats(part)
+            assert st["transfers"] == 0 and st["local_bytes"] == R.reshard_plan_stats(plan)["bytes_read"]
+            send = torch.empty(16, dtype=torch.uint8, device="cuda")
+            recv = torch.empty(16, dtype=torch.uint8, device="cuda")
+            sp, dp = R.workload_pointers(wl, lay)
+            exchange.reshard_exchange(part, sp, dp, send, recv, quant=wl.quant)
+            torch.cuda.synchronize()
+            assert_matches_oracle(wl, lay)
+    finally:
+        dist.destroy_process_group()
