@@ -623,11 +623,17 @@ int emit_tables(reshard_plan *plan, const std::vector<Role> &roles, const std::v
                   plan->titems[kUnpack], slab_ids, plan->slabs);
     }
   }
-#if RESHARD_SIZE_ORDER
+#if RESHARD_SIZE_ORDER == 1
   // largest items first: the persistent grid deals items round-robin, so CTAs finish together
   for (auto &iv : plan->items)
     std::stable_sort(iv.begin(), iv.end(), [](const Item &a, const Item &b) {
       return (int64_t)a.rows * a.run * a.esize > (int64_t)b.rows * b.run * b.esize;
+    });
+#elif RESHARD_SIZE_ORDER == 2
+  // by destination: items writing neighbouring bytes of one replica group run close together
+  for (auto &iv : plan->items)
+    std::stable_sort(iv.begin(), iv.end(), [](const Item &a, const Item &b) {
+      return a.group != b.group ? a.group < b.group : a.dst_off < b.dst_off;
     });
 #endif
   // transposing items grouped by element size: the executor launches one build of its

@@ -244,8 +244,8 @@ def uneven_tp(rows: int = 14336, cols: int = 4096, src: int = 6, dst: int = 5, s
 
 
 def mesh2d_to_1d(rows: int = 14336, cols: int = 4096, variant: str = "1d", seed: int = 5,
-                 dtype: str = "bf16") -> Workload:
-    """A (2,4) [Shard(0), Shard(1)] source into a 3-way column split.
+                 dtype: str = "bf16", src_cols: int = 4) -> Workload:
+    """A (2, src_cols) [Shard(0), Shard(1)] source into a 3-way column split.
 
     ``variant="1d"``: destination mesh (3,) [Shard(1)]; ``"2d"``: (3,2) [Shard(1), Replicate].
     """
@@ -254,9 +254,10 @@ def mesh2d_to_1d(rows: int = 14336, cols: int = 4096, variant: str = "1d", seed:
     else:
         dmesh, dpl = (3, 2), ("S1", "R")
     nd = int(np.prod(dmesh))
-    t = TensorDesc("w", (rows, cols), dtype, (2, 4), ("S0", "S1"), dmesh, dpl,
-                   _dense_views(8, 0), _dense_views(nd, 0), seed=seed, std=1.0)
-    return _size_buffers(Workload(f"mesh2x4_to_{'x'.join(map(str, dmesh))}_{rows}x{cols}", [t]), 8, nd)
+    ns = 2 * src_cols
+    t = TensorDesc("w", (rows, cols), dtype, (2, src_cols), ("S0", "S1"), dmesh, dpl,
+                   _dense_views(ns, 0), _dense_views(nd, 0), seed=seed, std=1.0)
+    return _size_buffers(Workload(f"mesh2x{src_cols}_to_{'x'.join(map(str, dmesh))}_{rows}x{cols}", [t]), ns, nd)
 
 
 def many_small(n: int = 10000, size_seed: int = 55, value_seed: int = 56, rows=(64, 512),
@@ -561,6 +562,9 @@ WORKLOAD_NAMES = {
     # the (2,4) -> (3,) mesh reshard at 4x the rows (470 MB each way, above the 129 MB L2)
     "mesh2x4_to_3_57344x4096": lambda: mesh2d_to_1d(rows=57344, variant="1d"),
     "mesh2x4_to_3x2_57344x4096": lambda: mesh2d_to_1d(rows=57344, variant="2d"),
+    # the same destination split from a (2,1) source: each destination row comes from one region
+    "mesh2x1_to_3_14336x4096": lambda: mesh2d_to_1d(variant="1d", src_cols=1),
+    "mesh2x1_to_3_57344x4096": lambda: mesh2d_to_1d(rows=57344, variant="1d", src_cols=1),
     "moe_1x128x1536x4096_ep16_to_tp4_mxfp8": lambda: moe_experts(layers=1, dst="tp4"),
     # buffers of more than 2^31 elements (64-bit element offsets)
     "large_offsets_65536x49152": lambda: large_offsets(),
