@@ -383,12 +383,13 @@ def test_pageable_host_memory_is_refused_before_any_launch():
 
 
 def test_misaligned_items_take_the_staged_kernel_or_the_general_walker():
-    """Misaligned items of many short rows in device memory run in the bulk-staged kernel; the
-    same items over page-locked host memory (no bulk copies there) in reshard_copy_rows_kernel;
-    misaligned single long rows in reshard_copy_kernel; more replicas than a staged descriptor
-    holds in the general walker too. All bit-exact."""
+    """Misaligned items of many short rows in device memory run in the bulk-staged kernel when
+    some group has two or more replicas or the rows move at least 512 MB; short single-replica
+    launches, and the same items over page-locked host memory (no bulk copies there), in
+    reshard_copy_rows_kernel; misaligned single long rows in reshard_copy_kernel; more replicas
+    than a staged descriptor holds in the general walker too. All bit-exact."""
     import dataclasses
-    wl = S.mesh2d_to_1d(rows=512, cols=4096, variant="1d")      # destination pitch 2732 bytes
+    wl = S.mesh2d_to_1d(rows=512, cols=4096, variant="2d")      # destination pitch 2732 bytes, 2 replicas
     lay, plan = run_gpu(wl)
     st = R.reshard_plan_stats(plan)
     assert st["last_staged_items"] > 0 and st["last_general_items"] == 0
@@ -401,6 +402,11 @@ def test_misaligned_items_take_the_staged_kernel_or_the_general_walker():
     st = R.reshard_plan_stats(plan)
     assert st["last_staged_items"] == 0 and st["last_general_items"] > 0 and st["last_rows_kernel"] == 1
     assert_matches_oracle(wl, hl)
+    wl = S.mesh2d_to_1d(rows=512, cols=4096, variant="1d")      # one replica, 8 MB: the many-rows walker
+    lay, plan = run_gpu(wl)
+    st = R.reshard_plan_stats(plan)
+    assert st["last_staged_items"] == 0 and st["last_general_items"] > 0 and st["last_rows_kernel"] == 1
+    assert_matches_oracle(wl, lay)
     wl = S.dense_ffn(layers=1, hidden=256, ffn=1000)               # contiguous runs, shifted by 2
     lay, plan = run_gpu(wl, misalign=2)
     st = R.reshard_plan_stats(plan)
@@ -415,14 +421,15 @@ def test_misaligned_items_take_the_staged_kernel_or_the_general_walker():
 
 def test_staged_kernel_row_shapes():
     """The staged kernel over rows of every phase pair: source and destination offsets and
-    pitches that are not multiples of 16 bytes, runs from 1 to 4096 bytes, several replicas
-    with different phases, many rows per stage and one row per stage."""
+    pitches that are not multiples of 16 bytes, runs from 1 to 4096 bytes, 2 to 8 replicas (odd
+    counts drain a pair of equal-phase replicas together and the last one alone), many rows per
+    stage and one row per stage."""
     cases = [
-        _one((300, 2048), (2,), ("S1",), (3,), ("S1",)),              # 683/682-column rows, 2-byte elements
-        _one((64, 4096), (1,), ("R",), (3,), ("S1",)),                # rows close to the 4 KiB limit
+        _one((300, 2048), (2,), ("S1",), (3, 3), ("S1", "R")),        # 683/682-column rows, 3 replicas
+        _one((64, 4096), (1,), ("R",), (3, 2), ("S1", "R")),          # rows close to the 4 KiB limit
         _one((500, 9), (1,), ("R",), (2, 2), ("S1", "R")),            # 4-5 element rows, 2 replicas
         _one((200, 1000), (3,), ("S0",), (2, 3), ("R", "S1"), dtype="u8"),
-        _one((77, 700), (2,), ("S1",), (5,), ("S1",), dtype="f32"),
+        _one((77, 702), (2,), ("S1",), (5, 3), ("S1", "R"), dtype="f32"),   # 564-byte rows
         _one((40, 130), (1,), ("R",), (8, 2), ("R", "S1")),           # 8 replicas: the staged maximum
     ]
     for wl in cases:
@@ -432,6 +439,15 @@ def test_staged_kernel_row_shapes():
             lay, plan = run_gpu(wl, misalign=mis)
             assert R.reshard_plan_stats(plan)["last_staged_items"] > 0 or mis == 0
             assert_matches_oracle(wl, lay)
+
+
+def test_staged_kernel_single_replica_at_size():
+    """One replica: the staged kernel takes the rows once they move 512 MB or more (here the
+    (2,4) -> (3,) mesh reshard at 4x the rows, 940 MB read + written); compared whole."""
+    wl = S.mesh2d_to_1d(rows=57344, variant="1d")
+    lay, plan = run_gpu(wl)
+    assert R.reshard_plan_stats(plan)["last_staged_items"] > 0
+    assert_matches_oracle(wl, lay)
 
 
 def test_readme_example():
