@@ -205,13 +205,27 @@ def time_oracle_parallel(wl, src_host, src_off, n_tensors: int):
 
 
 def _scaled_first_tensor(wl, frac: float):
-    """The workload's first tensor with dim 0 cut to about `frac` of its length (dense views)."""
+    """The workload's first tensor with one dim cut to about `frac` of its length (dense views):
+    the outermost dim with room for that cut in whole multiples of the shard counts that split
+    it (source times destination), else the dim with the most such room."""
     import numpy as np
     import synthetic as S
     t = wl.tensors[0]
-    step = int(np.prod(t.src_mesh)) * int(np.prod(t.dst_mesh))
-    rows = max(step, int(t.global_shape[0] * frac) // step * step)
-    shape = (rows,) + tuple(t.global_shape[1:])
+    nd_ = len(t.global_shape)
+
+    def splits(d):
+        g = 1
+        for mesh, pls in ((t.src_mesh, t.src_placements), (t.dst_mesh, t.dst_placements)):
+            g *= int(np.prod([m for m, p in zip(mesh, pls) if p == f"S{d}"] or [1]))
+        return g
+
+    room = [t.global_shape[d] // splits(d) for d in range(nd_)]
+    need = 1.0 / max(frac, 1e-9)
+    cut = next((d for d in range(nd_) if room[d] >= need), int(np.argmax(room)))
+    g = splits(cut)
+    shape = list(t.global_shape)
+    shape[cut] = max(g, int(t.global_shape[cut] * frac) // g * g)
+    shape = tuple(shape)
     ns, nd = int(np.prod(t.src_mesh)), int(np.prod(t.dst_mesh))
     d = S.TensorDesc(t.name, shape, t.dtype, t.src_mesh, t.src_placements, t.dst_mesh, t.dst_placements,
                      [S.View(i) for i in range(ns)], [S.View(i) for i in range(nd)], t.seed, t.std)
@@ -288,6 +302,7 @@ def dominant_kernel(R, plan, mode: str, quant: str) -> str:
     st = R.reshard_plan_stats(plan)
     counts = {"reshard_copy_aligned_kernel": st["last_aligned_items"],
               "reshard_copy_staged_kernel": st["last_staged_items"],
+              "reshard_copy_gather_kernel": st["last_gather_items"],
               ("reshard_copy_rows_kernel" if st["last_rows_kernel"] else "reshard_copy_kernel"): st["last_general_items"]}
     return max(counts, key=counts.get)
 
@@ -539,7 +554,7 @@ def our_arm(args, rank: int, world: int, local_rank: int) -> None:
         roofline["note"] = "packed mode: the step is the pack and unpack launches; achieved counts both passes' bytes"
     elif launches > 1:
         roofline["note"] = (f"the step is {launches} launches (aligned walker, bulk-staged kernel, general "
-                            "walker and/or transposing kernel, back to back on one stream): achieved and "
+                            "walker, gather kernel and/or transposing kernel, back to back on one stream): achieved and "
                             "frac cover the whole step; the kernel named is the one with the most items")
     same = copy_rate_same_run(dev)
     roofline["copy_rate_same_run"] = round(same, 1)
