@@ -68,7 +68,8 @@ class TensorSpecT(ctypes.Structure):
 STATS_FIELDS = ("n_tensors", "regions", "items", "dst_groups", "messages", "bytes_read", "bytes_written",
                 "wire_bytes", "message_bytes", "gather_bcast_bytes", "global_bytes", "last_launches",
                 "last_aligned_items", "last_general_items", "last_rows_kernel", "recv_bytes", "rank", "world",
-                "transfers", "sent_bytes", "forwarded_bytes", "local_bytes", "last_staged_items")
+                "transfers", "sent_bytes", "forwarded_bytes", "local_bytes", "last_staged_items", "gather_items",
+                "last_gather_items")
 
 
 class StatsT(ctypes.Structure):
@@ -521,14 +522,20 @@ TITEM_DTYPE = [("src_off", "<i8"), ("dst_off", "<i8"), ("src_pitch", "<i8"), ("d
                ("slab", "<i4"), ("x", "<i4"), ("y", "<i4")]
 
 
+GITEM_DTYPE = [("src_off", "<i8", (2,)), ("src_pitch", "<i8", (2,)), ("dst_off", "<i8"), ("dst_pitch", "<i8"),
+               ("run", "<i4", (2,)), ("src", "<i4", (2,)), ("rows", "<i4"), ("group", "<i4"), ("esize", "<i4"),
+               ("pad", "<i4")]
+
+
 def reshard_plan_items(plan: Plan, which: int = 0):
     """(items as a numpy structured array, group_start, member_ptr, member_off) of one table:
-    0/1/2 strided-copy items of the direct/pack/unpack pass, 3/4/5 their transposing items."""
+    0/1/2 strided-copy items of the direct/pack/unpack pass, 3/4/5 their transposing items, 6 the
+    direct pass's gather items (copy items they cover have pad[0] == 1)."""
     import numpy as np
     n, ng, nm = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
     _check(LIB.reshard_plan_items(plan.handle, which, 0, None, ctypes.byref(n), None, None, None,
                                   ctypes.byref(ng), ctypes.byref(nm)))
-    items = np.zeros(n.value, dtype=ITEM_DTYPE if which < 3 else TITEM_DTYPE)
+    items = np.zeros(n.value, dtype=ITEM_DTYPE if which < 3 else TITEM_DTYPE if which < 6 else GITEM_DTYPE)
     gs = np.zeros(ng.value + 1, np.int32)
     mp = np.zeros(max(1, nm.value), np.int32)
     mo = np.zeros(max(1, nm.value), np.int64)

@@ -463,6 +463,110 @@ __global__ void __launch_bounds__(kBlock, RESHARD_ROWS_MIN_BLOCKS) reshard_copy_
   if (wait_last) pdl_enter();
 }
 
+// ------------------------------------------------------------------------ gather rows --
+
+// One destination row assembled from two source pieces: row bytes [0, B) come from s0 (row byte
+// b at s0 + b), bytes [B, rb) from s1 (row byte b at s1 + b - B). The row's destination words
+// are taken piece by piece: piece 0's words (the first up to the one holding byte B - 1), then
+// piece 1's (from the one holding byte B), so a word that holds the boundary is written twice,
+// each time with only its own piece's bytes. Every word is one or two 16-byte block loads of its
+// piece and a funnel shift by that piece's phase, as in copy_shifted_rows; the lanes of one row
+// walk its words together. dst[f] are the row's starts in NF replicas with equal phase mod 16.
+template <int NF, int RU>
+__device__ __forceinline__ void gather_row(const uint8_t *s0, const uint8_t *s1, int64_t B, int64_t rb,
+                                           uint8_t *const *dst, int nf, int lane) {
+  const int a = (int)(reinterpret_cast<uintptr_t>(dst[0]) & 15);
+  const int nw = (int)((a + rb + 15) >> 4);   // destination words the row touches
+  const int wb0 = (int)((a + B - 1) >> 4);     // the last word with piece-0 bytes
+  const int wb1 = (int)((a + B) >> 4);         // the first word with piece-1 bytes
+  const int nv = wb0 + 1 + nw - wb1;           // words of both pieces, the shared one twice
+  const uintptr_t p0 = reinterpret_cast<uintptr_t>(s0) - a;      // source of word 0's byte 0, piece 0
+  const uintptr_t p1 = reinterpret_cast<uintptr_t>(s1) - B - a;  // ... piece 1 (never read there)
+  const int sh0 = (int)(p0 & 15), sh1 = (int)(p1 & 15);
+  for (int v0 = lane; v0 < nv; v0 += 32 * RU) {
+    uint4 lo[RU], hi[RU];
+    int kmin[RU], kmax[RU], sh[RU];
+    int64_t start[RU];
+#pragma unroll
+    for (int u = 0; u < RU; ++u) {
+      const int v = v0 + 32 * u;
+      kmin[u] = 16;
+      kmax[u] = 0;
+      sh[u] = 0;
+      start[u] = 0;
+      lo[u] = make_uint4(0, 0, 0, 0);
+      hi[u] = make_uint4(0, 0, 0, 0);
+      if (v < nv) {
+        const bool second = v > wb0;
+        const int w = second ? wb1 + (v - wb0 - 1) : v;
+        const int64_t st = 16 * (int64_t)w - a;  // row byte of the word's byte 0
+        const int64_t lo_b = second ? B : 0, hi_b = second ? rb : B;
+        kmin[u] = (int)(lo_b - st > 0 ? lo_b - st : 0);
+        kmax[u] = (int)(hi_b - st < 16 ? hi_b - st : 16);
+        sh[u] = second ? sh1 : sh0;
+        start[u] = st;
+        const uint8_t *blk = reinterpret_cast<const uint8_t *>((second ? p1 : p0) - sh[u]) + 16 * (int64_t)w;
+        if (kmin[u] < 16 - sh[u]) lo[u] = __ldg(reinterpret_cast<const uint4 *>(blk));
+        if (sh[u] && kmax[u] > 16 - sh[u]) hi[u] = __ldg(reinterpret_cast<const uint4 *>(blk + 16));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < RU; ++u) {
+      if (kmin[u] >= kmax[u]) continue;
+      const uint4 o = sh[u] ? shift_bytes(lo[u], hi[u], sh[u]) : lo[u];
+      if (kmin[u] == 0 && kmax[u] == 16) {
+#pragma unroll
+        for (int f = 0; f < NF; ++f)
+          if (f < nf) store_stream(dst[f] + start[u], o);
+      } else {
+#pragma unroll
+        for (int f = 0; f < NF; ++f)
+          if (f < nf) store_partial(dst[f] + start[u], o, kmin[u], kmax[u]);
+      }
+    }
+  }
+}
+
+// Gather items: a persistent grid deals items round-robin, and each CTA's warps take the item's
+// rows in turn. Replicas go two per pass when their phases agree mod 16, else one per pass.
+// `wait_last` as in reshard_copy_kernel.
+__global__ void __launch_bounds__(kBlock, RESHARD_ROWS_MIN_BLOCKS) reshard_copy_gather_kernel(
+    const GItem *__restrict__ items, int n_items, const uint64_t *__restrict__ ptrs,
+    const int32_t *__restrict__ gstart, const int32_t *__restrict__ mptr, const int64_t *__restrict__ moff,
+    int wait_last) {
+  if (!wait_last) pdl_enter();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int k = blockIdx.x; k < n_items; k += gridDim.x) {
+    pdl_last_item(k, n_items);
+    const GItem &it = items[k];
+    const int64_t es = it.esize;
+    const uint8_t *s0 = reinterpret_cast<const uint8_t *>(ptrs[it.src[0]]) + it.src_off[0] * es;
+    const uint8_t *s1 = reinterpret_cast<const uint8_t *>(ptrs[it.src[1]]) + it.src_off[1] * es;
+    const int64_t B = (int64_t)it.run[0] * es, rb = B + (int64_t)it.run[1] * es;
+    const int64_t sp0 = it.src_pitch[0] * es, sp1 = it.src_pitch[1] * es, dp = it.dst_pitch * es;
+    const int rows = it.rows;
+    const int g0 = gstart[it.group], nrep = gstart[it.group + 1] - g0;
+    for (int f0 = 0; f0 < nrep; f0 += 2) {
+      const int nf = min(2, nrep - f0);
+      uint8_t *dst[2];
+      dst[0] = reinterpret_cast<uint8_t *>(ptrs[mptr[g0 + f0]]) + (moff[g0 + f0] + it.dst_off) * es;
+      dst[1] = nf > 1 ? reinterpret_cast<uint8_t *>(ptrs[mptr[g0 + f0 + 1]]) + (moff[g0 + f0 + 1] + it.dst_off) * es
+                      : dst[0];
+      const bool same = ((reinterpret_cast<uintptr_t>(dst[0]) ^ reinterpret_cast<uintptr_t>(dst[1])) & 15) == 0;
+      for (int r = warp; r < rows; r += kBlock / 32) {
+        uint8_t *row[2] = {dst[0] + r * dp, dst[1] + r * dp};
+        if (same) {
+          gather_row<2, RESHARD_ROW_UNROLL>(s0 + r * sp0, s1 + r * sp1, B, rb, row, nf, lane);
+        } else {
+          gather_row<1, RESHARD_ROW_UNROLL>(s0 + r * sp0, s1 + r * sp1, B, rb, row, 1, lane);
+          gather_row<1, RESHARD_ROW_UNROLL>(s0 + r * sp0, s1 + r * sp1, B, rb, row + 1, 1, lane);
+        }
+      }
+    }
+  }
+  if (wait_last) pdl_enter();
+}
+
 // The aligned walker: items the host found 16-byte aligned everywhere (sources, every replica,
 // runs and pitches) for the current pointers; 16-byte copies only, more loads in flight. An
 // item that is not aligned after all is skipped and reported in bit 1 of the status word.
@@ -1411,6 +1515,7 @@ struct LaunchCaps {
   int aligned_grid = 0;
   int copy_grid = 0;
   int rows_grid = 0;
+  int gather_grid = 0;
   int staged_grid = 0;
   int mxfp8_grid = 0;
   int transpose_grid[4] = {0, 0, 0, 0};  // per element size 1, 2, 4, 8 bytes
@@ -1432,6 +1537,8 @@ int launch_caps(int device, LaunchCaps &c) {
   }
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, reshard_copy_kernel, kBlock, 0));
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b4, reshard_copy_rows_kernel, kBlock, 0));
+  int bg = 0;
+  RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bg, reshard_copy_gather_kernel, kBlock, 0));
   int bs = 0;
   RS_CUDA(cudaFuncSetAttribute(reshard_copy_staged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStagedSmem));
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bs, reshard_copy_staged_kernel, kBlock, kStagedSmem));
@@ -1446,6 +1553,7 @@ int launch_caps(int device, LaunchCaps &c) {
   g_caps.bulk_grid = sms * std::max(1, bb);
   g_caps.copy_grid = sms * std::max(1, b1);
   g_caps.rows_grid = sms * std::max(1, b4);
+  g_caps.gather_grid = sms * std::max(1, bg);
   g_caps.staged_grid = sms * std::max(1, bs);
   g_caps.mxfp8_grid = sms * std::max(1, b2);
   for (int k = 0; k < 4; ++k) g_caps.transpose_grid[k] = sms * std::max(1, bt[k]);
@@ -1628,8 +1736,11 @@ int classify(reshard_plan_t *p, int set, cudaStream_t stream) {
   int64_t gen_bytes = 0, row_bytes = 0;
   // bulk copies read device memory only (page-locked host memory goes through the walkers)
   const bool stage_ok = RESHARD_STAGED && !p->any_host;
+  // the direct pass's gather items write the rows of the copy items flagged kGathered
+  const bool gathered = set == kDirect && !p->gitems.empty();
   for (size_t i = 0; i < items.size(); ++i) {
     const Item &it = items[i];
+    if (gathered && it.pad[0] == kGathered) continue;
     const uint64_t es = (uint64_t)it.esize;
     uint64_t m = tab[(size_t)it.src] + (uint64_t)it.src_off * es;
     m |= (uint64_t)it.run * es;
@@ -1675,6 +1786,7 @@ int classify(reshard_plan_t *p, int set, cudaStream_t stream) {
   }
   p->n_aligned[set] = (int32_t)idx.size();
   p->n_staged[set] = (int32_t)staged.size();
+  p->n_general[set] = (int32_t)general.size();
   // the general items run in the many-rows build when most of their bytes are short rows
   p->gen_rows[set] = 2 * row_bytes > gen_bytes;
   idx.insert(idx.end(), staged.begin(), staged.end());
@@ -1703,11 +1815,13 @@ int launch(reshard_plan_t *p, int set, bool quant, cudaStream_t stream, const La
     ++p->last_launches;
   } else {
     if ((rc = classify(p, set, stream))) return rc;
-    const int na = p->n_aligned[set], ns = p->n_staged[set], ng = n - na - ns;
+    const int na = p->n_aligned[set], ns = p->n_staged[set], ng = p->n_general[set];
+    const int nx = set == kDirect ? (int)p->gitems.size() : 0;
     const int32_t *idx = p->d_cls_idx[set];
     p->last_aligned = na;
     p->last_staged = ns;
     p->last_general = ng;
+    if (nx) p->last_gather = nx;
     if (na > 0 && RESHARD_BULK && !p->any_host) {  // bulk copies over device memory only
       RS_CUDA(launch_kernel(true, reshard_bulk_kernel, std::min(na, caps.bulk_grid), 32, kBulkSmem, stream, items, idx, na,
                             p->d_ptrs, p->d_grp_start, p->d_mem_ptr, p->d_mem_off, p->d_status));
@@ -1737,6 +1851,18 @@ int launch(reshard_plan_t *p, int set, bool quant, cudaStream_t stream, const La
                             idx + na + ns, ng, p->d_ptrs, p->d_grp_start, p->d_mem_ptr, p->d_mem_off, wait_last));
       ++p->last_launches;
     }
+    if (nx > 0) {
+      if (!p->d_gitems) {
+        GItem *d = nullptr;
+        if ((rc = upload(&d, p->gitems))) return rc;
+        p->d_gitems = d;
+      }
+      const int wait_gather = RESHARD_GEN_OVERLAP && na + ns + ng > 0 ? 1 : 0;
+      RS_CUDA(launch_kernel(true, reshard_copy_gather_kernel, std::min(nx, caps.gather_grid), kBlock, 0, stream,
+                            static_cast<const GItem *>(p->d_gitems), nx, p->d_ptrs, p->d_grp_start, p->d_mem_ptr,
+                            p->d_mem_off, wait_gather));
+      ++p->last_launches;
+    }
   }
   RS_CUDA(cudaGetLastError());
   return RESHARD_OK;
@@ -1755,6 +1881,8 @@ void free_device(reshard_plan_t *p) {
     if (d) cudaFree(d);
     d = nullptr;
   }
+  if (p->d_gitems) cudaFree(p->d_gitems);
+  p->d_gitems = nullptr;
   if (p->d_maps) cudaFree(p->d_maps);
   if (p->d_map_ok) cudaFree(p->d_map_ok);
   if (p->d_status) cudaFree(p->d_status);
@@ -1950,6 +2078,7 @@ extern "C" int reshard_execute(reshard_plan_t *p, void *const *src_ptrs, void *c
   }
   if ((rc = stage_pointers(p, u, stream))) return rc;
   p->last_launches = 0;
+  p->last_gather = 0;
   if (mode == RESHARD_DIRECT) {
     rc = launch(p, kDirect, q, stream, caps);
   } else if (!(rc = launch(p, kPack, false, stream, caps))) {
@@ -1984,6 +2113,7 @@ extern "C" int reshard_execute_pack(reshard_plan_t *p, void *const *src_ptrs, vo
   u.emplace_back(p->workspace_ptr, reinterpret_cast<uint64_t>(send_buf));
   if ((rc = stage_pointers(p, u, stream))) return rc;
   p->last_launches = 0;
+  p->last_gather = 0;
   if (direct && (rc = launch(p, kDirect, q, stream, caps))) return rc;
   if (pack && (rc = launch(p, kPack, false, stream, caps))) return rc;
   record_done(p, stream);
@@ -2009,6 +2139,7 @@ extern "C" int reshard_execute_unpack(reshard_plan_t *p, const void *recv_buf, v
   u.emplace_back(p->workspace_ptr + 1, reinterpret_cast<uint64_t>(recv_buf));
   if ((rc = stage_pointers(p, u, stream))) return rc;
   p->last_launches = 0;
+  p->last_gather = 0;
   if ((rc = launch(p, kUnpack, q, stream, caps))) return rc;
   record_done(p, stream);
   return RESHARD_OK;

@@ -539,6 +539,127 @@ int64_t region_bytes(const reshard_plan &p, const Region &r) {
 
 int64_t align16(int64_t x) { return (x + 15) / 16 * 16; }
 
+// Element offset of region r's origin in its source's buffer, and that source's view.
+const RankView &region_source(const reshard_plan &p, const Region &r, int64_t &so) {
+  const TensorInfo &t = p.tensors[(size_t)r.tensor];
+  const Box &sb = t.src_box[(size_t)r.src];
+  const RankView &sv = t.src_view[(size_t)r.src];
+  so = sv.offset;
+  for (int d = 0; d < t.ndim; ++d) so += (r.box.lo[d] - sb.lo[d]) * sv.strides[d];
+  return sv;
+}
+
+// Element offset of region r's origin relative to a member of device group g (the members share
+// strides; each adds its own view offset), and those strides.
+const int64_t *region_dest(const reshard_plan &p, const Region &r, const Group &g, int64_t &dof) {
+  const TensorInfo &t = p.tensors[(size_t)r.tensor];
+  const RankView &dv = t.dst_view[(size_t)g.members[0]];
+  dof = 0;
+  for (int d = 0; d < t.ndim; ++d) dof += (r.box.lo[d] - g.box.lo[d]) * dv.strides[d];
+  return dv.strides;
+}
+
+// Pairs of direct regions that form whole destination rows together: same tensor and device
+// group, the same box but for the last dim, where region A ends at region B's start; the last
+// dim contiguous on both sources and the destination, at least two elements of each piece and
+// two rows. Only rows misaligned by construction pair up (the destination pitch or piece A's
+// length is not a multiple of 16 bytes), where the two plain items would each be walked as
+// short rows. partner[A] = B, partner[B] = -2 - A, -1 for an unpaired region.
+std::vector<int64_t> gather_pairs(const reshard_plan &p, const std::vector<Role> &roles,
+                                  const std::vector<Group> &dev_groups) {
+  std::vector<int64_t> partner(p.regions.size(), -1);
+  if (!RESHARD_GATHER) return partner;
+  // candidates keyed by (tensor, device group, the box outside the last dim)
+  std::map<std::vector<int64_t>, std::vector<size_t>> rows_of;
+  for (size_t i = 0; i < p.regions.size(); ++i) {
+    const Region &r = p.regions[i];
+    const TensorInfo &t = p.tensors[(size_t)r.tensor];
+    const int nd = t.ndim, last = nd - 1;
+    if (roles[i].direct < 0 || nd < 2) continue;
+    if (r.box.hi[last] - r.box.lo[last] < 2 || r.box.hi[last - 1] - r.box.lo[last - 1] < 2) continue;
+    if (t.src_view[(size_t)r.src].strides[last] != 1) continue;
+    const Group &g = dev_groups[(size_t)roles[i].direct];
+    if (t.dst_view[(size_t)g.members[0]].strides[last] != 1) continue;
+    std::vector<int64_t> key{r.tensor, roles[i].direct};
+    for (int d = 0; d < last; ++d) {
+      key.push_back(r.box.lo[d]);
+      key.push_back(r.box.hi[d]);
+    }
+    rows_of[key].push_back(i);
+  }
+  for (auto &kv : rows_of) {
+    std::vector<size_t> &v = kv.second;
+    if (v.size() < 2) continue;
+    const TensorInfo &t = p.tensors[(size_t)p.regions[v[0]].tensor];
+    const int last = t.ndim - 1;
+    std::sort(v.begin(), v.end(), [&](size_t a, size_t b) { return p.regions[a].box.lo[last] < p.regions[b].box.lo[last]; });
+    for (size_t k = 0; k + 1 < v.size(); ++k) {
+      const Region &a = p.regions[v[k]], &b = p.regions[v[k + 1]];
+      if (a.box.hi[last] != b.box.lo[last]) continue;
+      const Group &g = dev_groups[(size_t)roles[v[k]].direct];
+      const int64_t dpitch = t.dst_view[(size_t)g.members[0]].strides[last - 1] * t.esize;
+      const int64_t len_a = (a.box.hi[last] - a.box.lo[last]) * t.esize;
+      if (dpitch % 16 == 0 && len_a % 16 == 0) continue;
+      const int64_t row_b = (b.box.hi[last] - a.box.lo[last]) * t.esize;
+      if (row_b > INT32_MAX) continue;
+      partner[v[k]] = (int64_t)v[k + 1];
+      partner[v[k + 1]] = -2 - (int64_t)v[k];
+      ++k;  // rows of three or more pieces: the first two pair, the rest stay plain
+    }
+  }
+  return partner;
+}
+
+// Gather items of the pair (a, b): the rows dim is the last but one, outer dims are walked
+// explicitly, and each item takes about item_bytes of source.
+void emit_gather(reshard_plan &p, size_t a, size_t b, const std::vector<Role> &roles, const std::vector<Group> &dev_groups,
+                 int64_t item_bytes) {
+  const Region &ra = p.regions[a], &rb = p.regions[b];
+  const TensorInfo &t = p.tensors[(size_t)ra.tensor];
+  const int nd = t.ndim, last = nd - 1, rd = nd - 2;
+  int64_t so[2], dof;
+  const RankView &va = region_source(p, ra, so[0]);
+  const RankView &vb = region_source(p, rb, so[1]);
+  const int64_t *ds = region_dest(p, ra, dev_groups[(size_t)roles[a].direct], dof);
+  int64_t ext[kMaxDims];
+  for (int d = 0; d < nd; ++d) ext[d] = ra.box.hi[d] - ra.box.lo[d];
+  const int64_t len[2] = {ext[last], rb.box.hi[last] - rb.box.lo[last]};
+  const int64_t row_b = (len[0] + len[1]) * t.esize;
+  const int64_t per = std::max<int64_t>(1, item_bytes / row_b);
+  int64_t idx[kMaxDims] = {0, 0, 0, 0};
+  for (;;) {
+    int64_t s0[2] = {so[0], so[1]}, d0 = dof;
+    for (int d = 0; d < rd; ++d) {
+      s0[0] += idx[d] * va.strides[d];
+      s0[1] += idx[d] * vb.strides[d];
+      d0 += idx[d] * ds[d];
+    }
+    for (int64_t r = 0; r < ext[rd]; r += per) {
+      GItem g{};
+      g.rows = (int32_t)std::min(per, ext[rd] - r);
+      g.src_off[0] = s0[0] + r * va.strides[rd];
+      g.src_off[1] = s0[1] + r * vb.strides[rd];
+      g.src_pitch[0] = va.strides[rd];
+      g.src_pitch[1] = vb.strides[rd];
+      g.dst_off = d0 + r * ds[rd];
+      g.dst_pitch = ds[rd];
+      g.run[0] = (int32_t)len[0];
+      g.run[1] = (int32_t)len[1];
+      g.src[0] = (int32_t)(t.src_base + ra.src);
+      g.src[1] = (int32_t)(t.src_base + rb.src);
+      g.group = roles[a].direct;
+      g.esize = t.esize;
+      p.gitems.push_back(g);
+    }
+    int d = rd - 1;
+    for (; d >= 0; --d) {
+      if (++idx[d] < ext[d]) break;
+      idx[d] = 0;
+    }
+    if (d < 0) break;
+  }
+}
+
 // Steps 4 and 5: the device group table (the given replica sets plus the send-buffer group) and
 // the work items of the three passes, each region as its role says. `dev_groups` are replica
 // sets of destination pointer indices within a tensor's run; a role's group indexes them.
@@ -570,6 +691,8 @@ int emit_tables(reshard_plan *plan, const std::vector<Role> &roles, const std::v
   int64_t item_bytes = kMaxItemBytes;
   while (item_bytes > kMinItemBytes && plan_bytes / item_bytes < kItemsPerPlan) item_bytes /= 2;
   std::map<SlabSpec, int32_t> slab_ids;
+  const std::vector<int64_t> partner = gather_pairs(*plan, roles, dev_groups);
+  plan->gitems.clear();
   for (size_t i = 0; i < plan->regions.size(); ++i) {
     const Region &r = plan->regions[i];
     const Role &role = roles[i];
@@ -606,8 +729,14 @@ int emit_tables(reshard_plan *plan, const std::vector<Role> &roles, const std::v
     if (role.direct >= 0) {
       int64_t dof;
       const int64_t *ds = dst_side(role.direct, dof);
+      const size_t n0 = plan->items[kDirect].size();
       emit_region(nd, ext, so, sv.strides, from_src, dof, ds, role.direct, t.esize, item_bytes, plan->items[kDirect],
                   plan->titems[kDirect], slab_ids, plan->slabs);
+      // a paired region's rows are written by gather items; its plain items stay in the table
+      // (flagged) for the passes that walk plain items only
+      if (partner[i] != -1)
+        for (size_t k = n0; k < plan->items[kDirect].size(); ++k) plan->items[kDirect][k].pad[0] = kGathered;
+      if (partner[i] >= 0) emit_gather(*plan, i, (size_t)partner[i], roles, dev_groups, item_bytes);
     }
     if (role.send_off >= 0) {
       const int64_t mo = role.send_off / t.esize;
@@ -671,13 +800,15 @@ int emit_tables(reshard_plan *plan, const std::vector<Role> &roles, const std::v
   st.n_tensors = (int64_t)plan->tensors.size();
   st.regions = (int64_t)plan->regions.size();
   st.items = (int64_t)(plan->items[kDirect].size() + plan->titems[kDirect].size());
+  st.gather_items = (int64_t)plan->gitems.size();
   st.dst_groups = (int64_t)plan->groups.size();
   st.gather_bcast_bytes = 2 * global_bytes;
   st.global_bytes = global_bytes;
   st.rank = plan->rank;
   st.world = plan->world;
   if ((int64_t)(plan->items[kDirect].size() + plan->items[kPack].size() + plan->items[kUnpack].size() +
-                plan->titems[kDirect].size() + plan->titems[kPack].size() + plan->titems[kUnpack].size()) > INT32_MAX ||
+                plan->titems[kDirect].size() + plan->titems[kPack].size() + plan->titems[kUnpack].size() +
+                plan->gitems.size()) > INT32_MAX ||
       (int64_t)plan->mem_ptr.size() > INT32_MAX || (int64_t)plan->slabs.size() > INT32_MAX ||
       pointer_table_size(plan) > INT32_MAX) {
     return fail(RESHARD_ERR_UNSUPPORTED, "plan too large (more than 2^31 items, members or pointers)");
@@ -1078,6 +1209,7 @@ extern "C" int reshard_plan_stats(const reshard_plan_t *plan, reshard_stats_t *o
   out->last_general_items = plan->last_general;
   out->last_rows_kernel = plan->last_rows_kernel;
   out->last_staged_items = plan->last_staged;
+  out->last_gather_items = plan->last_gather;
   return RESHARD_OK;
 }
 
@@ -1114,12 +1246,23 @@ extern "C" int reshard_plan_items(const reshard_plan_t *plan, int set, int64_t c
                                   int32_t *group_start, int32_t *member_ptr, int64_t *member_off,
                                   int64_t *n_groups_out, int64_t *n_members_out) {
   if (!plan) return fail(RESHARD_ERR_INVALID_ARG, "plan is NULL");
-  if (set < 0 || set >= 2 * kNumSets) return fail(RESHARD_ERR_INVALID_ARG, "set must be in 0..5");
+  if (set < 0 || set > 2 * kNumSets) return fail(RESHARD_ERR_INVALID_ARG, "set must be in 0..6");
   static_assert(sizeof(Item) == sizeof(TItem), "both item kinds are 64 bytes");
-  const size_t count = set < kNumSets ? plan->items[set].size() : plan->titems[set - kNumSets].size();
-  const void *data = set < kNumSets ? (const void *)plan->items[set].data() : (const void *)plan->titems[set - kNumSets].data();
+  size_t count, size = sizeof(Item);
+  const void *data;
+  if (set < kNumSets) {
+    count = plan->items[set].size();
+    data = plan->items[set].data();
+  } else if (set < 2 * kNumSets) {
+    count = plan->titems[set - kNumSets].size();
+    data = plan->titems[set - kNumSets].data();
+  } else {
+    count = plan->gitems.size();
+    data = plan->gitems.data();
+    size = sizeof(GItem);
+  }
   if (n_out) *n_out = (int64_t)count;
-  if (items && cap > 0) std::memcpy(items, data, (size_t)std::min<int64_t>(cap, (int64_t)count) * sizeof(Item));
+  if (items && cap > 0) std::memcpy(items, data, (size_t)std::min<int64_t>(cap, (int64_t)count) * size);
   if (n_groups_out) *n_groups_out = (int64_t)plan->grp_start.size() - 1;
   if (n_members_out) *n_members_out = (int64_t)plan->mem_ptr.size();
   if (group_start) std::memcpy(group_start, plan->grp_start.data(), plan->grp_start.size() * sizeof(int32_t));

@@ -80,6 +80,33 @@ struct alignas(16) TItem {
 };
 static_assert(sizeof(TItem) == 64, "transposing item is one 64-byte descriptor");
 
+// Pair direct regions into gather items (0 turns it off: every region is walked as plain items).
+#ifndef RESHARD_GATHER
+#define RESHARD_GATHER 1
+#endif
+
+// Gather item of the direct pass: `rows` destination rows each made of two pieces that sit side
+// by side along the destination's contiguous dim, piece 0's `run[0]` elements then piece 1's
+// `run[1]`. Row i of piece p is read at src_off[p] + i * src_pitch[p] of pointer src[p]; row i of
+// destination replica m starts at member_offset[m] + dst_off + i * dst_pitch of that member's
+// pointer. It replaces the two plain items flagged kGathered (the allocation-free entry point and
+// the alignment classes still use the plain items).
+struct alignas(16) GItem {
+  int64_t src_off[2];
+  int64_t src_pitch[2];
+  int64_t dst_off;
+  int64_t dst_pitch;
+  int32_t run[2];
+  int32_t src[2];
+  int32_t rows;
+  int32_t group;
+  int32_t esize;
+  int32_t pad;
+};
+static_assert(sizeof(GItem) == 80, "gather item is one 80-byte descriptor");
+// Item.pad[0] flag: the item's rows are written by a gather item instead
+constexpr int32_t kGathered = 1;
+
 // A 2-D source slab read by TMA: element (y, x) at base_off + y * pitch + x (elements) of
 // pointer `ptr`, extents x < cols, y < rows.
 struct SlabSpec {
@@ -165,6 +192,7 @@ struct reshard_plan {
   int64_t n_src_ptrs = 0, n_dst_ptrs = 0;
   std::vector<reshard::Item> items[reshard::kNumSets];
   std::vector<reshard::TItem> titems[reshard::kNumSets];  // transposing items of each pass
+  std::vector<reshard::GItem> gitems;                      // gather items of the direct pass
   std::vector<reshard::SlabSpec> slabs;                    // TMA source slabs (all passes)
   // group table (device layout): members of group g are [grp_start[g], grp_start[g + 1])
   std::vector<int32_t> grp_start;
@@ -188,6 +216,7 @@ struct reshard_plan {
   int device = -1;
   void *d_items[reshard::kNumSets] = {nullptr, nullptr, nullptr};
   void *d_titems[reshard::kNumSets] = {nullptr, nullptr, nullptr};
+  void *d_gitems = nullptr;
   void *d_maps = nullptr;      // one 128-byte CUtensorMap per slab (64-byte aligned)
   int32_t *d_map_ok = nullptr; // 1 where the slab's map could be encoded
   int32_t *d_status = nullptr; // device-side status word (bit 0: a TMA wait timed out)
@@ -197,6 +226,7 @@ struct reshard_plan {
   std::vector<int32_t> cls_idx[reshard::kNumSets];
   int32_t n_aligned[reshard::kNumSets] = {0, 0, 0};
   int32_t n_staged[reshard::kNumSets] = {0, 0, 0};  // next in cls_idx: the bulk-staged items
+  int32_t n_general[reshard::kNumSets] = {0, 0, 0}; // last in cls_idx: the rest (gathered items are left out)
   int32_t *d_cls_idx[reshard::kNumSets] = {nullptr, nullptr, nullptr};
   uint64_t cls_version[reshard::kNumSets] = {0, 0, 0};
   uint64_t ptr_version = 0;  // bumped whenever the pointer table changes
@@ -205,6 +235,7 @@ struct reshard_plan {
   int64_t last_general = 0;  // ... and the general walker
   int64_t last_rows_kernel = 0;  // 1 when those ran in the many-rows build of the general walker
   int64_t last_staged = 0;       // copy items of the last pass run by the bulk-staged kernel
+  int64_t last_gather = 0;       // gather items of the last direct pass
   bool gen_rows[reshard::kNumSets] = {false, false, false};  // general items mostly short rows
   int32_t *d_grp_start = nullptr;
   int32_t *d_mem_ptr = nullptr;

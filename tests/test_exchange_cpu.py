@@ -154,7 +154,7 @@ def _rank_main(rank, world, port, combos, out):
             dst = np.full(lay.dst_slab.numel(), CANARY, np.uint8)
             table = table_for(wl, lay, st["message_bytes"], st["recv_bytes"])
             arrays = {"src": src, "dst": dst, "send": send, "recv": recv}
-            run_items(rp, 0, table, arrays)          # local copies
+            run_items(rp, 0, table, arrays, gather=True)   # local copies, gather items included
             run_items(rp, 1, table, arrays)          # outgoing messages
             exchange.run_transfers(rp, torch.from_numpy(send), torch.from_numpy(recv))
             run_items(rp, 2, table, arrays)          # received messages
@@ -333,7 +333,7 @@ def test_brute_force_partitions_through_the_loopback_transport():
             recv = np.zeros(max(16, st["recv_bytes"]), np.uint8)
             a = {"src": src, "dst": dst, "send": send, "recv": recv}
             table = table_for(wl, lay, st["message_bytes"], st["recv_bytes"])
-            run_items(rp, 0, table, a)
+            run_items(rp, 0, table, a, gather=True)
             run_items(rp, 1, table, a)
             parts.append((rp, table))
             sends.append(torch.from_numpy(send))

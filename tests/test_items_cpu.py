@@ -109,15 +109,50 @@ def check_transpose_bounds(wl, lay, plan, which, ws=None):
     assert (end <= hi[sl[:, 0]]).all(), "a TMA slab reaches past its buffer"
 
 
-def emulate(wl, lay, plan, mode):
-    """Apply the item tables to host copies of the slabs (plain copies only)."""
+def check_gather_bounds(wl, lay, plan, ws=None):
+    """Gather items: both pieces' reads and every row's writes stay in their buffers, and the
+    gather items carry exactly the bytes of the direct copy items flagged as theirs."""
+    items, gs, mp, mo = R.reshard_plan_items(plan, 6)
+    plain = R.reshard_plan_items(plan, DIRECT)[0]
+    flagged = plain[plain["pad"][:, 0] == 1]
+    assert set(np.unique(plain["pad"][:, 0])) <= {0, 1}
+    if len(items) == 0:
+        assert len(flagged) == 0
+        return
+    es = items["esize"].astype(np.int64)
+    rows = items["rows"].astype(np.int64)
+    assert (rows > 0).all() and (items["run"] >= 2).all()
+    assert int((rows * (items["run"][:, 0] + items["run"][:, 1]) * es).sum()) == \
+        int((flagged["rows"].astype(np.int64) * flagged["run"] * flagged["esize"]).sum())
+    table = _ranges(wl, lay, plan, ws)
+    lo = np.array([r[1] for r in table], np.int64)
+    hi = np.array([r[2] for r in table], np.int64)
+    for p in (0, 1):
+        sp = items["src"][:, p]
+        s0 = lo[sp] + items["src_off"][:, p] * es
+        s1 = lo[sp] + (items["src_off"][:, p] + (rows - 1) * items["src_pitch"][:, p] + items["run"][:, p]) * es
+        assert (s0 >= lo[sp]).all() and (s1 <= hi[sp]).all(), "gather read out of bounds"
+    counts = gs[items["group"] + 1] - gs[items["group"]]
+    for k in range(int(counts.max())):
+        sel = counts > k
+        m = gs[items["group"][sel]] + k
+        ptr, off, it = mp[m], mo[m], items[sel]
+        run = it["run"][:, 0].astype(np.int64) + it["run"][:, 1]
+        d0 = lo[ptr] + (off + it["dst_off"]) * es[sel]
+        d1 = lo[ptr] + (off + it["dst_off"] + (rows[sel] - 1) * it["dst_pitch"] + run) * es[sel]
+        assert (d0 >= lo[ptr]).all() and (d1 <= hi[ptr]).all(), "gather write out of bounds"
+
+
+def emulate(wl, lay, plan, mode, gather=False):
+    """Apply the item tables to host copies of the slabs (plain copies only); with `gather`, the
+    direct pass as the executor runs it when the plan has gather items."""
     src = lay.src_slab.numpy()
     dst = np.full(lay.dst_slab.numel(), 0xA5, np.uint8)
     ws = np.zeros(max(1, R.reshard_plan_stats(plan)["message_bytes"]), np.uint8)
     table = _ranges(wl, lay, plan)
     arrays = {"src": src, "dst": dst, "ws": ws}
     for which in ((DIRECT,) if mode == "direct" else (PACK, UNPACK)):
-        run_items(plan, which, table, arrays)
+        run_items(plan, which, table, arrays, gather=gather)
     return dst
 
 
@@ -137,7 +172,11 @@ def test_item_tables_reproduce_oracle(name, mode):
     for which in (DIRECT, PACK, UNPACK):
         check_bounds(wl, lay, plan, which)
         check_transpose_bounds(wl, lay, plan, which)
-    assert np.array_equal(emulate(wl, lay, plan, mode), _oracle(wl, lay))
+    check_gather_bounds(wl, lay, plan)
+    want = _oracle(wl, lay)
+    assert np.array_equal(emulate(wl, lay, plan, mode), want)
+    if mode == "direct":
+        assert np.array_equal(emulate(wl, lay, plan, mode, gather=True), want)
 
 
 def test_item_tables_brute_force():
@@ -147,8 +186,11 @@ def test_item_tables_brute_force():
         plan = R.plan_workload(wl)
         for which in (DIRECT, PACK, UNPACK):
             check_bounds(wl, lay, plan, which)
+        check_gather_bounds(wl, lay, plan)
+        want = _oracle(wl, lay)
         for mode in ("direct", "packed"):
-            assert np.array_equal(emulate(wl, lay, plan, mode), _oracle(wl, lay))
+            assert np.array_equal(emulate(wl, lay, plan, mode), want)
+        assert np.array_equal(emulate(wl, lay, plan, "direct", gather=True), want)
 
 
 @pytest.mark.parametrize("case", ["moe_tp4", "six_replicas"])
@@ -177,6 +219,55 @@ def test_full_size_item_bounds(name):
     for which in (DIRECT, PACK, UNPACK):
         check_bounds(wl, lay, plan, which, quant=wl.quant == "mxfp8")
         check_transpose_bounds(wl, lay, plan, which)
+    check_gather_bounds(wl, lay, plan)
+
+
+# rows of a misaligned column split assembled from two source pieces, as (piece 0, piece 1)
+# bytes: 1024-column source shards of a 2 x 4 mesh into destinations of 1366, 1366 and 1364
+# columns (torch.chunk of 4096 by 3)
+MESH_PIECES = {(2048, 684), (1364, 1368), (680, 2048)}
+GATHER_EXPECT = {name: MESH_PIECES for name in ("mesh2x4_to_3_14336x4096", "mesh2x4_to_3x2_14336x4096",
+                                                "mesh2x4_to_3_57344x4096", "mesh2x4_to_3x2_57344x4096")}
+
+
+@pytest.mark.parametrize("name", sorted(S.WORKLOAD_NAMES))
+def test_gather_items_where_rows_are_split_and_misaligned(name):
+    """Gather items appear exactly where a destination row is two source pieces and the rows are
+    misaligned by construction; their pieces are the expected column splits, every row of every
+    paired region is covered, and a region is paired at most once."""
+    wl = S.workload_by_name(name)
+    plan = R.plan_workload(wl)
+    items = R.reshard_plan_items(plan, 6)[0]
+    assert R.reshard_plan_stats(plan)["gather_items"] == len(items)
+    if name not in GATHER_EXPECT:
+        assert len(items) == 0, name
+        return
+    es = items["esize"].astype(np.int64)
+    got = {(int(a), int(b)) for a, b in zip(items["run"][:, 0] * es, items["run"][:, 1] * es)}
+    assert got == GATHER_EXPECT[name]
+    assert (items["dst_pitch"] * es == (items["run"][:, 0] + items["run"][:, 1]) * es).all()
+    t = wl.tensors[0]
+    n_rep = int(np.prod(t.dst_mesh)) // 3
+    gs = R.reshard_plan_items(plan, 6)[1]
+    assert all(gs[g + 1] - gs[g] == n_rep for g in items["group"])
+    # every destination row of the tensor is written by exactly one gather item
+    assert int(items["rows"].sum()) == t.global_shape[0] * 3
+
+
+def test_gather_pairs_follow_the_alignment_rule():
+    """A column split whose pieces and destination pitch are 16-byte multiples pairs nothing;
+    one whose destination pitch is not pairs every row; a replicated source counts once."""
+    from test_parity_gpu import _one
+    aligned = _one((64, 1024), (2,), ("S1",), (4,), ("S1",))           # 512-col pieces, 256-col rows
+    assert R.reshard_plan_stats(R.plan_workload(aligned))["gather_items"] == 0
+    split = _one((64, 1000), (4,), ("S1",), (3,), ("S1",))             # 250-col sources, 334-col rows
+    st = R.reshard_plan_stats(R.plan_workload(split))
+    assert st["gather_items"] > 0
+    items = R.reshard_plan_items(R.plan_workload(split), 6)[0]
+    assert int(items["rows"].sum()) == 64 * 3
+    rep = _one((64, 1000), (2, 4), ("R", "S1"), (3,), ("S1",))         # the same with two replicas
+    items2 = R.reshard_plan_items(R.plan_workload(rep), 6)[0]
+    assert int(items2["rows"].sum()) == 64 * 3
 
 
 def test_item_tables_fuzzed_layouts():
@@ -188,5 +279,8 @@ def test_item_tables_fuzzed_layouts():
         for which in (DIRECT, PACK, UNPACK):
             check_bounds(wl, lay, plan, which)
             check_transpose_bounds(wl, lay, plan, which)
+        check_gather_bounds(wl, lay, plan)
+        want = _oracle(wl, lay)
         for mode in ("direct", "packed"):
-            assert np.array_equal(emulate(wl, lay, plan, mode), _oracle(wl, lay)), (wl.tensors[0], mode)
+            assert np.array_equal(emulate(wl, lay, plan, mode), want), (wl.tensors[0], mode)
+        assert np.array_equal(emulate(wl, lay, plan, "direct", gather=True), want), wl.tensors[0]

@@ -338,6 +338,7 @@ HOST_CASES = {
     "transposed": lambda: S.transposed(shape=(300, 256), src_mesh=(4,), src_pl=("S0",)),
     "moe_tp4_mxfp8": lambda: S.moe_experts(layers=1, experts=16, hidden=256, ffn=128, dst="tp4"),
     "many_small": lambda: S.many_small(n=20),
+    "mesh2x4_to_3x2_gather": lambda: S.mesh2d_to_1d(rows=143, cols=409, variant="2d"),
 }
 
 
@@ -389,7 +390,8 @@ def test_misaligned_items_take_the_staged_kernel_or_the_general_walker():
     reshard_copy_rows_kernel; misaligned single long rows in reshard_copy_kernel; more replicas
     than a staged descriptor holds in the general walker too. All bit-exact."""
     import dataclasses
-    wl = S.mesh2d_to_1d(rows=512, cols=4096, variant="2d")      # destination pitch 2732 bytes, 2 replicas
+    # whole source rows (a (2, 1) mesh) into a 3-way column split: destination pitch 2732 bytes
+    wl = S.mesh2d_to_1d(rows=512, cols=4096, variant="2d", src_cols=1)      # 2 replicas
     lay, plan = run_gpu(wl)
     st = R.reshard_plan_stats(plan)
     assert st["last_staged_items"] > 0 and st["last_general_items"] == 0
@@ -402,7 +404,7 @@ def test_misaligned_items_take_the_staged_kernel_or_the_general_walker():
     st = R.reshard_plan_stats(plan)
     assert st["last_staged_items"] == 0 and st["last_general_items"] > 0 and st["last_rows_kernel"] == 1
     assert_matches_oracle(wl, hl)
-    wl = S.mesh2d_to_1d(rows=512, cols=4096, variant="1d")      # one replica, 8 MB: the many-rows walker
+    wl = S.mesh2d_to_1d(rows=512, cols=4096, variant="1d", src_cols=1)      # one replica, 8 MB: many-rows walker
     lay, plan = run_gpu(wl)
     st = R.reshard_plan_stats(plan)
     assert st["last_staged_items"] == 0 and st["last_general_items"] > 0 and st["last_rows_kernel"] == 1
@@ -412,7 +414,7 @@ def test_misaligned_items_take_the_staged_kernel_or_the_general_walker():
     st = R.reshard_plan_stats(plan)
     assert st["last_general_items"] > 0 and st["last_rows_kernel"] == 0
     assert_matches_oracle(wl, lay)
-    wl = _one((96, 333), (2,), ("S1",), (12,), ("R",))            # 12 replicas of odd-width rows
+    wl = _one((96, 333), (2,), ("S0",), (2, 12), ("S1", "R"))     # 12 replicas of 167/166-column rows
     lay, plan = run_gpu(wl)
     st = R.reshard_plan_stats(plan)
     assert st["last_staged_items"] == 0 and st["last_general_items"] > 0
@@ -425,7 +427,7 @@ def test_staged_kernel_row_shapes():
     counts drain a pair of equal-phase replicas together and the last one alone), many rows per
     stage and one row per stage."""
     cases = [
-        _one((300, 2048), (2,), ("S1",), (3, 3), ("S1", "R")),        # 683/682-column rows, 3 replicas
+        _one((300, 2048), (1,), ("R",), (3, 3), ("S1", "R")),         # 683/682-column rows, 3 replicas
         _one((64, 4096), (1,), ("R",), (3, 2), ("S1", "R")),          # rows close to the 4 KiB limit
         _one((500, 9), (1,), ("R",), (2, 2), ("S1", "R")),            # 4-5 element rows, 2 replicas
         _one((200, 1000), (3,), ("S0",), (2, 3), ("R", "S1"), dtype="u8"),
@@ -443,11 +445,67 @@ def test_staged_kernel_row_shapes():
 
 def test_staged_kernel_single_replica_at_size():
     """One replica: the staged kernel takes the rows once they move 512 MB or more (here the
-    (2,4) -> (3,) mesh reshard at 4x the rows, 940 MB read + written); compared whole."""
-    wl = S.mesh2d_to_1d(rows=57344, variant="1d")
+    (2,1) -> (3,) mesh reshard at 4x the rows, 940 MB read + written); compared whole."""
+    wl = S.mesh2d_to_1d(rows=57344, variant="1d", src_cols=1)
     lay, plan = run_gpu(wl)
     assert R.reshard_plan_stats(plan)["last_staged_items"] > 0
     assert_matches_oracle(wl, lay)
+
+
+def _split(shape, ns, nd, reps=1, dtype="bf16", shift=0, dim=-1):
+    """`ns` source shards along `dim` into `nd` destination shards along it, each destination
+    replicated `reps` times; replica j of a destination starts `shift * j` elements into its
+    buffer (replicas whose rows differ in phase mod 16 bytes)."""
+    d = len(shape) + dim if dim < 0 else dim
+    dm, dp = ((nd, reps), (f"S{d}", "R")) if reps > 1 else ((nd,), (f"S{d}",))
+    t = S.TensorDesc("w", shape, dtype, (ns,), (f"S{d}",), dm, dp, [S.View(i) for i in range(ns)],
+                     [S.View(i, shift * (i % reps)) for i in range(nd * reps)], seed=43)
+    return S.workloads._size_buffers(S.Workload("split", [t]), ns, nd * reps)
+
+
+GATHER_CASES = {
+    "mesh_pieces_2048_684": lambda: _split((300, 4096), 4, 3),
+    "two_replicas": lambda: _split((257, 1000), 4, 3, reps=2),
+    "replicas_out_of_phase": lambda: _split((129, 1000), 4, 3, reps=2, shift=3),
+    "three_replicas_out_of_phase": lambda: _split((65, 1000), 4, 3, reps=3, shift=5),
+    "pieces_of_two_elements": lambda: _split((64, 18), 9, 2),             # 4-byte pieces, 18-byte rows
+    "u8_odd": lambda: _split((77, 333), 4, 3, reps=2, dtype="u8"),
+    "f32": lambda: _split((90, 702), 2, 5, dtype="f32"),                # pairs only across the middle
+    "i64_rows": lambda: _split((40, 301), 4, 3, dtype="i64"),
+    "three_dims": lambda: _split((3, 50, 1000), 4, 3),
+    "long_rows": lambda: _split((16, 40000), 4, 3, reps=2),              # 26.7 KB rows
+}
+
+
+@pytest.mark.parametrize("misalign", [0, 2, 6])
+@pytest.mark.parametrize("name", sorted(GATHER_CASES))
+def test_gather_rows_bit_exact(name, misalign):
+    """Destination rows assembled from two source pieces run in reshard_copy_gather_kernel: every
+    piece length (4 bytes up), element sizes 1 to 8, replicas in and out of phase, outer dims,
+    rows longer than a warp's pass; buffers shifted by 0, 2 or 6 bytes. Bit-exact, canary intact."""
+    wl = GATHER_CASES[name]()
+    if misalign % S.DTYPES[wl.tensors[0].dtype][1]:
+        pytest.skip("shift not a multiple of the element size")
+    lay, plan = run_gpu(wl, misalign=misalign)
+    st = R.reshard_plan_stats(plan)
+    assert st["gather_items"] > 0 and st["last_gather_items"] == st["gather_items"]
+    assert_matches_oracle(wl, lay)
+    lay, plan = run_gpu(wl, mode="packed", misalign=misalign, plan=plan)   # plain items, unflagged
+    assert R.reshard_plan_stats(plan)["last_gather_items"] == 0
+    assert_matches_oracle(wl, lay)
+
+
+def test_gather_items_carry_the_whole_mesh_reshard():
+    """The (2,4) -> (3,) and (3,2) mesh reshards: every destination row is two source pieces, so
+    the gather kernel is the pass's only launch; the allocation-free entry point walks the same
+    plan's plain items and gives the same bytes."""
+    for variant in ("1d", "2d"):
+        wl = S.mesh2d_to_1d(rows=1434, cols=4096, variant=variant)
+        lay, plan = run_gpu(wl)
+        st = R.reshard_plan_stats(plan)
+        assert st["last_launches"] == 1 and st["last_gather_items"] == st["gather_items"] > 0
+        assert st["last_aligned_items"] + st["last_staged_items"] + st["last_general_items"] == 0
+        assert_matches_oracle(wl, lay)
 
 
 def test_readme_example():
