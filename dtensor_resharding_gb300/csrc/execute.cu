@@ -473,20 +473,19 @@ __global__ void __launch_bounds__(kBlock, RESHARD_ROWS_MIN_BLOCKS) reshard_copy_
 // piece and a funnel shift by that piece's phase, as in copy_shifted_rows; the lanes of one row
 // walk its words together. dst[f] are the row's starts in NF replicas with equal phase mod 16.
 template <int NF, int RU>
-__device__ __forceinline__ void gather_row(const uint8_t *s0, const uint8_t *s1, int64_t B, int64_t rb,
-                                           uint8_t *const *dst, int nf, int lane) {
+__device__ __forceinline__ void gather_row(const uint8_t *s0, const uint8_t *s1, int B, int rb, uint8_t *const *dst,
+                                           int nf, int lane) {
   const int a = (int)(reinterpret_cast<uintptr_t>(dst[0]) & 15);
-  const int nw = (int)((a + rb + 15) >> 4);   // destination words the row touches
-  const int wb0 = (int)((a + B - 1) >> 4);     // the last word with piece-0 bytes
-  const int wb1 = (int)((a + B) >> 4);         // the first word with piece-1 bytes
-  const int nv = wb0 + 1 + nw - wb1;           // words of both pieces, the shared one twice
+  const int nw = (a + rb + 15) >> 4;   // destination words the row touches
+  const int wb0 = (a + B - 1) >> 4;    // the last word with piece-0 bytes
+  const int wb1 = (a + B) >> 4;        // the first word with piece-1 bytes
+  const int nv = wb0 + 1 + nw - wb1;   // words of both pieces, the shared one twice
   const uintptr_t p0 = reinterpret_cast<uintptr_t>(s0) - a;      // source of word 0's byte 0, piece 0
   const uintptr_t p1 = reinterpret_cast<uintptr_t>(s1) - B - a;  // ... piece 1 (never read there)
   const int sh0 = (int)(p0 & 15), sh1 = (int)(p1 & 15);
   for (int v0 = lane; v0 < nv; v0 += 32 * RU) {
     uint4 lo[RU], hi[RU];
-    int kmin[RU], kmax[RU], sh[RU];
-    int64_t start[RU];
+    int kmin[RU], kmax[RU], sh[RU], start[RU];
 #pragma unroll
     for (int u = 0; u < RU; ++u) {
       const int v = v0 + 32 * u;
@@ -499,13 +498,13 @@ __device__ __forceinline__ void gather_row(const uint8_t *s0, const uint8_t *s1,
       if (v < nv) {
         const bool second = v > wb0;
         const int w = second ? wb1 + (v - wb0 - 1) : v;
-        const int64_t st = 16 * (int64_t)w - a;  // row byte of the word's byte 0
-        const int64_t lo_b = second ? B : 0, hi_b = second ? rb : B;
-        kmin[u] = (int)(lo_b - st > 0 ? lo_b - st : 0);
-        kmax[u] = (int)(hi_b - st < 16 ? hi_b - st : 16);
+        const int st = 16 * w - a;  // row byte of the word's byte 0
+        const int lo_b = second ? B : 0, hi_b = second ? rb : B;
+        kmin[u] = max(lo_b - st, 0);
+        kmax[u] = min(hi_b - st, 16);
         sh[u] = second ? sh1 : sh0;
         start[u] = st;
-        const uint8_t *blk = reinterpret_cast<const uint8_t *>((second ? p1 : p0) - sh[u]) + 16 * (int64_t)w;
+        const uint8_t *blk = reinterpret_cast<const uint8_t *>((second ? p1 : p0) - sh[u]) + 16 * w;
         if (kmin[u] < 16 - sh[u]) lo[u] = __ldg(reinterpret_cast<const uint4 *>(blk));
         if (sh[u] && kmax[u] > 16 - sh[u]) hi[u] = __ldg(reinterpret_cast<const uint4 *>(blk + 16));
       }
@@ -527,42 +526,64 @@ __device__ __forceinline__ void gather_row(const uint8_t *s0, const uint8_t *s1,
   }
 }
 
-// Gather items: a persistent grid deals items round-robin, and each CTA's warps take the item's
-// rows in turn. Replicas go two per pass when their phases agree mod 16, else one per pass.
-// `wait_last` as in reshard_copy_kernel.
-__global__ void __launch_bounds__(kBlock, RESHARD_ROWS_MIN_BLOCKS) reshard_copy_gather_kernel(
-    const GItem *__restrict__ items, int n_items, const uint64_t *__restrict__ ptrs,
+#ifndef RESHARD_GATHER_UNROLL
+#define RESHARD_GATHER_UNROLL RESHARD_ROW_UNROLL
+#endif
+#ifndef RESHARD_GATHER_MIN_BLOCKS
+#define RESHARD_GATHER_MIN_BLOCKS RESHARD_ROWS_MIN_BLOCKS
+#endif
+
+// Gather items, resolved by the host for the current pointers: a persistent grid deals them
+// round-robin (adjacent CTAs take adjacent items, so the grid streams through neighbouring rows)
+// and each CTA's warps take an item's rows in turn. Descriptors are double-buffered in shared
+// memory: 24 threads fetch the next one while the current one is copied. Replicas go two per
+// pass when their phases agree mod 16, else one per pass. `wait_last` as in reshard_copy_kernel.
+__global__ void __launch_bounds__(kBlock, RESHARD_GATHER_MIN_BLOCKS) reshard_copy_gather_kernel(
+    const GBound *__restrict__ items, int n_items, const uint64_t *__restrict__ ptrs,
     const int32_t *__restrict__ gstart, const int32_t *__restrict__ mptr, const int64_t *__restrict__ moff,
     int wait_last) {
   if (!wait_last) pdl_enter();
+  __shared__ GBound s_item[2];
+  constexpr int kWords = (int)(sizeof(GBound) / sizeof(uint32_t));
+  if (threadIdx.x < kWords && blockIdx.x < n_items)
+    reinterpret_cast<uint32_t *>(&s_item[0])[threadIdx.x] =
+        __ldg(reinterpret_cast<const uint32_t *>(items + blockIdx.x) + threadIdx.x);
+  __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int k = blockIdx.x; k < n_items; k += gridDim.x) {
+  int buf = 0;
+  for (int k = blockIdx.x; k < n_items; k += gridDim.x, buf ^= 1) {
     pdl_last_item(k, n_items);
-    const GItem &it = items[k];
-    const int64_t es = it.esize;
-    const uint8_t *s0 = reinterpret_cast<const uint8_t *>(ptrs[it.src[0]]) + it.src_off[0] * es;
-    const uint8_t *s1 = reinterpret_cast<const uint8_t *>(ptrs[it.src[1]]) + it.src_off[1] * es;
-    const int64_t B = (int64_t)it.run[0] * es, rb = B + (int64_t)it.run[1] * es;
-    const int64_t sp0 = it.src_pitch[0] * es, sp1 = it.src_pitch[1] * es, dp = it.dst_pitch * es;
-    const int rows = it.rows;
-    const int g0 = gstart[it.group], nrep = gstart[it.group + 1] - g0;
+    if (threadIdx.x < kWords && k + (int)gridDim.x < n_items)
+      reinterpret_cast<uint32_t *>(&s_item[buf ^ 1])[threadIdx.x] =
+          __ldg(reinterpret_cast<const uint32_t *>(items + k + gridDim.x) + threadIdx.x);
+    const GBound &it = s_item[buf];
+    const uint8_t *s0 = reinterpret_cast<const uint8_t *>(it.src[0]);
+    const uint8_t *s1 = reinterpret_cast<const uint8_t *>(it.src[1]);
+    const int B = it.B, rb = it.rb, rows = it.rows, nrep = it.nrep;
+    const int64_t sp0 = it.sp[0], sp1 = it.sp[1], dp = it.dp;
     for (int f0 = 0; f0 < nrep; f0 += 2) {
       const int nf = min(2, nrep - f0);
       uint8_t *dst[2];
-      dst[0] = reinterpret_cast<uint8_t *>(ptrs[mptr[g0 + f0]]) + (moff[g0 + f0] + it.dst_off) * es;
-      dst[1] = nf > 1 ? reinterpret_cast<uint8_t *>(ptrs[mptr[g0 + f0 + 1]]) + (moff[g0 + f0 + 1] + it.dst_off) * es
-                      : dst[0];
+      if (f0 == 0) {
+        dst[0] = reinterpret_cast<uint8_t *>(it.dst[0]);
+        dst[1] = reinterpret_cast<uint8_t *>(it.dst[1]);
+      } else {
+        const int m = gstart[it.group] + f0;
+        dst[0] = reinterpret_cast<uint8_t *>(ptrs[mptr[m]]) + moff[m] * it.esize + it.dst_off_b;
+        dst[1] = nf > 1 ? reinterpret_cast<uint8_t *>(ptrs[mptr[m + 1]]) + moff[m + 1] * it.esize + it.dst_off_b : dst[0];
+      }
       const bool same = ((reinterpret_cast<uintptr_t>(dst[0]) ^ reinterpret_cast<uintptr_t>(dst[1])) & 15) == 0;
       for (int r = warp; r < rows; r += kBlock / 32) {
         uint8_t *row[2] = {dst[0] + r * dp, dst[1] + r * dp};
         if (same) {
-          gather_row<2, RESHARD_ROW_UNROLL>(s0 + r * sp0, s1 + r * sp1, B, rb, row, nf, lane);
+          gather_row<2, RESHARD_GATHER_UNROLL>(s0 + r * sp0, s1 + r * sp1, B, rb, row, nf, lane);
         } else {
-          gather_row<1, RESHARD_ROW_UNROLL>(s0 + r * sp0, s1 + r * sp1, B, rb, row, 1, lane);
-          gather_row<1, RESHARD_ROW_UNROLL>(s0 + r * sp0, s1 + r * sp1, B, rb, row + 1, 1, lane);
+          gather_row<1, RESHARD_GATHER_UNROLL>(s0 + r * sp0, s1 + r * sp1, B, rb, row, 1, lane);
+          gather_row<1, RESHARD_GATHER_UNROLL>(s0 + r * sp0, s1 + r * sp1, B, rb, row + 1, 1, lane);
         }
       }
     }
+    __syncthreads();  // everyone is done with s_item[buf]; s_item[buf ^ 1] is complete
   }
   if (wait_last) pdl_enter();
 }
@@ -1726,7 +1747,7 @@ int launch_transpose(reshard_plan_t *p, int set, cudaStream_t stream, const Laun
 // Split the copy items of `set` into those 16-byte aligned everywhere for the current pointers
 // (source, every replica, run, pitches) and the rest; upload the order on `stream`.
 int classify(reshard_plan_t *p, int set, cudaStream_t stream) {
-  if (p->d_cls_idx[set] && p->cls_version[set] == p->ptr_version) return RESHARD_OK;
+  if (p->cls_version[set] == p->ptr_version && (p->d_cls_idx[set] || p->cls_idx[set].empty())) return RESHARD_OK;
   const std::vector<Item> &items = p->items[set];
   const std::vector<uint64_t> &tab = p->dev_ptrs;
   std::vector<int32_t> &idx = p->cls_idx[set];
@@ -1800,6 +1821,43 @@ int classify(reshard_plan_t *p, int set, cudaStream_t stream) {
   return RESHARD_OK;
 }
 
+// Resolve the gather items for the current pointer table (absolute addresses of both pieces and
+// of the first two replicas) and upload them on `stream`, when the table has changed.
+int bind_gather(reshard_plan_t *p, cudaStream_t stream) {
+  if (p->d_gbound && p->gbound_version == p->ptr_version) return RESHARD_OK;
+  const std::vector<uint64_t> &tab = p->dev_ptrs;
+  const size_t n = p->gitems.size();
+  p->gbound.resize(n);
+  for (size_t i = 0; i < n; ++i) {
+    const GItem &g = p->gitems[i];
+    GBound &b = p->gbound[i];
+    const uint64_t es = (uint64_t)g.esize;
+    const int32_t m0 = p->grp_start[(size_t)g.group];
+    const int32_t nrep = p->grp_start[(size_t)g.group + 1] - m0;
+    for (int k = 0; k < 2; ++k) {
+      b.src[k] = tab[(size_t)g.src[k]] + (uint64_t)g.src_off[k] * es;
+      b.sp[k] = g.src_pitch[k] * (int64_t)es;
+    }
+    for (int f = 0; f < 2; ++f) {
+      const int32_t m = m0 + (f < nrep ? f : 0);
+      b.dst[f] = tab[(size_t)p->mem_ptr[(size_t)m]] + (uint64_t)(p->mem_off[(size_t)m] + g.dst_off) * es;
+    }
+    b.dp = g.dst_pitch * (int64_t)es;
+    b.dst_off_b = g.dst_off * (int64_t)es;
+    b.B = g.run[0] * g.esize;
+    b.rb = b.B + g.run[1] * g.esize;
+    b.rows = g.rows;
+    b.group = g.group;
+    b.nrep = nrep;
+    b.esize = g.esize;
+    b.pad[0] = b.pad[1] = 0;
+  }
+  if (!p->d_gbound) RS_CUDA(cudaMalloc(&p->d_gbound, n * sizeof(GBound)));
+  RS_CUDA(cudaMemcpyAsync(p->d_gbound, p->gbound.data(), n * sizeof(GBound), cudaMemcpyHostToDevice, stream));
+  p->gbound_version = p->ptr_version;
+  return RESHARD_OK;
+}
+
 int launch(reshard_plan_t *p, int set, bool quant, cudaStream_t stream, const LaunchCaps &caps) {
   int rc = launch_transpose(p, set, stream, caps);  // counts its own launches
   if (rc) return rc;
@@ -1852,14 +1910,10 @@ int launch(reshard_plan_t *p, int set, bool quant, cudaStream_t stream, const La
       ++p->last_launches;
     }
     if (nx > 0) {
-      if (!p->d_gitems) {
-        GItem *d = nullptr;
-        if ((rc = upload(&d, p->gitems))) return rc;
-        p->d_gitems = d;
-      }
+      if ((rc = bind_gather(p, stream))) return rc;
       const int wait_gather = RESHARD_GEN_OVERLAP && na + ns + ng > 0 ? 1 : 0;
       RS_CUDA(launch_kernel(true, reshard_copy_gather_kernel, std::min(nx, caps.gather_grid), kBlock, 0, stream,
-                            static_cast<const GItem *>(p->d_gitems), nx, p->d_ptrs, p->d_grp_start, p->d_mem_ptr,
+                            static_cast<const GBound *>(p->d_gbound), nx, p->d_ptrs, p->d_grp_start, p->d_mem_ptr,
                             p->d_mem_off, wait_gather));
       ++p->last_launches;
     }
@@ -1881,8 +1935,8 @@ void free_device(reshard_plan_t *p) {
     if (d) cudaFree(d);
     d = nullptr;
   }
-  if (p->d_gitems) cudaFree(p->d_gitems);
-  p->d_gitems = nullptr;
+  if (p->d_gbound) cudaFree(p->d_gbound);
+  p->d_gbound = nullptr;
   if (p->d_maps) cudaFree(p->d_maps);
   if (p->d_map_ok) cudaFree(p->d_map_ok);
   if (p->d_status) cudaFree(p->d_status);

@@ -84,6 +84,12 @@ static_assert(sizeof(TItem) == 64, "transposing item is one 64-byte descriptor")
 #ifndef RESHARD_GATHER
 #define RESHARD_GATHER 1
 #endif
+// Bytes a gather item moves (read + written over all replicas), in rows of a multiple of 8.
+#ifndef RESHARD_GATHER_ITEM_KIB
+#define RESHARD_GATHER_ITEM_KIB 96
+#endif
+constexpr int64_t kGatherItemBytes = RESHARD_GATHER_ITEM_KIB * 1024;
+constexpr int64_t kGatherRowStep = 8;
 
 // Gather item of the direct pass: `rows` destination rows each made of two pieces that sit side
 // by side along the destination's contiguous dim, piece 0's `run[0]` elements then piece 1's
@@ -104,6 +110,26 @@ struct alignas(16) GItem {
   int32_t pad;
 };
 static_assert(sizeof(GItem) == 80, "gather item is one 80-byte descriptor");
+
+// A gather item with its addresses resolved for the current pointer table (built on the host
+// whenever the table changes, so the kernel follows no pointer table): row 0 of both pieces and
+// of the first two replicas, pitches and lengths in bytes. Replicas past the second are looked up
+// through the group table, at member_offset * esize + dst_off_b of each member's pointer.
+struct alignas(16) GBound {
+  uint64_t src[2];
+  uint64_t dst[2];      // dst[1] == dst[0] with one replica
+  int64_t sp[2];
+  int64_t dp;
+  int64_t dst_off_b;
+  int32_t B;            // piece 0's bytes per row
+  int32_t rb;           // bytes per row
+  int32_t rows;
+  int32_t group;
+  int32_t nrep;
+  int32_t esize;
+  int32_t pad[2];
+};
+static_assert(sizeof(GBound) == 96, "resolved gather item is one 96-byte descriptor");
 // Item.pad[0] flag: the item's rows are written by a gather item instead
 constexpr int32_t kGathered = 1;
 
@@ -193,6 +219,7 @@ struct reshard_plan {
   std::vector<reshard::Item> items[reshard::kNumSets];
   std::vector<reshard::TItem> titems[reshard::kNumSets];  // transposing items of each pass
   std::vector<reshard::GItem> gitems;                      // gather items of the direct pass
+  std::vector<reshard::GBound> gbound;                     // ... resolved for the current pointer table
   std::vector<reshard::SlabSpec> slabs;                    // TMA source slabs (all passes)
   // group table (device layout): members of group g are [grp_start[g], grp_start[g + 1])
   std::vector<int32_t> grp_start;
@@ -216,7 +243,8 @@ struct reshard_plan {
   int device = -1;
   void *d_items[reshard::kNumSets] = {nullptr, nullptr, nullptr};
   void *d_titems[reshard::kNumSets] = {nullptr, nullptr, nullptr};
-  void *d_gitems = nullptr;
+  void *d_gbound = nullptr;     // the resolved gather items (gbound)
+  uint64_t gbound_version = 0;  // the pointer-table version they were resolved for
   void *d_maps = nullptr;      // one 128-byte CUtensorMap per slab (64-byte aligned)
   int32_t *d_map_ok = nullptr; // 1 where the slab's map could be encoded
   int32_t *d_status = nullptr; // device-side status word (bit 0: a TMA wait timed out)
