@@ -231,8 +231,10 @@ int reshard_plan_blockwise_fp8(const reshard_tensor_spec_t *specs, int n_tensors
  * `stream`, the TMA tensor maps of transposing regions are re-encoded, and the copy items are
  * re-sorted on the host into those 16-byte aligned everywhere (run by the aligned walker),
  * misaligned items of rows shorter than 4 KiB in device memory (run by the bulk-staged kernel)
- * and the rest (run by the general walker): host work proportional to the plan's items, none
- * when the pointers repeat.
+ * and the rest (run by the general walker), and the gather items (destination rows of two
+ * source pieces, reshard_plan_items set 6; run by the gather kernel in the direct mode without
+ * quantization) are resolved to absolute addresses and re-uploaded on `stream`: host work
+ * proportional to the plan's items, none when the pointers repeat.
  * Buffers must stay valid until the stream reaches the end of the work. Executes of one plan
  * on different streams that overlap in time race on its tables and workspace.
  * Errors: INVALID_ARG (NULL pointer of a shard the plan reads or writes, a pointer the device
