@@ -495,6 +495,25 @@ def test_gather_rows_bit_exact(name, misalign):
     assert_matches_oracle(wl, lay)
 
 
+def test_gather_items_follow_pointer_changes():
+    """The resolved gather table is rebuilt whenever the pointers change: one plan executed on
+    three layouts (shifted by 0, 6 and 0 bytes, the last with new buffers), each checked whole,
+    and a repeat with unchanged pointers."""
+    wl = S.mesh2d_to_1d(rows=143, cols=409, variant="2d")
+    lay1, plan = run_gpu(wl)
+    assert_matches_oracle(wl, lay1)
+    lay2, _ = run_gpu(wl, plan=plan, misalign=6)
+    assert_matches_oracle(wl, lay2)
+    lay3, _ = run_gpu(wl, plan=plan)
+    assert_matches_oracle(wl, lay3)
+    S.fill_canary(lay3)
+    sp, dp = R.workload_pointers(wl, lay3)
+    R.reshard_execute(plan, sp, dp, stream=torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert R.reshard_plan_stats(plan)["last_gather_items"] > 0
+    assert_matches_oracle(wl, lay3)
+
+
 def test_gather_items_carry_the_whole_mesh_reshard():
     """The (2,4) -> (3,) and (3,2) mesh reshards: every destination row is two source pieces, so
     the gather kernel is the pass's only launch; the allocation-free entry point walks the same
