@@ -632,17 +632,26 @@ void emit_gather(reshard_plan &p, size_t a, size_t b, const std::vector<Role> &r
   const int64_t nrep = (int64_t)dev_groups[(size_t)roles[a].direct].members.size();
   int64_t per = kGatherItemBytes / (row_b * (1 + nrep)) / kGatherRowStep * kGatherRowStep;
   per = std::min(std::max(per, kGatherRowStep), std::max<int64_t>(1, item_bytes / row_b));
+  // outer dims merge into the rows dim while both sources and the destination step uniformly
+  // over them (as the plain items' rows do); the rest are walked explicitly
+  int64_t rows = ext[rd];
+  int k = rd - 1;
+  while (k >= 0 && (ext[k] == 1 || (va.strides[k] == rows * va.strides[rd] && vb.strides[k] == rows * vb.strides[rd] &&
+                                    ds[k] == rows * ds[rd]))) {
+    rows *= ext[k];
+    --k;
+  }
   int64_t idx[kMaxDims] = {0, 0, 0, 0};
   for (;;) {
     int64_t s0[2] = {so[0], so[1]}, d0 = dof;
-    for (int d = 0; d < rd; ++d) {
+    for (int d = 0; d <= k; ++d) {
       s0[0] += idx[d] * va.strides[d];
       s0[1] += idx[d] * vb.strides[d];
       d0 += idx[d] * ds[d];
     }
-    for (int64_t r = 0; r < ext[rd]; r += per) {
+    for (int64_t r = 0; r < rows; r += per) {
       GItem g{};
-      g.rows = (int32_t)std::min(per, ext[rd] - r);
+      g.rows = (int32_t)std::min(per, rows - r);
       g.src_off[0] = s0[0] + r * va.strides[rd];
       g.src_off[1] = s0[1] + r * vb.strides[rd];
       g.src_pitch[0] = va.strides[rd];
@@ -657,7 +666,7 @@ void emit_gather(reshard_plan &p, size_t a, size_t b, const std::vector<Role> &r
       g.esize = t.esize;
       p.gitems.push_back(g);
     }
-    int d = rd - 1;
+    int d = k;
     for (; d >= 0; --d) {
       if (++idx[d] < ext[d]) break;
       idx[d] = 0;

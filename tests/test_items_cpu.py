@@ -270,6 +270,35 @@ def test_gather_pairs_follow_the_alignment_rule():
     assert int(items2["rows"].sum()) == 64 * 3
 
 
+def test_gather_items_merge_outer_dims():
+    """A 3-D column split whose middle dim is short: outer dims merge into the gather items' rows
+    when both sources and the destination step uniformly over them (64 x 3 rows per pair, not 64
+    items of 3 rows), and the tables still reproduce the oracle; a padded destination pitch on
+    the outer dim keeps them apart."""
+    from test_parity_gpu import _split
+    wl = _split((64, 3, 1000), 4, 3)
+    plan = R.plan_workload(wl)
+    items = R.reshard_plan_items(plan, 6)[0]
+    assert int(items["rows"].sum()) == 64 * 3 * 3
+    assert len(items) <= 3 * -(-64 * 3 // 8)
+    lay = S.allocate(wl, "cpu", misalign=2)
+    S.fill_sources(wl, lay)
+    check_gather_bounds(wl, lay, plan)
+    assert np.array_equal(emulate(wl, lay, plan, "direct", gather=True), _oracle(wl, lay))
+    # destination shards with a padded outer stride: the outer dim is walked explicitly
+    t = wl.tensors[0]
+    cols = [334, 333, 333]
+    t.dst_views = [S.View(i, 0, (3 * c + 8, c, 1)) for i, c in enumerate(cols)]
+    wl = S.workloads._size_buffers(S.Workload("padded", [t]), 4, 3)
+    plan = R.plan_workload(wl)
+    items = R.reshard_plan_items(plan, 6)[0]
+    assert len(items) == 3 * 64 and (items["rows"] == 3).all()
+    lay = S.allocate(wl, "cpu")
+    S.fill_sources(wl, lay)
+    check_gather_bounds(wl, lay, plan)
+    assert np.array_equal(emulate(wl, lay, plan, "direct", gather=True), _oracle(wl, lay))
+
+
 def test_item_tables_fuzzed_layouts():
     """Random shapes, meshes, dtypes and per-rank layouts (dense, padded, column-major, offset)."""
     for wl in S.fuzz_cases(60, seed=23):
