@@ -463,6 +463,21 @@ def _split(shape, ns, nd, reps=1, dtype="bf16", shift=0, dim=-1):
     return S.workloads._size_buffers(S.Workload("split", [t]), ns, nd * reps)
 
 
+def _split_padded_outer(shape, ns, nd):
+    """`_split` along the last dim of a 3-D tensor with every destination's outer stride padded
+    by 8 elements (its outer dim cannot merge into the rows)."""
+    wl = _split(shape, ns, nd)
+    t = wl.tensors[0]
+    cols = [len(range(*sl)) for sl in _chunks(shape[-1], nd)]
+    t.dst_views = [S.View(i, 0, (shape[1] * c + 8, c, 1)) for i, c in enumerate(cols)]
+    return S.workloads._size_buffers(S.Workload("split_padded", [t]), ns, nd)
+
+
+def _chunks(n, k):
+    c = -(-n // k)
+    return [(min(i * c, n), min((i + 1) * c, n)) for i in range(k)]
+
+
 GATHER_CASES = {
     "mesh_pieces_2048_684": lambda: _split((300, 4096), 4, 3),
     "two_replicas": lambda: _split((257, 1000), 4, 3, reps=2),
@@ -473,6 +488,8 @@ GATHER_CASES = {
     "f32": lambda: _split((90, 702), 2, 5, dtype="f32"),                # pairs only across the middle
     "i64_rows": lambda: _split((40, 301), 4, 3, dtype="i64"),
     "three_dims": lambda: _split((3, 50, 1000), 4, 3),
+    "four_dims_merged": lambda: _split((2, 3, 20, 1000), 4, 3),
+    "outer_stride_padded": lambda: _split_padded_outer((16, 3, 1000), 4, 3),
     "long_rows": lambda: _split((16, 40000), 4, 3, reps=2),              # 26.7 KB rows
 }
 
