@@ -351,6 +351,37 @@ def e2e_run(R, wl, plan, sp, dp, lay, args, quant, world, dev, dst_bytes, barrie
            "path": "reshard_execute on page-locked host sources and destinations: the kernels read "
                    "and write host memory over the host link inside the timed region"}
 
+    # --- the host link's ceiling in this run: copy-engine H2D and D2H at the same time (the
+    # same pinned buffers and device slabs; the H2D rewrites the device sources with their own
+    # bytes), against which the in-place step's bytes in and out are set
+    nb = min(hsrc.numel(), hdst.numel(), lay.dst_slab.numel(), 1 << 31)
+    s_a, s_b = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def both():
+        with torch.cuda.stream(s_a):
+            lay.src_slab[:nb].copy_(hsrc[:nb], non_blocking=True)
+        with torch.cuda.stream(s_b):
+            hdst[:nb].copy_(lay.dst_slab[:nb], non_blocking=True)
+
+    both()
+    torch.cuda.synchronize()
+    start, end_a, end_b = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    start.record(s_a)
+    s_b.wait_event(start)
+    reps = 3
+    for _ in range(reps):
+        both()
+    end_a.record(s_a)
+    end_b.record(s_b)
+    torch.cuda.synchronize()
+    l_ms = max(start.elapsed_time(end_a), start.elapsed_time(end_b))
+    link_each = nb * reps / (l_ms / 1e3) / 1e9
+    in_place_each = (st["bytes_read"] + dst_bytes) / 2 * ek / (e_ms / 1e3) / 1e9
+    out["link"] = {"copy_engines_each_way_GBps": round(link_each, 1), "in_place_each_way_GBps": round(in_place_each, 1),
+                   "frac_of_link": round(in_place_each / link_each, 3),
+                   "what": "copy-engine H2D and D2H of 2 GiB pinned buffers at the same time, this run; the "
+                           "in-place step's source bytes in and destination bytes out per second, averaged"}
+
     # --- staged through device memory with copy-engine transfers
     s_in, s_run, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
 
