@@ -307,6 +307,45 @@ def dominant_kernel(R, plan, mode: str, quant: str) -> str:
     return max(counts, key=counts.get)
 
 
+# page-locked host copies of one rank's slabs may take at most this share of the host's memory,
+# split over the ranks on the host; past it the end-to-end leg runs on a prefix of the tensors
+E2E_HOST_FRACTION = 0.45
+
+
+def host_ram_bytes():
+    """Physical memory of this host in bytes, or None where sysconf does not say."""
+    try:
+        return os.sysconf("SC_PAGE_SIZE") * os.sysconf("SC_PHYS_PAGES")
+    except (ValueError, OSError, AttributeError):
+        return None
+
+
+def e2e_prefix(wl, budget: int):
+    """(workload, k): `wl` cut to its longest prefix of k tensors whose page-locked host copies
+    (source, destination and scale slabs, laid out as for the device) fit in `budget` bytes;
+    `wl` itself when all of it fits, (None, 0) when not even the first tensor does."""
+    import synthetic as S
+
+    def sub(k):
+        w = S.Workload(wl.name, wl.tensors[:k], wl.quant, wl.values)
+        return S.workloads._size_buffers(w, len(wl.src_buffer_numel), len(wl.dst_buffer_numel))
+
+    def host_bytes(w):
+        lay = S.allocate(w, "meta")
+        return lay.src_slab.numel() + lay.dst_slab.numel() + (lay.scale_slab.numel() if lay.scale_slab is not None else 0)
+
+    if host_bytes(wl) <= budget:
+        return wl, len(wl.tensors)
+    lo, hi = 0, len(wl.tensors) - 1  # the largest k that fits lies in [lo, hi]
+    while lo < hi:
+        mid = (lo + hi + 1) // 2
+        if host_bytes(sub(mid)) <= budget:
+            lo = mid
+        else:
+            hi = mid - 1
+    return (sub(lo), lo) if lo else (None, 0)
+
+
 def e2e_run(R, wl, plan, sp, dp, lay, args, quant, world, dev, dst_bytes, barrier, st):
     """End to end through the public call with host buffers.
 
@@ -603,8 +642,32 @@ def our_arm(args, rank: int, world: int, local_rank: int) -> None:
     # destinations go to page-locked host memory inside the timed region
     e2e = None
     if not args.no_e2e:
+        ranks_here = max(1, int(os.environ.get("LOCAL_WORLD_SIZE", str(world))))
+        ram = host_ram_bytes()
+        frac = args.e2e_host_fraction
+        budget = int(frac * ram / ranks_here) if ram else None
         try:
-            e2e = e2e_run(R, wl, plan, sp, dp, lay, args, quant, world, dev, dst_bytes, barrier, st)
+            ew, k = (wl, len(wl.tensors)) if budget is None else e2e_prefix(wl, budget)
+            if ew is wl:
+                e2e = e2e_run(R, wl, plan, sp, dp, lay, args, quant, world, dev, dst_bytes, barrier, st)
+            elif k == 0:
+                e2e = {"value": None, "unit": "GB/s",
+                       "skipped": f"one tensor's page-locked copies exceed {budget / 1e9:.1f} GB per rank"}
+            else:
+                lay_e = S.allocate(ew, dev)
+                S.fill_sources(ew, lay_e)
+                S.fill_canary(lay_e)
+                plan_e = R.plan_workload(ew)
+                sp_e, dp_e = R.workload_pointers(ew, lay_e)
+                # the device-resident result the host one is compared with
+                R.reshard_execute(plan_e, sp_e, dp_e, mode=args.mode, quant=quant, stream=sh)
+                torch.cuda.synchronize()
+                e2e = e2e_run(R, ew, plan_e, sp_e, dp_e, lay_e, args, quant, world, dev, ew.dst_bytes(), barrier,
+                              R.reshard_plan_stats(plan_e))
+                e2e["sample"] = (f"first {k} of {len(wl.tensors)} tensors per rank: page-locked copies of the whole "
+                                 f"workload for {ranks_here} rank(s) would pass {frac:.0%} of this "
+                                 f"host's {ram / 1e9:.0f} GB")
+                del lay_e, plan_e
         except RuntimeError as e:
             e2e = {"value": None, "unit": "GB/s", "error": str(e)[:200]}
 
@@ -680,6 +743,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-targets", action="store_true", help="skip the other north-star workloads")
     ap.add_argument("--suite", default=None, help="also append the JSON line to this file")
+    ap.add_argument("--e2e-host-fraction", type=float, default=E2E_HOST_FRACTION,
+                    help="share of host memory the end-to-end leg's page-locked copies may take, split over "
+                         "the ranks on the host; past it the leg runs on the longest prefix of tensors that fits")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
