@@ -529,8 +529,8 @@ GITEM_DTYPE = [("src_off", "<i8", (2,)), ("src_pitch", "<i8", (2,)), ("dst_off",
 
 def reshard_plan_items(plan: Plan, which: int = 0):
     """(items as a numpy structured array, group_start, member_ptr, member_off) of one table:
-    0/1/2 strided-copy items of the direct/pack/unpack pass, 3/4/5 their transposing items, 6 the
-    direct pass's gather items (copy items they cover have pad[0] == 1)."""
+    0/1/2 strided-copy items of the direct/pack/unpack pass, 3/4/5 their transposing items, 6/7/8
+    their gather items (copy items they cover have pad[0] == 1; the pack pass has none)."""
     import numpy as np
     n, ng, nm = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
     _check(LIB.reshard_plan_items(plan.handle, which, 0, None, ctypes.byref(n), None, None, None,

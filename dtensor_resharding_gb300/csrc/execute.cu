@@ -1757,8 +1757,8 @@ int classify(reshard_plan_t *p, int set, cudaStream_t stream) {
   int64_t gen_bytes = 0, row_bytes = 0;
   // bulk copies read device memory only (page-locked host memory goes through the walkers)
   const bool stage_ok = RESHARD_STAGED && !p->any_host;
-  // the direct pass's gather items write the rows of the copy items flagged kGathered
-  const bool gathered = set == kDirect && !p->gitems.empty();
+  // the pass's gather items write the rows of the copy items flagged kGathered
+  const bool gathered = !p->gitems[set].empty();
   for (size_t i = 0; i < items.size(); ++i) {
     const Item &it = items[i];
     if (gathered && it.pad[0] == kGathered) continue;
@@ -1821,16 +1821,17 @@ int classify(reshard_plan_t *p, int set, cudaStream_t stream) {
   return RESHARD_OK;
 }
 
-// Resolve the gather items for the current pointer table (absolute addresses of both pieces and
-// of the first two replicas) and upload them on `stream`, when the table has changed.
-int bind_gather(reshard_plan_t *p, cudaStream_t stream) {
-  if (p->d_gbound && p->gbound_version == p->ptr_version) return RESHARD_OK;
+// Resolve the gather items of pass `set` for the current pointer table (absolute addresses of both
+// pieces and of the first two replicas) and upload them on `stream`, when the table has changed.
+int bind_gather(reshard_plan_t *p, int set, cudaStream_t stream) {
+  if (p->d_gbound[set] && p->gbound_version[set] == p->ptr_version) return RESHARD_OK;
   const std::vector<uint64_t> &tab = p->dev_ptrs;
-  const size_t n = p->gitems.size();
-  p->gbound.resize(n);
+  const size_t n = p->gitems[set].size();
+  std::vector<GBound> &bound = p->gbound[set];
+  bound.resize(n);
   for (size_t i = 0; i < n; ++i) {
-    const GItem &g = p->gitems[i];
-    GBound &b = p->gbound[i];
+    const GItem &g = p->gitems[set][i];
+    GBound &b = bound[i];
     const uint64_t es = (uint64_t)g.esize;
     const int32_t m0 = p->grp_start[(size_t)g.group];
     const int32_t nrep = p->grp_start[(size_t)g.group + 1] - m0;
@@ -1852,9 +1853,9 @@ int bind_gather(reshard_plan_t *p, cudaStream_t stream) {
     b.esize = g.esize;
     b.pad[0] = b.pad[1] = 0;
   }
-  if (!p->d_gbound) RS_CUDA(cudaMalloc(&p->d_gbound, n * sizeof(GBound)));
-  RS_CUDA(cudaMemcpyAsync(p->d_gbound, p->gbound.data(), n * sizeof(GBound), cudaMemcpyHostToDevice, stream));
-  p->gbound_version = p->ptr_version;
+  if (!p->d_gbound[set]) RS_CUDA(cudaMalloc(&p->d_gbound[set], n * sizeof(GBound)));
+  RS_CUDA(cudaMemcpyAsync(p->d_gbound[set], bound.data(), n * sizeof(GBound), cudaMemcpyHostToDevice, stream));
+  p->gbound_version[set] = p->ptr_version;
   return RESHARD_OK;
 }
 
@@ -1874,12 +1875,12 @@ int launch(reshard_plan_t *p, int set, bool quant, cudaStream_t stream, const La
   } else {
     if ((rc = classify(p, set, stream))) return rc;
     const int na = p->n_aligned[set], ns = p->n_staged[set], ng = p->n_general[set];
-    const int nx = set == kDirect ? (int)p->gitems.size() : 0;
+    const int nx = (int)p->gitems[set].size();
     const int32_t *idx = p->d_cls_idx[set];
     p->last_aligned = na;
     p->last_staged = ns;
     p->last_general = ng;
-    if (nx) p->last_gather = nx;
+    p->last_gather += nx;
     if (na > 0 && RESHARD_BULK && !p->any_host) {  // bulk copies over device memory only
       RS_CUDA(launch_kernel(true, reshard_bulk_kernel, std::min(na, caps.bulk_grid), 32, kBulkSmem, stream, items, idx, na,
                             p->d_ptrs, p->d_grp_start, p->d_mem_ptr, p->d_mem_off, p->d_status));
@@ -1910,10 +1911,10 @@ int launch(reshard_plan_t *p, int set, bool quant, cudaStream_t stream, const La
       ++p->last_launches;
     }
     if (nx > 0) {
-      if ((rc = bind_gather(p, stream))) return rc;
+      if ((rc = bind_gather(p, set, stream))) return rc;
       const int wait_gather = RESHARD_GEN_OVERLAP && na + ns + ng > 0 ? 1 : 0;
       RS_CUDA(launch_kernel(true, reshard_copy_gather_kernel, std::min(nx, caps.gather_grid), kBlock, 0, stream,
-                            static_cast<const GBound *>(p->d_gbound), nx, p->d_ptrs, p->d_grp_start, p->d_mem_ptr,
+                            static_cast<const GBound *>(p->d_gbound[set]), nx, p->d_ptrs, p->d_grp_start, p->d_mem_ptr,
                             p->d_mem_off, wait_gather));
       ++p->last_launches;
     }
@@ -1935,8 +1936,10 @@ void free_device(reshard_plan_t *p) {
     if (d) cudaFree(d);
     d = nullptr;
   }
-  if (p->d_gbound) cudaFree(p->d_gbound);
-  p->d_gbound = nullptr;
+  for (auto &d : p->d_gbound) {
+    if (d) cudaFree(d);
+    d = nullptr;
+  }
   if (p->d_maps) cudaFree(p->d_maps);
   if (p->d_map_ok) cudaFree(p->d_map_ok);
   if (p->d_status) cudaFree(p->d_status);

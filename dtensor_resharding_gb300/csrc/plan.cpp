@@ -566,9 +566,12 @@ const int64_t *region_dest(const reshard_plan &p, const Region &r, const Group &
 // length is not a multiple of 16 bytes), where the two plain items would each be walked as
 // short rows. partner[A] = B, partner[B] = -2 - A, -1 for an unpaired region.
 std::vector<int64_t> gather_pairs(const reshard_plan &p, const std::vector<Role> &roles,
-                                  const std::vector<Group> &dev_groups) {
+                                  const std::vector<Group> &dev_groups, int set) {
   std::vector<int64_t> partner(p.regions.size(), -1);
   if (!RESHARD_GATHER) return partner;
+  // the region's destination group in this pass (the unpack pass reads dense message blocks,
+  // contiguous along the last dim by construction)
+  auto group_of = [&](size_t i) { return set == kDirect ? roles[i].direct : roles[i].unpack; };
 
   // candidates keyed by (tensor, device group, the box outside the last dim)
   std::map<std::vector<int64_t>, std::vector<size_t>> rows_of;
@@ -576,12 +579,12 @@ std::vector<int64_t> gather_pairs(const reshard_plan &p, const std::vector<Role>
     const Region &r = p.regions[i];
     const TensorInfo &t = p.tensors[(size_t)r.tensor];
     const int nd = t.ndim, last = nd - 1;
-    if (roles[i].direct < 0 || nd < 2) continue;
+    if (group_of(i) < 0 || nd < 2) continue;
     if (r.box.hi[last] - r.box.lo[last] < 2 || r.box.hi[last - 1] - r.box.lo[last - 1] < 2) continue;
-    if (t.src_view[(size_t)r.src].strides[last] != 1) continue;
-    const Group &g = dev_groups[(size_t)roles[i].direct];
+    if (set == kDirect && t.src_view[(size_t)r.src].strides[last] != 1) continue;
+    const Group &g = dev_groups[(size_t)group_of(i)];
     if (t.dst_view[(size_t)g.members[0]].strides[last] != 1) continue;
-    std::vector<int64_t> key{r.tensor, roles[i].direct};
+    std::vector<int64_t> key{r.tensor, group_of(i)};
     for (int d = 0; d < last; ++d) {
       key.push_back(r.box.lo[d]);
       key.push_back(r.box.hi[d]);
@@ -597,7 +600,7 @@ std::vector<int64_t> gather_pairs(const reshard_plan &p, const std::vector<Role>
     for (size_t k = 0; k + 1 < v.size(); ++k) {
       const Region &a = p.regions[v[k]], &b = p.regions[v[k + 1]];
       if (a.box.hi[last] != b.box.lo[last]) continue;
-      const Group &g = dev_groups[(size_t)roles[v[k]].direct];
+      const Group &g = dev_groups[(size_t)group_of(v[k])];
       const int64_t dpitch = t.dst_view[(size_t)g.members[0]].strides[last - 1] * t.esize;
       const int64_t len_a = (a.box.hi[last] - a.box.lo[last]) * t.esize;
       if (dpitch % 16 == 0 && len_a % 16 == 0) continue;
@@ -617,26 +620,46 @@ std::vector<int64_t> gather_pairs(const reshard_plan &p, const std::vector<Role>
 // (3,) / (3,2) mesh reshards: 16 rows of 2,732 bytes with one replica, 8 with two, against
 // 0.78-0.83 of the copy rate for items of about item_bytes of source).
 void emit_gather(reshard_plan &p, size_t a, size_t b, const std::vector<Role> &roles, const std::vector<Group> &dev_groups,
-                 int64_t item_bytes) {
+                 int64_t item_bytes, int set) {
   const Region &ra = p.regions[a], &rb = p.regions[b];
   const TensorInfo &t = p.tensors[(size_t)ra.tensor];
   const int nd = t.ndim, last = nd - 1, rd = nd - 2;
-  int64_t so[2], dof;
-  const RankView &va = region_source(p, ra, so[0]);
-  const RankView &vb = region_source(p, rb, so[1]);
-  const int64_t *ds = region_dest(p, ra, dev_groups[(size_t)roles[a].direct], dof);
+  const int32_t dg = set == kDirect ? roles[a].direct : roles[a].unpack;
   int64_t ext[kMaxDims];
   for (int d = 0; d < nd; ++d) ext[d] = ra.box.hi[d] - ra.box.lo[d];
   const int64_t len[2] = {ext[last], rb.box.hi[last] - rb.box.lo[last]};
+  // each piece's source: its source shard (direct), or its dense block of the received message
+  // (unpack: row-major over the region's extents, at the region's byte offset recv_off)
+  int64_t so[2], sst[2][kMaxDims];
+  int32_t sptr[2];
+  for (int q = 0; q < 2; ++q) {
+    const size_t ri = q ? b : a;
+    const Region &r = p.regions[ri];
+    if (set == kDirect) {
+      const RankView &v = region_source(p, r, so[q]);
+      for (int d = 0; d < nd; ++d) sst[q][d] = v.strides[d];
+      sptr[q] = (int32_t)(t.src_base + r.src);
+    } else {
+      so[q] = roles[ri].recv_off / t.esize;
+      int64_t acc = 1;
+      for (int d = nd - 1; d >= 0; --d) {
+        sst[q][d] = acc;
+        acc *= d == last ? len[q] : ext[d];
+      }
+      sptr[q] = (int32_t)(p.workspace_ptr + 1);
+    }
+  }
+  int64_t dof;
+  const int64_t *ds = region_dest(p, ra, dev_groups[(size_t)dg], dof);
   const int64_t row_b = (len[0] + len[1]) * t.esize;
-  const int64_t nrep = (int64_t)dev_groups[(size_t)roles[a].direct].members.size();
+  const int64_t nrep = (int64_t)dev_groups[(size_t)dg].members.size();
   int64_t per = kGatherItemBytes / (row_b * (1 + nrep)) / kGatherRowStep * kGatherRowStep;
   per = std::min(std::max(per, kGatherRowStep), std::max<int64_t>(1, item_bytes / row_b));
   // outer dims merge into the rows dim while both sources and the destination step uniformly
   // over them (as the plain items' rows do); the rest are walked explicitly
   int64_t rows = ext[rd];
   int k = rd - 1;
-  while (k >= 0 && (ext[k] == 1 || (va.strides[k] == rows * va.strides[rd] && vb.strides[k] == rows * vb.strides[rd] &&
+  while (k >= 0 && (ext[k] == 1 || (sst[0][k] == rows * sst[0][rd] && sst[1][k] == rows * sst[1][rd] &&
                                     ds[k] == rows * ds[rd]))) {
     rows *= ext[k];
     --k;
@@ -645,26 +668,26 @@ void emit_gather(reshard_plan &p, size_t a, size_t b, const std::vector<Role> &r
   for (;;) {
     int64_t s0[2] = {so[0], so[1]}, d0 = dof;
     for (int d = 0; d <= k; ++d) {
-      s0[0] += idx[d] * va.strides[d];
-      s0[1] += idx[d] * vb.strides[d];
+      s0[0] += idx[d] * sst[0][d];
+      s0[1] += idx[d] * sst[1][d];
       d0 += idx[d] * ds[d];
     }
     for (int64_t r = 0; r < rows; r += per) {
       GItem g{};
       g.rows = (int32_t)std::min(per, rows - r);
-      g.src_off[0] = s0[0] + r * va.strides[rd];
-      g.src_off[1] = s0[1] + r * vb.strides[rd];
-      g.src_pitch[0] = va.strides[rd];
-      g.src_pitch[1] = vb.strides[rd];
+      g.src_off[0] = s0[0] + r * sst[0][rd];
+      g.src_off[1] = s0[1] + r * sst[1][rd];
+      g.src_pitch[0] = sst[0][rd];
+      g.src_pitch[1] = sst[1][rd];
       g.dst_off = d0 + r * ds[rd];
       g.dst_pitch = ds[rd];
       g.run[0] = (int32_t)len[0];
       g.run[1] = (int32_t)len[1];
-      g.src[0] = (int32_t)(t.src_base + ra.src);
-      g.src[1] = (int32_t)(t.src_base + rb.src);
-      g.group = roles[a].direct;
+      g.src[0] = sptr[0];
+      g.src[1] = sptr[1];
+      g.group = dg;
       g.esize = t.esize;
-      p.gitems.push_back(g);
+      p.gitems[set].push_back(g);
     }
     int d = k;
     for (; d >= 0; --d) {
@@ -706,8 +729,9 @@ int emit_tables(reshard_plan *plan, const std::vector<Role> &roles, const std::v
   int64_t item_bytes = kMaxItemBytes;
   while (item_bytes > kMinItemBytes && plan_bytes / item_bytes < kItemsPerPlan) item_bytes /= 2;
   std::map<SlabSpec, int32_t> slab_ids;
-  const std::vector<int64_t> partner = gather_pairs(*plan, roles, dev_groups);
-  plan->gitems.clear();
+  const std::vector<int64_t> partner = gather_pairs(*plan, roles, dev_groups, kDirect);
+  const std::vector<int64_t> partner_u = gather_pairs(*plan, roles, dev_groups, kUnpack);
+  for (auto &gv : plan->gitems) gv.clear();
   for (size_t i = 0; i < plan->regions.size(); ++i) {
     const Region &r = plan->regions[i];
     const Role &role = roles[i];
@@ -751,7 +775,7 @@ int emit_tables(reshard_plan *plan, const std::vector<Role> &roles, const std::v
       // (flagged) for the passes that walk plain items only
       if (partner[i] != -1)
         for (size_t k = n0; k < plan->items[kDirect].size(); ++k) plan->items[kDirect][k].pad[0] = kGathered;
-      if (partner[i] >= 0) emit_gather(*plan, i, (size_t)partner[i], roles, dev_groups, item_bytes);
+      if (partner[i] >= 0) emit_gather(*plan, i, (size_t)partner[i], roles, dev_groups, item_bytes, kDirect);
     }
     if (role.send_off >= 0) {
       const int64_t mo = role.send_off / t.esize;
@@ -763,8 +787,12 @@ int emit_tables(reshard_plan *plan, const std::vector<Role> &roles, const std::v
       const ReadSide from_msg{recv_ptr, mo, zero, ext};
       int64_t dof;
       const int64_t *ds = dst_side(role.unpack, dof);
+      const size_t n0 = plan->items[kUnpack].size();
       emit_region(nd, ext, mo, ms, from_msg, dof, ds, role.unpack, t.esize, item_bytes, plan->items[kUnpack],
                   plan->titems[kUnpack], slab_ids, plan->slabs);
+      if (partner_u[i] != -1)
+        for (size_t k = n0; k < plan->items[kUnpack].size(); ++k) plan->items[kUnpack][k].pad[0] = kGathered;
+      if (partner_u[i] >= 0) emit_gather(*plan, i, (size_t)partner_u[i], roles, dev_groups, item_bytes, kUnpack);
     }
   }
 #if RESHARD_SIZE_ORDER == 1
@@ -815,7 +843,7 @@ int emit_tables(reshard_plan *plan, const std::vector<Role> &roles, const std::v
   st.n_tensors = (int64_t)plan->tensors.size();
   st.regions = (int64_t)plan->regions.size();
   st.items = (int64_t)(plan->items[kDirect].size() + plan->titems[kDirect].size());
-  st.gather_items = (int64_t)plan->gitems.size();
+  st.gather_items = (int64_t)(plan->gitems[kDirect].size() + plan->gitems[kUnpack].size());
   st.dst_groups = (int64_t)plan->groups.size();
   st.gather_bcast_bytes = 2 * global_bytes;
   st.global_bytes = global_bytes;
@@ -823,7 +851,7 @@ int emit_tables(reshard_plan *plan, const std::vector<Role> &roles, const std::v
   st.world = plan->world;
   if ((int64_t)(plan->items[kDirect].size() + plan->items[kPack].size() + plan->items[kUnpack].size() +
                 plan->titems[kDirect].size() + plan->titems[kPack].size() + plan->titems[kUnpack].size() +
-                plan->gitems.size()) > INT32_MAX ||
+                plan->gitems[kDirect].size() + plan->gitems[kUnpack].size()) > INT32_MAX ||
       (int64_t)plan->mem_ptr.size() > INT32_MAX || (int64_t)plan->slabs.size() > INT32_MAX ||
       pointer_table_size(plan) > INT32_MAX) {
     return fail(RESHARD_ERR_UNSUPPORTED, "plan too large (more than 2^31 items, members or pointers)");
@@ -1261,7 +1289,7 @@ extern "C" int reshard_plan_items(const reshard_plan_t *plan, int set, int64_t c
                                   int32_t *group_start, int32_t *member_ptr, int64_t *member_off,
                                   int64_t *n_groups_out, int64_t *n_members_out) {
   if (!plan) return fail(RESHARD_ERR_INVALID_ARG, "plan is NULL");
-  if (set < 0 || set > 2 * kNumSets) return fail(RESHARD_ERR_INVALID_ARG, "set must be in 0..6");
+  if (set < 0 || set >= 3 * kNumSets) return fail(RESHARD_ERR_INVALID_ARG, "set must be in 0..8");
   static_assert(sizeof(Item) == sizeof(TItem), "both item kinds are 64 bytes");
   size_t count, size = sizeof(Item);
   const void *data;
@@ -1272,8 +1300,8 @@ extern "C" int reshard_plan_items(const reshard_plan_t *plan, int set, int64_t c
     count = plan->titems[set - kNumSets].size();
     data = plan->titems[set - kNumSets].data();
   } else {
-    count = plan->gitems.size();
-    data = plan->gitems.data();
+    count = plan->gitems[set - 2 * kNumSets].size();
+    data = plan->gitems[set - 2 * kNumSets].data();
     size = sizeof(GItem);
   }
   if (n_out) *n_out = (int64_t)count;

@@ -91,12 +91,13 @@ static_assert(sizeof(TItem) == 64, "transposing item is one 64-byte descriptor")
 constexpr int64_t kGatherItemBytes = RESHARD_GATHER_ITEM_KIB * 1024;
 constexpr int64_t kGatherRowStep = 8;
 
-// Gather item of the direct pass: `rows` destination rows each made of two pieces that sit side
-// by side along the destination's contiguous dim, piece 0's `run[0]` elements then piece 1's
-// `run[1]`. Row i of piece p is read at src_off[p] + i * src_pitch[p] of pointer src[p]; row i of
-// destination replica m starts at member_offset[m] + dst_off + i * dst_pitch of that member's
-// pointer. It replaces the two plain items flagged kGathered (the allocation-free entry point and
-// the alignment classes still use the plain items).
+// Gather item of the direct or unpack pass: `rows` destination rows each made of two pieces that
+// sit side by side along the destination's contiguous dim, piece 0's `run[0]` elements then piece
+// 1's `run[1]`. Row i of piece p is read at src_off[p] + i * src_pitch[p] of pointer src[p] (a
+// source shard in the direct pass, the receive buffer in the unpack pass); row i of destination
+// replica m starts at member_offset[m] + dst_off + i * dst_pitch of that member's pointer. It
+// replaces the plain items of its two regions, which stay in the pass's table flagged kGathered
+// (the MXFP8 passes and the allocation-free entry point walk the plain items).
 struct alignas(16) GItem {
   int64_t src_off[2];
   int64_t src_pitch[2];
@@ -218,8 +219,8 @@ struct reshard_plan {
   int64_t n_src_ptrs = 0, n_dst_ptrs = 0;
   std::vector<reshard::Item> items[reshard::kNumSets];
   std::vector<reshard::TItem> titems[reshard::kNumSets];  // transposing items of each pass
-  std::vector<reshard::GItem> gitems;                      // gather items of the direct pass
-  std::vector<reshard::GBound> gbound;                     // ... resolved for the current pointer table
+  std::vector<reshard::GItem> gitems[reshard::kNumSets];   // gather items of each pass (none in pack)
+  std::vector<reshard::GBound> gbound[reshard::kNumSets];  // ... resolved for the current pointer table
   std::vector<reshard::SlabSpec> slabs;                    // TMA source slabs (all passes)
   // group table (device layout): members of group g are [grp_start[g], grp_start[g + 1])
   std::vector<int32_t> grp_start;
@@ -243,8 +244,8 @@ struct reshard_plan {
   int device = -1;
   void *d_items[reshard::kNumSets] = {nullptr, nullptr, nullptr};
   void *d_titems[reshard::kNumSets] = {nullptr, nullptr, nullptr};
-  void *d_gbound = nullptr;     // the resolved gather items (gbound)
-  uint64_t gbound_version = 0;  // the pointer-table version they were resolved for
+  void *d_gbound[reshard::kNumSets] = {nullptr, nullptr, nullptr};  // the resolved gather items
+  uint64_t gbound_version[reshard::kNumSets] = {0, 0, 0};           // the pointer-table version of each
   void *d_maps = nullptr;      // one 128-byte CUtensorMap per slab (64-byte aligned)
   int32_t *d_map_ok = nullptr; // 1 where the slab's map could be encoded
   int32_t *d_status = nullptr; // device-side status word (bit 0: a TMA wait timed out)
@@ -263,7 +264,7 @@ struct reshard_plan {
   int64_t last_general = 0;  // ... and the general walker
   int64_t last_rows_kernel = 0;  // 1 when those ran in the many-rows build of the general walker
   int64_t last_staged = 0;       // copy items of the last pass run by the bulk-staged kernel
-  int64_t last_gather = 0;       // gather items of the last direct pass
+  int64_t last_gather = 0;       // gather items run by the last execute (all its passes)
   bool gen_rows[reshard::kNumSets] = {false, false, false};  // general items mostly short rows
   int32_t *d_grp_start = nullptr;
   int32_t *d_mem_ptr = nullptr;

@@ -160,8 +160,9 @@ typedef struct {
   int64_t local_bytes;        /* source bytes this rank copies to its own destinations directly */
   int64_t last_staged_items;  /* copy items of the last execute's last pass run by the bulk-staged
                                  kernel (reshard_copy_staged_kernel: misaligned rows < 4 KiB) */
-  int64_t gather_items;       /* gather items of the direct mode: destination rows assembled from
-                                 two source pieces side by side (reshard_plan_items set 6) */
+  int64_t gather_items;       /* gather items of the direct and unpack passes: destination rows
+                                 assembled from two source pieces side by side (reshard_plan_items
+                                 sets 6 and 8) */
   int64_t last_gather_items;  /* gather items run by the last execute (reshard_copy_gather_kernel) */
 } reshard_stats_t;
 
@@ -232,7 +233,7 @@ int reshard_plan_blockwise_fp8(const reshard_tensor_spec_t *specs, int n_tensors
  * re-sorted on the host into those 16-byte aligned everywhere (run by the aligned walker),
  * misaligned items of rows shorter than 4 KiB in device memory (run by the bulk-staged kernel)
  * and the rest (run by the general walker), and the gather items (destination rows of two
- * source pieces, reshard_plan_items set 6; run by the gather kernel in the direct mode without
+ * source pieces, reshard_plan_items sets 6 and 8; run by the gather kernel in passes without
  * quantization) are resolved to absolute addresses and re-uploaded on `stream`: host work
  * proportional to the plan's items, none when the pointers repeat.
  * Buffers must stay valid until the stream reaches the end of the work. Executes of one plan
@@ -371,7 +372,8 @@ int reshard_plan_group_members(const reshard_plan_t *plan, int64_t g, int64_t ca
 /*
  * reshard_plan_items -- copy a device work-item table for inspection. set 0/1/2: the strided
  * copy items of the direct / pack / unpack pass; set 3/4/5: the transposing items of the same
- * passes (64 bytes each); set 6: the gather items of the direct pass (80 bytes each).
+ * passes (64 bytes each); set 6/7/8: the gather items of the same passes (80 bytes each; the
+ * pack pass has none).
  * Copy item: int64 src_off, dst_off, src_pitch, dst_pitch (elements); int32 rows, run (elements
  * per row), src (pointer-table index), group, esize (bytes), 3 x int32 padding. It moves `rows`
  * rows of `run` elements from src_off + r * src_pitch of pointer `src` to
@@ -383,9 +385,10 @@ int reshard_plan_group_members(const reshard_plan_t *plan, int64_t g, int64_t ca
  * group, esize, padding. Destination row r is piece 0's run[0] elements from
  * src_off[0] + r * src_pitch[0] of pointer src[0], then piece 1's run[1] elements from
  * src_off[1] + r * src_pitch[1] of pointer src[1], written at member_offset + dst_off +
- * r * dst_pitch of every member of `group`. The direct pass's copy items that a gather item covers
- * carry 1 in their first padding word; the copy walkers skip them when gather items run, and
- * every other pass over the copy items (MXFP8, the allocation-free entry point) takes them.
+ * r * dst_pitch of every member of `group` (in the unpack pass both pieces are read from the
+ * receive buffer's entry). A pass's copy items that a gather item covers carry 1 in their first
+ * padding word; the copy walkers skip them when gather items run, and every other walk of the copy
+ * items (MXFP8, the allocation-free entry point) takes them.
  * Pointer table: [sources | destination data | destination scales | send buffer | receive
  * buffer] (pack items write the send buffer's group, unpack items read the receive buffer). Up to
  * cap items go to `items` (may be NULL); *n_out gets the count. Copy items are ordered largest

@@ -14,8 +14,8 @@ import dtensor_resharding_gb300 as R
 
 def run_items(plan, which, table, arrays, gather=False):
     """Apply pass `which` (0 direct, 1 pack, 2 unpack) of `plan` to the named host arrays. With
-    `gather`, the direct pass runs as the executor runs it when gather items are present: the
-    gather items, and the copy items they do not cover (pad[0] == 0)."""
+    `gather`, the pass runs as the executor runs it when it has gather items: the gather items,
+    and the copy items they do not cover (pad[0] == 0)."""
     items, gs, mp, mo = R.reshard_plan_items(plan, which + 3)
     for it in items:
         e = int(it["esize"])
@@ -28,8 +28,8 @@ def run_items(plan, which, table, arrays, gather=False):
             doff = dbase + (int(mo[m]) + int(it["dst_off"]) + cc * int(it["dst_pitch"]) + rr) * e
             arrays[dkind][(doff[..., None] + np.arange(e)).reshape(-1)] = vals
     skip_flagged = False
-    if gather and which == 0:
-        gitems, gs, mp, mo = R.reshard_plan_items(plan, 6)
+    if gather:
+        gitems, gs, mp, mo = R.reshard_plan_items(plan, 6 + which)
         skip_flagged = len(gitems) > 0
         for it in gitems:
             e = int(it["esize"])

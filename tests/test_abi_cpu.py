@@ -290,7 +290,7 @@ def test_every_entry_point_refuses_null_and_out_of_range_arguments():
     assert L.reshard_plan_stats(plan.handle, None) == inv
     assert L.reshard_plan_group_members(plan.handle, 10 ** 6, 0, None, ctypes.byref(n)) == inv
     assert L.reshard_plan_group_members(plan.handle, -1, 0, None, ctypes.byref(n)) == inv
-    assert L.reshard_plan_items(plan.handle, 7, 0, None, ctypes.byref(n), None, None, None, None, None) == inv
+    assert L.reshard_plan_items(plan.handle, 9, 0, None, ctypes.byref(n), None, None, None, None, None) == inv
     assert L.reshard_plan_items(plan.handle, -1, 0, None, ctypes.byref(n), None, None, None, None, None) == inv
     assert L.reshard_plan_transfers(plan.handle, 3, 0, None, ctypes.byref(n)) == inv
     assert L.reshard_plan_partition(plan.handle, None, None, 1, 0, 0, None) == inv

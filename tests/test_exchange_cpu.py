@@ -157,7 +157,7 @@ def _rank_main(rank, world, port, combos, out):
             run_items(rp, 0, table, arrays, gather=True)   # local copies, gather items included
             run_items(rp, 1, table, arrays)          # outgoing messages
             exchange.run_transfers(rp, torch.from_numpy(send), torch.from_numpy(recv))
-            run_items(rp, 2, table, arrays)          # received messages
+            run_items(rp, 2, table, arrays, gather=True)   # received messages
             want = np.full(lay.dst_slab.numel(), CANARY, np.uint8)
             coracle.run_workload(wl, lay.src_slab.numpy(), lay.src_off, want, lay.dst_off)
             bad_local, bad_other = 0, 0
@@ -341,5 +341,5 @@ def test_brute_force_partitions_through_the_loopback_transport():
             arrays.append(a)
         exchange.loopback_transfers([p for p, _ in parts], sends, recvs)
         for (rp, table), a in zip(parts, arrays):
-            run_items(rp, 2, table, a)
+            run_items(rp, 2, table, a, gather=True)
         assert np.array_equal(dst, want), (i, wl.tensors[0], world, so, do)

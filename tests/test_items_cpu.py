@@ -109,11 +109,17 @@ def check_transpose_bounds(wl, lay, plan, which, ws=None):
     assert (end <= hi[sl[:, 0]]).all(), "a TMA slab reaches past its buffer"
 
 
-def check_gather_bounds(wl, lay, plan, ws=None):
-    """Gather items: both pieces' reads and every row's writes stay in their buffers, and the
-    gather items carry exactly the bytes of the direct copy items flagged as theirs."""
-    items, gs, mp, mo = R.reshard_plan_items(plan, 6)
-    plain = R.reshard_plan_items(plan, DIRECT)[0]
+def check_gather_bounds(wl, lay, plan, ws=None, which=None):
+    """Gather items of the direct and unpack passes (or of pass `which`): both pieces' reads and
+    every row's writes stay in their buffers, and a pass's gather items carry exactly the bytes
+    of its copy items flagged as theirs."""
+    if which is None:
+        assert len(R.reshard_plan_items(plan, 6 + PACK)[0]) == 0
+        for w in (DIRECT, UNPACK):
+            check_gather_bounds(wl, lay, plan, ws, w)
+        return
+    items, gs, mp, mo = R.reshard_plan_items(plan, 6 + which)
+    plain = R.reshard_plan_items(plan, which)[0]
     flagged = plain[plain["pad"][:, 0] == 1]
     assert set(np.unique(plain["pad"][:, 0])) <= {0, 1}
     if len(items) == 0:
@@ -175,8 +181,7 @@ def test_item_tables_reproduce_oracle(name, mode):
     check_gather_bounds(wl, lay, plan)
     want = _oracle(wl, lay)
     assert np.array_equal(emulate(wl, lay, plan, mode), want)
-    if mode == "direct":
-        assert np.array_equal(emulate(wl, lay, plan, mode, gather=True), want)
+    assert np.array_equal(emulate(wl, lay, plan, mode, gather=True), want)
 
 
 def test_item_tables_brute_force():
@@ -190,7 +195,7 @@ def test_item_tables_brute_force():
         want = _oracle(wl, lay)
         for mode in ("direct", "packed"):
             assert np.array_equal(emulate(wl, lay, plan, mode), want)
-        assert np.array_equal(emulate(wl, lay, plan, "direct", gather=True), want)
+            assert np.array_equal(emulate(wl, lay, plan, mode, gather=True), want)
 
 
 @pytest.mark.parametrize("case", ["moe_tp4", "six_replicas"])
@@ -238,10 +243,15 @@ def test_gather_items_where_rows_are_split_and_misaligned(name):
     wl = S.workload_by_name(name)
     plan = R.plan_workload(wl)
     items = R.reshard_plan_items(plan, 6)[0]
-    assert R.reshard_plan_stats(plan)["gather_items"] == len(items)
+    unpack = R.reshard_plan_items(plan, 8)[0]
+    assert R.reshard_plan_stats(plan)["gather_items"] == len(items) + len(unpack)
     if name not in GATHER_EXPECT:
-        assert len(items) == 0, name
+        assert len(items) == 0 and len(unpack) == 0, name
         return
+    # the unpack pass pairs the same rows (pieces read from the received message)
+    es = unpack["esize"].astype(np.int64)
+    assert {(int(a), int(b)) for a, b in zip(unpack["run"][:, 0] * es, unpack["run"][:, 1] * es)} == GATHER_EXPECT[name]
+    assert int(unpack["rows"].sum()) == int(items["rows"].sum())
     es = items["esize"].astype(np.int64)
     got = {(int(a), int(b)) for a, b in zip(items["run"][:, 0] * es, items["run"][:, 1] * es)}
     assert got == GATHER_EXPECT[name]
@@ -281,10 +291,13 @@ def test_gather_items_merge_outer_dims():
     items = R.reshard_plan_items(plan, 6)[0]
     assert int(items["rows"].sum()) == 64 * 3 * 3
     assert len(items) <= 3 * -(-64 * 3 // 8)
+    unpack = R.reshard_plan_items(plan, 8)[0]   # message blocks are dense: their rows merge too
+    assert int(unpack["rows"].sum()) == 64 * 3 * 3 and len(unpack) == len(items)
     lay = S.allocate(wl, "cpu", misalign=2)
     S.fill_sources(wl, lay)
     check_gather_bounds(wl, lay, plan)
     assert np.array_equal(emulate(wl, lay, plan, "direct", gather=True), _oracle(wl, lay))
+    assert np.array_equal(emulate(wl, lay, plan, "packed", gather=True), _oracle(wl, lay))
     # destination shards with a padded outer stride: the outer dim is walked explicitly
     t = wl.tensors[0]
     cols = [334, 333, 333]
@@ -312,4 +325,4 @@ def test_item_tables_fuzzed_layouts():
         want = _oracle(wl, lay)
         for mode in ("direct", "packed"):
             assert np.array_equal(emulate(wl, lay, plan, mode), want), (wl.tensors[0], mode)
-        assert np.array_equal(emulate(wl, lay, plan, "direct", gather=True), want), wl.tensors[0]
+            assert np.array_equal(emulate(wl, lay, plan, mode, gather=True), want), (wl.tensors[0], mode)

@@ -504,11 +504,13 @@ def test_gather_rows_bit_exact(name, misalign):
     if misalign % S.DTYPES[wl.tensors[0].dtype][1]:
         pytest.skip("shift not a multiple of the element size")
     lay, plan = run_gpu(wl, misalign=misalign)
+    n_direct, n_unpack = len(R.reshard_plan_items(plan, 6)[0]), len(R.reshard_plan_items(plan, 8)[0])
     st = R.reshard_plan_stats(plan)
-    assert st["gather_items"] > 0 and st["last_gather_items"] == st["gather_items"]
+    assert n_direct > 0 and st["last_gather_items"] == n_direct and st["gather_items"] == n_direct + n_unpack
     assert_matches_oracle(wl, lay)
-    lay, plan = run_gpu(wl, mode="packed", misalign=misalign, plan=plan)   # plain items, unflagged
-    assert R.reshard_plan_stats(plan)["last_gather_items"] == 0
+    # packed: pack items into messages, then the unpack pass's gather items out of them
+    lay, plan = run_gpu(wl, mode="packed", misalign=misalign, plan=plan)
+    assert n_unpack > 0 and R.reshard_plan_stats(plan)["last_gather_items"] == n_unpack
     assert_matches_oracle(wl, lay)
 
 
@@ -539,7 +541,7 @@ def test_gather_items_carry_the_whole_mesh_reshard():
         wl = S.mesh2d_to_1d(rows=1434, cols=4096, variant=variant)
         lay, plan = run_gpu(wl)
         st = R.reshard_plan_stats(plan)
-        assert st["last_launches"] == 1 and st["last_gather_items"] == st["gather_items"] > 0
+        assert st["last_launches"] == 1 and st["last_gather_items"] == len(R.reshard_plan_items(plan, 6)[0]) > 0
         assert st["last_aligned_items"] + st["last_staged_items"] + st["last_general_items"] == 0
         assert_matches_oracle(wl, lay)
 
