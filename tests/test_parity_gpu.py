@@ -308,20 +308,29 @@ def test_fuzzed_layouts_bit_exact(mode):
         assert_matches_oracle(wl, lay)
 
 
-def test_execute_replays_from_a_cuda_graph():
+@pytest.mark.parametrize("mode", ["direct", "packed"])
+@pytest.mark.parametrize("name", ["dense", "mesh_gather", "transposed"])
+def test_execute_replays_from_a_cuda_graph(name, mode):
     """Once a plan has run with some pointers, executes with the same pointers only launch
-    kernels, so they can be captured into a CUDA graph and replayed."""
-    wl = S.dense_ffn(layers=1, hidden=256, ffn=1024)
-    lay, plan = run_gpu(wl)                      # binds the plan and uploads its tables
+    kernels, so they can be captured into a CUDA graph and replayed: aligned items, gather items
+    (direct and unpack passes, their resolved tables already uploaded) and TMA transposes."""
+    wl = {"dense": lambda: S.dense_ffn(layers=1, hidden=256, ffn=1024),
+          "mesh_gather": lambda: S.mesh2d_to_1d(rows=1434, cols=4096, variant="2d"),
+          "transposed": lambda: S.transposed(shape=(300, 256), src_mesh=(4,), src_pl=("S0",))}[name]()
+    lay, plan = run_gpu(wl, mode=mode)           # binds the plan and uploads its tables
     S.fill_canary(lay)
     sp, dp = R.workload_pointers(wl, lay)
     s = torch.cuda.Stream()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
-        R.reshard_execute(plan, sp, dp, stream=s.cuda_stream)
-    g.replay()
+        R.reshard_execute(plan, sp, dp, mode=mode, stream=s.cuda_stream)
+    for _ in range(2):
+        g.replay()
     torch.cuda.synchronize()
+    assert R.reshard_plan_status(plan) == 0
     assert_matches_oracle(wl, lay)
+    if name == "mesh_gather":
+        assert R.reshard_plan_stats(plan)["last_gather_items"] > 0
 
 
 def _pinned_like(t, fill=None):
