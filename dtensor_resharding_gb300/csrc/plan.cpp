@@ -559,12 +559,14 @@ const int64_t *region_dest(const reshard_plan &p, const Region &r, const Group &
   return dv.strides;
 }
 
-// Pairs of direct regions that form whole destination rows together: same tensor and device
-// group, the same box but for the last dim, where region A ends at region B's start; the last
-// dim contiguous on both sources and the destination, at least two elements of each piece and
-// two rows. Only rows misaligned by construction pair up (the destination pitch or piece A's
-// length is not a multiple of 16 bytes), where the two plain items would each be walked as
-// short rows. partner[A] = B, partner[B] = -2 - A, -1 for an unpaired region.
+// Pairs of regions of one pass (direct or unpack) that form whole destination rows together:
+// same tensor and device group in that pass, the same box but for the last dim, where region A
+// ends at region B's start; the last dim contiguous on both sources (message blocks always are)
+// and the destination, at least two elements of each piece and two rows. Only rows misaligned by
+// construction pair up (the destination pitch or piece A's length is not a multiple of 16
+// bytes), where the two plain items would each be walked as short rows. Rows of three or more
+// pieces pair consecutive pieces two by two; an odd last piece stays plain. partner[A] = B,
+// partner[B] = -2 - A, -1 for an unpaired region.
 std::vector<int64_t> gather_pairs(const reshard_plan &p, const std::vector<Role> &roles,
                                   const std::vector<Group> &dev_groups, int set) {
   std::vector<int64_t> partner(p.regions.size(), -1);
@@ -608,14 +610,15 @@ std::vector<int64_t> gather_pairs(const reshard_plan &p, const std::vector<Role>
       if (row_b > INT32_MAX) continue;
       partner[v[k]] = (int64_t)v[k + 1];
       partner[v[k + 1]] = -2 - (int64_t)v[k];
-      ++k;  // rows of three or more pieces: the first two pair, the rest stay plain
+      ++k;  // the next pair starts after piece B
     }
   }
   return partner;
 }
 
-// Gather items of the pair (a, b): the rows dim is the last but one, outer dims are walked
-// explicitly, and each item moves about kGatherItemBytes (read + written over all replicas) in a
+// Gather items of the pair (a, b) in pass `set`: the rows dim is the last but one (outer dims
+// merge into it while both sources and the destination step uniformly over them, and are walked
+// explicitly otherwise), and each item moves about kGatherItemBytes (read + written over all replicas) in a
 // multiple of 8 rows, one or more per warp of the CTA that takes it (measured on the (2,4) ->
 // (3,) / (3,2) mesh reshards: 16 rows of 2,732 bytes with one replica, 8 with two, against
 // 0.78-0.83 of the copy rate for items of about item_bytes of source).
