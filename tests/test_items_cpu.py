@@ -280,6 +280,26 @@ def test_gather_pairs_follow_the_alignment_rule():
     assert int(items2["rows"].sum()) == 64 * 3
 
 
+@pytest.mark.parametrize("ns,nd,per_row", [(8, 2, 4), (9, 3, 3)])
+def test_gather_pairs_rows_of_more_pieces(ns, nd, per_row):
+    """Rows of four pieces form two gather pairs; rows of three form one pair and keep the last
+    piece as a plain item. Both emulate to the oracle."""
+    from test_parity_gpu import _split
+    wl = _split((64, ns * 111), ns, nd)
+    plan = R.plan_workload(wl)
+    items = R.reshard_plan_items(plan, 6)[0]
+    plain = R.reshard_plan_items(plan, DIRECT)[0]
+    pairs = per_row // 2
+    assert int(items["rows"].sum()) == 64 * nd * pairs
+    unflagged = plain[plain["pad"][:, 0] == 0]
+    assert int((unflagged["rows"].astype(np.int64) * unflagged["run"]).sum()) == 64 * nd * (per_row % 2) * 111
+    lay = S.allocate(wl, "cpu", misalign=2)
+    S.fill_sources(wl, lay)
+    check_gather_bounds(wl, lay, plan)
+    for mode in ("direct", "packed"):
+        assert np.array_equal(emulate(wl, lay, plan, mode, gather=True), _oracle(wl, lay))
+
+
 def test_gather_items_merge_outer_dims():
     """A 3-D column split whose middle dim is short: outer dims merge into the gather items' rows
     when both sources and the destination step uniformly over them (64 x 3 rows per pair, not 64

@@ -500,6 +500,8 @@ GATHER_CASES = {
     "four_dims_merged": lambda: _split((2, 3, 20, 1000), 4, 3),
     "outer_stride_padded": lambda: _split_padded_outer((16, 3, 1000), 4, 3),
     "long_rows": lambda: _split((16, 40000), 4, 3, reps=2),              # 26.7 KB rows
+    "rows_of_four_pieces": lambda: _split((64, 888), 8, 2),              # two pairs per row
+    "rows_of_three_pieces": lambda: _split((64, 999), 9, 3, reps=2),     # a pair and a plain piece
 }
 
 
