@@ -235,7 +235,9 @@ int reshard_plan_blockwise_fp8(const reshard_tensor_spec_t *specs, int n_tensors
  * and the rest (run by the general walker), and the gather items (destination rows of two
  * source pieces, reshard_plan_items sets 6 and 8; run by the gather kernel in passes without
  * quantization) are resolved to absolute addresses and re-uploaded on `stream`: host work
- * proportional to the plan's items, none when the pointers repeat.
+ * proportional to the plan's items, none when the pointers repeat. Those uploads copy from the
+ * plan's host tables, so an execute captured into a CUDA graph should repeat the pointers of an
+ * execute made before the capture (it then enqueues kernel launches only).
  * Buffers must stay valid until the stream reaches the end of the work. Executes of one plan
  * on different streams that overlap in time race on its tables and workspace.
  * Errors: INVALID_ARG (NULL pointer of a shard the plan reads or writes, a pointer the device
