@@ -176,7 +176,7 @@ def _rank_main(rank, world, port, combos, out):
 
 
 def _run(world, combos):
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_rank_main, args=(world, _free_port(), combos, out), nprocs=world, join=True)
         return dict(out)

@@ -40,7 +40,7 @@ def _rank(rank, world, port, out):
 
 def test_two_gloo_ranks_replicas():
     world = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_rank, args=(world, _free_port(), out), nprocs=world, join=True)
         res = dict(out)
