@@ -522,15 +522,17 @@ TITEM_DTYPE = [("src_off", "<i8"), ("dst_off", "<i8"), ("src_pitch", "<i8"), ("d
                ("slab", "<i4"), ("x", "<i4"), ("y", "<i4")]
 
 
-GITEM_DTYPE = [("src_off", "<i8", (2,)), ("src_pitch", "<i8", (2,)), ("dst_off", "<i8"), ("dst_pitch", "<i8"),
-               ("run", "<i4", (2,)), ("src", "<i4", (2,)), ("rows", "<i4"), ("group", "<i4"), ("esize", "<i4"),
-               ("pad", "<i4")]
+GITEM_DTYPE = [("src_off", "<i8", (2,)), ("src_pitch", "<i8", (2,)), ("dst_off", "<i8", (2,)),
+               ("dst_pitch", "<i8", (2,)), ("run", "<i4", (2,)), ("src", "<i4", (2,)), ("rows", "<i4"),
+               ("group", "<i4"), ("esize", "<i4"), ("kind", "<i4")]
 
 
 def reshard_plan_items(plan: Plan, which: int = 0):
     """(items as a numpy structured array, group_start, member_ptr, member_off) of one table:
     0/1/2 strided-copy items of the direct/pack/unpack pass, 3/4/5 their transposing items, 6/7/8
-    their gather items (copy items they cover have pad[0] == 1; the pack pass has none)."""
+    their pair items (kind 0: a destination row of two source pieces, direct and unpack passes;
+    kind 1: a source row into two message blocks, pack pass; copy items they cover have
+    pad[0] == 1)."""
     import numpy as np
     n, ng, nm = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
     _check(LIB.reshard_plan_items(plan.handle, which, 0, None, ctypes.byref(n), None, None, None,

@@ -560,7 +560,7 @@ __global__ void __launch_bounds__(kBlock, RESHARD_GATHER_MIN_BLOCKS) reshard_cop
     const uint8_t *s0 = reinterpret_cast<const uint8_t *>(it.src[0]);
     const uint8_t *s1 = reinterpret_cast<const uint8_t *>(it.src[1]);
     const int B = it.B, rb = it.rb, rows = it.rows, nrep = it.nrep;
-    const int64_t sp0 = it.sp[0], sp1 = it.sp[1], dp = it.dp;
+    const int64_t sp0 = it.sp[0], sp1 = it.sp[1], dp = it.dp[0];
     for (int f0 = 0; f0 < nrep; f0 += 2) {
       const int nf = min(2, nrep - f0);
       uint8_t *dst[2];
@@ -583,6 +583,92 @@ __global__ void __launch_bounds__(kBlock, RESHARD_GATHER_MIN_BLOCKS) reshard_cop
         }
       }
     }
+    __syncthreads();  // everyone is done with s_item[buf]; s_item[buf ^ 1] is complete
+  }
+  if (wait_last) pdl_enter();
+}
+
+// One source row split into two destination rows (the pack pass's scatter items): row bytes
+// [0, B) go to d0, bytes [B, rb) to d1, each destination on its own 16-byte word grid. The warp
+// walks piece 0's destination words, then piece 1's; each word is one or two 16-byte block
+// loads of the source row and a funnel shift by that piece's phase, as in gather_row.
+template <int RU>
+__device__ __forceinline__ void scatter_row(const uint8_t *s, int B, int rb, uint8_t *d0, uint8_t *d1, int lane) {
+  const int a0 = (int)(reinterpret_cast<uintptr_t>(d0) & 15), a1 = (int)(reinterpret_cast<uintptr_t>(d1) & 15);
+  const int len1 = rb - B;
+  const int nw0 = (a0 + B + 15) >> 4;               // piece 0's destination words
+  const int nv = nw0 + ((a1 + len1 + 15) >> 4);     // ... and piece 1's
+  const uintptr_t p0 = reinterpret_cast<uintptr_t>(s) - a0;      // source of piece 0's word 0, byte 0
+  const uintptr_t p1 = reinterpret_cast<uintptr_t>(s) + B - a1;  // ... piece 1's
+  const int sh0 = (int)(p0 & 15), sh1 = (int)(p1 & 15);
+  for (int v0 = lane; v0 < nv; v0 += 32 * RU) {
+    uint4 lo[RU], hi[RU];
+    int kmin[RU], kmax[RU], sh[RU], pos[RU];  // pos: 2 x (piece byte of the word's byte 0) + piece
+#pragma unroll
+    for (int u = 0; u < RU; ++u) {
+      const int v = v0 + 32 * u;
+      kmin[u] = 16;
+      kmax[u] = 0;
+      sh[u] = 0;
+      pos[u] = 0;
+      lo[u] = make_uint4(0, 0, 0, 0);
+      hi[u] = make_uint4(0, 0, 0, 0);
+      if (v < nv) {
+        const bool second = v >= nw0;
+        const int w = second ? v - nw0 : v;
+        const int a = second ? a1 : a0, len = second ? len1 : B;
+        const int st = 16 * w - a;  // piece byte of the word's byte 0
+        kmin[u] = max(-st, 0);
+        kmax[u] = min(len - st, 16);
+        sh[u] = second ? sh1 : sh0;
+        pos[u] = 2 * st + (second ? 1 : 0);
+        const uint8_t *blk = reinterpret_cast<const uint8_t *>((second ? p1 : p0) - sh[u]) + 16 * w;
+        if (kmin[u] < 16 - sh[u]) lo[u] = __ldg(reinterpret_cast<const uint4 *>(blk));
+        if (sh[u] && kmax[u] > 16 - sh[u]) hi[u] = __ldg(reinterpret_cast<const uint4 *>(blk + 16));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < RU; ++u) {
+      if (kmin[u] >= kmax[u]) continue;
+      const uint4 o = sh[u] ? shift_bytes(lo[u], hi[u], sh[u]) : lo[u];
+      uint8_t *dw = ((pos[u] & 1) ? d1 : d0) + (pos[u] >> 1);
+      if (kmin[u] == 0 && kmax[u] == 16)
+        store_stream(dw, o);
+      else
+        store_partial(dw, o, kmin[u], kmax[u]);
+    }
+  }
+}
+
+// Scatter items of the pack pass (one destination, the send buffer): dealt like the gather
+// kernel's items, the rows of an item to the CTA's warps in turn.
+#ifndef RESHARD_SCATTER_MIN_BLOCKS
+#define RESHARD_SCATTER_MIN_BLOCKS RESHARD_GATHER_MIN_BLOCKS
+#endif
+__global__ void __launch_bounds__(kBlock, RESHARD_SCATTER_MIN_BLOCKS) reshard_copy_scatter_kernel(
+    const GBound *__restrict__ items, int n_items, int wait_last) {
+  if (!wait_last) pdl_enter();
+  __shared__ GBound s_item[2];
+  constexpr int kWords = (int)(sizeof(GBound) / sizeof(uint32_t));
+  if (threadIdx.x < kWords && blockIdx.x < n_items)
+    reinterpret_cast<uint32_t *>(&s_item[0])[threadIdx.x] =
+        __ldg(reinterpret_cast<const uint32_t *>(items + blockIdx.x) + threadIdx.x);
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int buf = 0;
+  for (int k = blockIdx.x; k < n_items; k += gridDim.x, buf ^= 1) {
+    pdl_last_item(k, n_items);
+    if (threadIdx.x < kWords && k + (int)gridDim.x < n_items)
+      reinterpret_cast<uint32_t *>(&s_item[buf ^ 1])[threadIdx.x] =
+          __ldg(reinterpret_cast<const uint32_t *>(items + k + gridDim.x) + threadIdx.x);
+    const GBound &it = s_item[buf];
+    const uint8_t *s = reinterpret_cast<const uint8_t *>(it.src[0]);
+    uint8_t *d0 = reinterpret_cast<uint8_t *>(it.dst[0]);
+    uint8_t *d1 = reinterpret_cast<uint8_t *>(it.dst[1]);
+    const int B = it.B, rb = it.rb, rows = it.rows;
+    const int64_t sp = it.sp[0], dp0 = it.dp[0], dp1 = it.dp[1];
+    for (int r = warp; r < rows; r += kBlock / 32)
+      scatter_row<RESHARD_GATHER_UNROLL>(s + r * sp, B, rb, d0 + r * dp0, d1 + r * dp1, lane);
     __syncthreads();  // everyone is done with s_item[buf]; s_item[buf ^ 1] is complete
   }
   if (wait_last) pdl_enter();
@@ -1537,6 +1623,7 @@ struct LaunchCaps {
   int copy_grid = 0;
   int rows_grid = 0;
   int gather_grid = 0;
+  int scatter_grid = 0;
   int staged_grid = 0;
   int mxfp8_grid = 0;
   int transpose_grid[4] = {0, 0, 0, 0};  // per element size 1, 2, 4, 8 bytes
@@ -1558,8 +1645,9 @@ int launch_caps(int device, LaunchCaps &c) {
   }
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, reshard_copy_kernel, kBlock, 0));
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b4, reshard_copy_rows_kernel, kBlock, 0));
-  int bg = 0;
+  int bg = 0, bsc = 0;
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bg, reshard_copy_gather_kernel, kBlock, 0));
+  RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bsc, reshard_copy_scatter_kernel, kBlock, 0));
   int bs = 0;
   RS_CUDA(cudaFuncSetAttribute(reshard_copy_staged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStagedSmem));
   RS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bs, reshard_copy_staged_kernel, kBlock, kStagedSmem));
@@ -1575,6 +1663,7 @@ int launch_caps(int device, LaunchCaps &c) {
   g_caps.copy_grid = sms * std::max(1, b1);
   g_caps.rows_grid = sms * std::max(1, b4);
   g_caps.gather_grid = sms * std::max(1, bg);
+  g_caps.scatter_grid = sms * std::max(1, bsc);
   g_caps.staged_grid = sms * std::max(1, bs);
   g_caps.mxfp8_grid = sms * std::max(1, b2);
   for (int k = 0; k < 4; ++k) g_caps.transpose_grid[k] = sms * std::max(1, bt[k]);
@@ -1840,18 +1929,23 @@ int bind_gather(reshard_plan_t *p, int set, cudaStream_t stream) {
       b.sp[k] = g.src_pitch[k] * (int64_t)es;
     }
     for (int f = 0; f < 2; ++f) {
-      const int32_t m = m0 + (f < nrep ? f : 0);
-      b.dst[f] = tab[(size_t)p->mem_ptr[(size_t)m]] + (uint64_t)(p->mem_off[(size_t)m] + g.dst_off) * es;
+      if (g.kind == kScatterRow) {  // piece f's row 0 in the group's one member (the send buffer)
+        b.dst[f] = tab[(size_t)p->mem_ptr[(size_t)m0]] + (uint64_t)(p->mem_off[(size_t)m0] + g.dst_off[f]) * es;
+      } else {                      // row 0 in replica f
+        const int32_t m = m0 + (f < nrep ? f : 0);
+        b.dst[f] = tab[(size_t)p->mem_ptr[(size_t)m]] + (uint64_t)(p->mem_off[(size_t)m] + g.dst_off[0]) * es;
+      }
+      b.dp[f] = g.dst_pitch[f] * (int64_t)es;
     }
-    b.dp = g.dst_pitch * (int64_t)es;
-    b.dst_off_b = g.dst_off * (int64_t)es;
+    b.dst_off_b = g.dst_off[0] * (int64_t)es;
     b.B = g.run[0] * g.esize;
     b.rb = b.B + g.run[1] * g.esize;
     b.rows = g.rows;
     b.group = g.group;
     b.nrep = nrep;
     b.esize = g.esize;
-    b.pad[0] = b.pad[1] = 0;
+    b.kind = g.kind;
+    b.pad = 0;
   }
   if (!p->d_gbound[set]) RS_CUDA(cudaMalloc(&p->d_gbound[set], n * sizeof(GBound)));
   RS_CUDA(cudaMemcpyAsync(p->d_gbound[set], bound.data(), n * sizeof(GBound), cudaMemcpyHostToDevice, stream));
@@ -1913,9 +2007,13 @@ int launch(reshard_plan_t *p, int set, bool quant, cudaStream_t stream, const La
     if (nx > 0) {
       if ((rc = bind_gather(p, set, stream))) return rc;
       const int wait_gather = RESHARD_GEN_OVERLAP && na + ns + ng > 0 ? 1 : 0;
-      RS_CUDA(launch_kernel(true, reshard_copy_gather_kernel, std::min(nx, caps.gather_grid), kBlock, 0, stream,
-                            static_cast<const GBound *>(p->d_gbound[set]), nx, p->d_ptrs, p->d_grp_start, p->d_mem_ptr,
-                            p->d_mem_off, wait_gather));
+      const GBound *gb = static_cast<const GBound *>(p->d_gbound[set]);
+      if (set == kPack)
+        RS_CUDA(launch_kernel(true, reshard_copy_scatter_kernel, std::min(nx, caps.scatter_grid), kBlock, 0, stream, gb,
+                              nx, wait_gather));
+      else
+        RS_CUDA(launch_kernel(true, reshard_copy_gather_kernel, std::min(nx, caps.gather_grid), kBlock, 0, stream, gb,
+                              nx, p->d_ptrs, p->d_grp_start, p->d_mem_ptr, p->d_mem_off, wait_gather));
       ++p->last_launches;
     }
   }

@@ -200,6 +200,26 @@ void side_layout(const reshard_tensor_spec_t &s, bool src, TensorInfo &t, const 
       }
     }
     const int64_t vol = volume(b, s.ndim);
+    // a destination's elements must have distinct offsets (else what it receives depends on
+    // the order of the writes): taken by increasing stride, every dim's stride must pass the
+    // span of the dims below it (views interleaving two dims otherwise are refused too)
+    if (!src && !w.dense && vol > 1) {
+      int order[kMaxDims], k = 0;
+      for (int d = 0; d < s.ndim; ++d)
+        if (ext[d] > 1) order[k++] = d;
+      std::sort(order, order + k, [&](int x, int y) { return w.strides[x] < w.strides[y]; });
+      int64_t span = 0;
+      for (int q = 0; q < k; ++q) {
+        const int d = order[q];
+        if (w.strides[d] <= span) {
+          v.add(RESHARD_ERR_INVALID_ARG, pre + side + " view " + std::to_string(p) + " maps two elements to one offset (stride " +
+                                             std::to_string(w.strides[d]) + " of dim " + std::to_string(d) +
+                                             " within the span of the smaller strides)");
+          break;
+        }
+        span += w.strides[d] * (ext[d] - 1);
+      }
+    }
     if (capacity > 0 && vol > 0) {
       int64_t last = w.offset;
       for (int d = 0; d < s.ndim; ++d) last += (ext[d] - 1) * w.strides[d];
@@ -559,6 +579,50 @@ const int64_t *region_dest(const reshard_plan &p, const Region &r, const Group &
   return dv.strides;
 }
 
+// Pack-pass pairs: regions read from the same source shard with the same box but for the last
+// dim, region A ending where region B starts, both packed into messages (the send buffer), the
+// last dim contiguous in the source, at least two elements of each piece and two rows: one
+// source row feeds two message blocks. Only rows misaligned by construction pair up (a piece's
+// bytes per row not a multiple of 16: its dense message rows are then misaligned). Same encoding
+// of partner[] as gather_pairs.
+std::vector<int64_t> scatter_pairs(const reshard_plan &p, const std::vector<Role> &roles) {
+  std::vector<int64_t> partner(p.regions.size(), -1);
+  std::map<std::vector<int64_t>, std::vector<size_t>> rows_of;
+  for (size_t i = 0; i < p.regions.size(); ++i) {
+    const Region &r = p.regions[i];
+    const TensorInfo &t = p.tensors[(size_t)r.tensor];
+    const int nd = t.ndim, last = nd - 1;
+    if (roles[i].send_off < 0 || nd < 2) continue;
+    if (r.box.hi[last] - r.box.lo[last] < 2 || r.box.hi[last - 1] - r.box.lo[last - 1] < 2) continue;
+    if (t.src_view[(size_t)r.src].strides[last] != 1) continue;
+    std::vector<int64_t> key{r.tensor, r.src};
+    for (int d = 0; d < last; ++d) {
+      key.push_back(r.box.lo[d]);
+      key.push_back(r.box.hi[d]);
+    }
+    rows_of[key].push_back(i);
+  }
+  for (auto &kv : rows_of) {
+    std::vector<size_t> &v = kv.second;
+    if (v.size() < 2) continue;
+    const TensorInfo &t = p.tensors[(size_t)p.regions[v[0]].tensor];
+    const int last = t.ndim - 1;
+    std::sort(v.begin(), v.end(), [&](size_t a, size_t b) { return p.regions[a].box.lo[last] < p.regions[b].box.lo[last]; });
+    for (size_t k = 0; k + 1 < v.size(); ++k) {
+      const Region &a = p.regions[v[k]], &b = p.regions[v[k + 1]];
+      if (a.box.hi[last] != b.box.lo[last]) continue;
+      const int64_t len_a = (a.box.hi[last] - a.box.lo[last]) * t.esize;
+      const int64_t len_b = (b.box.hi[last] - b.box.lo[last]) * t.esize;
+      if (len_a % 16 == 0 && len_b % 16 == 0) continue;
+      if (len_a + len_b > INT32_MAX) continue;
+      partner[v[k]] = (int64_t)v[k + 1];
+      partner[v[k + 1]] = -2 - (int64_t)v[k];
+      ++k;  // the next pair starts after piece B
+    }
+  }
+  return partner;
+}
+
 // Pairs of regions of one pass (direct or unpack) that form whole destination rows together:
 // same tensor and device group in that pass, the same box but for the last dim, where region A
 // ends at region B's start; the last dim contiguous on both sources (message blocks always are)
@@ -571,6 +635,7 @@ std::vector<int64_t> gather_pairs(const reshard_plan &p, const std::vector<Role>
                                   const std::vector<Group> &dev_groups, int set) {
   std::vector<int64_t> partner(p.regions.size(), -1);
   if (!RESHARD_GATHER) return partner;
+  if (set == kPack) return scatter_pairs(p, roles);
   // the region's destination group in this pass (the unpack pass reads dense message blocks,
   // contiguous along the last dim by construction)
   auto group_of = [&](size_t i) { return set == kDirect ? roles[i].direct : roles[i].unpack; };
@@ -624,72 +689,85 @@ std::vector<int64_t> gather_pairs(const reshard_plan &p, const std::vector<Role>
 // 0.78-0.83 of the copy rate for items of about item_bytes of source).
 void emit_gather(reshard_plan &p, size_t a, size_t b, const std::vector<Role> &roles, const std::vector<Group> &dev_groups,
                  int64_t item_bytes, int set) {
-  const Region &ra = p.regions[a], &rb = p.regions[b];
+  const Region &ra = p.regions[a];
   const TensorInfo &t = p.tensors[(size_t)ra.tensor];
   const int nd = t.ndim, last = nd - 1, rd = nd - 2;
-  const int32_t dg = set == kDirect ? roles[a].direct : roles[a].unpack;
+  const int32_t dg = set == kDirect ? roles[a].direct : set == kUnpack ? roles[a].unpack : p.workspace_group;
   int64_t ext[kMaxDims];
   for (int d = 0; d < nd; ++d) ext[d] = ra.box.hi[d] - ra.box.lo[d];
-  const int64_t len[2] = {ext[last], rb.box.hi[last] - rb.box.lo[last]};
-  // each piece's source: its source shard (direct), or its dense block of the received message
-  // (unpack: row-major over the region's extents, at the region's byte offset recv_off)
-  int64_t so[2], sst[2][kMaxDims];
+  const int64_t len[2] = {ext[last], p.regions[b].box.hi[last] - p.regions[b].box.lo[last]};
+  // dense row-major strides of a piece's message block (its region's extents)
+  auto dense = [&](int q, int64_t *st) {
+    int64_t acc = 1;
+    for (int d = nd - 1; d >= 0; --d) {
+      st[d] = acc;
+      acc *= d == last ? len[q] : ext[d];
+    }
+  };
+  // each piece's source: its source shard (direct, pack), or its dense block of the received
+  // message (unpack: at the region's byte offset recv_off); its destination: the replica group's
+  // row (direct, unpack), or its dense block of the outgoing message (pack: at send_off)
+  int64_t so[2], sst[2][kMaxDims], dof[2], dst_st[2][kMaxDims];
   int32_t sptr[2];
   for (int q = 0; q < 2; ++q) {
     const size_t ri = q ? b : a;
     const Region &r = p.regions[ri];
-    if (set == kDirect) {
+    if (set == kUnpack) {
+      so[q] = roles[ri].recv_off / t.esize;
+      dense(q, sst[q]);
+      sptr[q] = (int32_t)(p.workspace_ptr + 1);
+    } else {
       const RankView &v = region_source(p, r, so[q]);
       for (int d = 0; d < nd; ++d) sst[q][d] = v.strides[d];
       sptr[q] = (int32_t)(t.src_base + r.src);
+    }
+    if (set == kPack) {
+      dof[q] = roles[ri].send_off / t.esize;
+      dense(q, dst_st[q]);
     } else {
-      so[q] = roles[ri].recv_off / t.esize;
-      int64_t acc = 1;
-      for (int d = nd - 1; d >= 0; --d) {
-        sst[q][d] = acc;
-        acc *= d == last ? len[q] : ext[d];
-      }
-      sptr[q] = (int32_t)(p.workspace_ptr + 1);
+      const int64_t *ds = region_dest(p, r, dev_groups[(size_t)dg], dof[q]);
+      for (int d = 0; d < nd; ++d) dst_st[q][d] = ds[d];
     }
   }
-  int64_t dof;
-  const int64_t *ds = region_dest(p, ra, dev_groups[(size_t)dg], dof);
   const int64_t row_b = (len[0] + len[1]) * t.esize;
-  const int64_t nrep = (int64_t)dev_groups[(size_t)dg].members.size();
+  const int64_t nrep = set == kPack ? 1 : (int64_t)dev_groups[(size_t)dg].members.size();
   int64_t per = kGatherItemBytes / (row_b * (1 + nrep)) / kGatherRowStep * kGatherRowStep;
   per = std::min(std::max(per, kGatherRowStep), std::max<int64_t>(1, item_bytes / row_b));
-  // outer dims merge into the rows dim while both sources and the destination step uniformly
-  // over them (as the plain items' rows do); the rest are walked explicitly
+  // outer dims merge into the rows dim while both pieces' sources and destinations step
+  // uniformly over them (as the plain items' rows do); the rest are walked explicitly
   int64_t rows = ext[rd];
   int k = rd - 1;
-  while (k >= 0 && (ext[k] == 1 || (sst[0][k] == rows * sst[0][rd] && sst[1][k] == rows * sst[1][rd] &&
-                                    ds[k] == rows * ds[rd]))) {
+  auto uniform = [&](int d) {
+    for (int q = 0; q < 2; ++q)
+      if (sst[q][d] != rows * sst[q][rd] || dst_st[q][d] != rows * dst_st[q][rd]) return false;
+    return true;
+  };
+  while (k >= 0 && (ext[k] == 1 || uniform(k))) {
     rows *= ext[k];
     --k;
   }
   int64_t idx[kMaxDims] = {0, 0, 0, 0};
   for (;;) {
-    int64_t s0[2] = {so[0], so[1]}, d0 = dof;
-    for (int d = 0; d <= k; ++d) {
-      s0[0] += idx[d] * sst[0][d];
-      s0[1] += idx[d] * sst[1][d];
-      d0 += idx[d] * ds[d];
-    }
+    int64_t s0[2] = {so[0], so[1]}, d0[2] = {dof[0], dof[1]};
+    for (int d = 0; d <= k; ++d)
+      for (int q = 0; q < 2; ++q) {
+        s0[q] += idx[d] * sst[q][d];
+        d0[q] += idx[d] * dst_st[q][d];
+      }
     for (int64_t r = 0; r < rows; r += per) {
       GItem g{};
       g.rows = (int32_t)std::min(per, rows - r);
-      g.src_off[0] = s0[0] + r * sst[0][rd];
-      g.src_off[1] = s0[1] + r * sst[1][rd];
-      g.src_pitch[0] = sst[0][rd];
-      g.src_pitch[1] = sst[1][rd];
-      g.dst_off = d0 + r * ds[rd];
-      g.dst_pitch = ds[rd];
-      g.run[0] = (int32_t)len[0];
-      g.run[1] = (int32_t)len[1];
-      g.src[0] = sptr[0];
-      g.src[1] = sptr[1];
+      for (int q = 0; q < 2; ++q) {
+        g.src_off[q] = s0[q] + r * sst[q][rd];
+        g.src_pitch[q] = sst[q][rd];
+        g.dst_off[q] = d0[q] + r * dst_st[q][rd];
+        g.dst_pitch[q] = dst_st[q][rd];
+        g.run[q] = (int32_t)len[q];
+        g.src[q] = sptr[q];
+      }
       g.group = dg;
       g.esize = t.esize;
+      g.kind = set == kPack ? kScatterRow : kGatherRow;
       p.gitems[set].push_back(g);
     }
     int d = k;
@@ -734,6 +812,7 @@ int emit_tables(reshard_plan *plan, const std::vector<Role> &roles, const std::v
   std::map<SlabSpec, int32_t> slab_ids;
   const std::vector<int64_t> partner = gather_pairs(*plan, roles, dev_groups, kDirect);
   const std::vector<int64_t> partner_u = gather_pairs(*plan, roles, dev_groups, kUnpack);
+  const std::vector<int64_t> partner_p = gather_pairs(*plan, roles, dev_groups, kPack);
   for (auto &gv : plan->gitems) gv.clear();
   for (size_t i = 0; i < plan->regions.size(); ++i) {
     const Region &r = plan->regions[i];
@@ -782,8 +861,12 @@ int emit_tables(reshard_plan *plan, const std::vector<Role> &roles, const std::v
     }
     if (role.send_off >= 0) {
       const int64_t mo = role.send_off / t.esize;
+      const size_t n0 = plan->items[kPack].size();
       emit_region(nd, ext, so, sv.strides, from_src, mo, ms, plan->workspace_group, t.esize, item_bytes,
                   plan->items[kPack], plan->titems[kPack], slab_ids, plan->slabs);
+      if (partner_p[i] != -1)
+        for (size_t k = n0; k < plan->items[kPack].size(); ++k) plan->items[kPack][k].pad[0] = kGathered;
+      if (partner_p[i] >= 0) emit_gather(*plan, i, (size_t)partner_p[i], roles, dev_groups, item_bytes, kPack);
     }
     if (role.unpack >= 0) {
       const int64_t mo = role.recv_off / t.esize;
@@ -846,7 +929,7 @@ int emit_tables(reshard_plan *plan, const std::vector<Role> &roles, const std::v
   st.n_tensors = (int64_t)plan->tensors.size();
   st.regions = (int64_t)plan->regions.size();
   st.items = (int64_t)(plan->items[kDirect].size() + plan->titems[kDirect].size());
-  st.gather_items = (int64_t)(plan->gitems[kDirect].size() + plan->gitems[kUnpack].size());
+  st.gather_items = (int64_t)(plan->gitems[kDirect].size() + plan->gitems[kPack].size() + plan->gitems[kUnpack].size());
   st.dst_groups = (int64_t)plan->groups.size();
   st.gather_bcast_bytes = 2 * global_bytes;
   st.global_bytes = global_bytes;
@@ -854,7 +937,7 @@ int emit_tables(reshard_plan *plan, const std::vector<Role> &roles, const std::v
   st.world = plan->world;
   if ((int64_t)(plan->items[kDirect].size() + plan->items[kPack].size() + plan->items[kUnpack].size() +
                 plan->titems[kDirect].size() + plan->titems[kPack].size() + plan->titems[kUnpack].size() +
-                plan->gitems[kDirect].size() + plan->gitems[kUnpack].size()) > INT32_MAX ||
+                plan->gitems[kDirect].size() + plan->gitems[kPack].size() + plan->gitems[kUnpack].size()) > INT32_MAX ||
       (int64_t)plan->mem_ptr.size() > INT32_MAX || (int64_t)plan->slabs.size() > INT32_MAX ||
       pointer_table_size(plan) > INT32_MAX) {
     return fail(RESHARD_ERR_UNSUPPORTED, "plan too large (more than 2^31 items, members or pointers)");

@@ -91,46 +91,54 @@ static_assert(sizeof(TItem) == 64, "transposing item is one 64-byte descriptor")
 constexpr int64_t kGatherItemBytes = RESHARD_GATHER_ITEM_KIB * 1024;
 constexpr int64_t kGatherRowStep = 8;
 
-// Gather item of the direct or unpack pass: `rows` destination rows each made of two pieces that
-// sit side by side along the destination's contiguous dim, piece 0's `run[0]` elements then piece
-// 1's `run[1]`. Row i of piece p is read at src_off[p] + i * src_pitch[p] of pointer src[p] (a
-// source shard in the direct pass, the receive buffer in the unpack pass); row i of destination
-// replica m starts at member_offset[m] + dst_off + i * dst_pitch of that member's pointer. It
-// replaces the plain items of its two regions, which stay in the pass's table flagged kGathered
-// (the MXFP8 passes and the allocation-free entry point walk the plain items).
+// Pair item: `rows` rows of two pieces, walked together by one warp. Row i of piece p is
+// run[p] elements read at src_off[p] + i * src_pitch[p] of pointer src[p] and written at
+// member_offset[m] + dst_off[p] + i * dst_pitch[p] of every member m of `group`.
+//   kGatherRow (direct and unpack passes): one destination row made of two source pieces side by
+//     side (dst_off[1] = dst_off[0] + run[0], dst_pitch[1] = dst_pitch[0]); the sources are two
+//     source shards in the direct pass, two message blocks of the receive buffer in the unpack
+//     pass.
+//   kScatterRow (pack pass): one source row split into two message blocks (src[1] = src[0],
+//     src_off[1] = src_off[0] + run[0]); the group is the send buffer's.
+// A pair item replaces the plain items of its two regions, which stay in the pass's table
+// flagged kGathered (the MXFP8 passes and the allocation-free entry point walk the plain items).
+constexpr int32_t kGatherRow = 0;
+constexpr int32_t kScatterRow = 1;
 struct alignas(16) GItem {
   int64_t src_off[2];
   int64_t src_pitch[2];
-  int64_t dst_off;
-  int64_t dst_pitch;
+  int64_t dst_off[2];
+  int64_t dst_pitch[2];
   int32_t run[2];
   int32_t src[2];
   int32_t rows;
   int32_t group;
   int32_t esize;
-  int32_t pad;
+  int32_t kind;
 };
-static_assert(sizeof(GItem) == 80, "gather item is one 80-byte descriptor");
+static_assert(sizeof(GItem) == 96, "pair item is one 96-byte descriptor");
 
-// A gather item with its addresses resolved for the current pointer table (built on the host
-// whenever the table changes, so the kernel follows no pointer table): row 0 of both pieces and
-// of the first two replicas, pitches and lengths in bytes. Replicas past the second are looked up
-// through the group table, at member_offset * esize + dst_off_b of each member's pointer.
+// A pair item with its addresses resolved for the current pointer table (built on the host
+// whenever the table changes, so the kernel follows no pointer table): row 0 of both pieces'
+// sources; for a gather row, row 0 in the first two replicas (replicas past the second are looked
+// up through the group table, at member_offset * esize + dst_off_b of each member's pointer); for
+// a scatter row, row 0 of each piece's destination. Pitches and lengths in bytes.
 struct alignas(16) GBound {
   uint64_t src[2];
-  uint64_t dst[2];      // dst[1] == dst[0] with one replica
+  uint64_t dst[2];      // gather: replicas 0 and 1 (dst[1] == dst[0] with one); scatter: pieces 0 and 1
   int64_t sp[2];
-  int64_t dp;
+  int64_t dp[2];        // destination pitch (gather: dp[0]; scatter: per piece)
   int64_t dst_off_b;
   int32_t B;            // piece 0's bytes per row
-  int32_t rb;           // bytes per row
+  int32_t rb;           // bytes per row, both pieces
   int32_t rows;
   int32_t group;
   int32_t nrep;
   int32_t esize;
-  int32_t pad[2];
+  int32_t kind;
+  int32_t pad;
 };
-static_assert(sizeof(GBound) == 96, "resolved gather item is one 96-byte descriptor");
+static_assert(sizeof(GBound) == 112, "resolved pair item is one 112-byte descriptor");
 // Item.pad[0] flag: the item's rows are written by a gather item instead
 constexpr int32_t kGathered = 1;
 

@@ -104,7 +104,10 @@ typedef struct {
 /* Where a rank's local shard sits in its buffer ("DTensorRef" local tensor, or a slice of a
  * fused parameter such as gate_up: design doc, "Execution Flow: Setup Time").
  * The element at local index i is at buffer element offset_elems + sum_d i[d] * strides[d].
- * Strides are any non-negative values that do not make elements alias. When the source and the
+ * Strides are non-negative. A destination view must not map two elements to one offset: taken
+ * by increasing stride, each dim's stride must exceed the span of the dims below it (dense,
+ * padded, transposed and interleaved layouts all do); the plan refuses one that does not
+ * (INVALID_ARG naming the view). Source views are only read and may alias. When the source and the
  * destination of a region are contiguous along the same dim, the region is a strided copy;
  * when they are contiguous along different dims (a transposed layout on one side, e.g. a
  * destination that keeps W^T), the region goes through the TMA transposing kernel; with no
@@ -160,10 +163,11 @@ typedef struct {
   int64_t local_bytes;        /* source bytes this rank copies to its own destinations directly */
   int64_t last_staged_items;  /* copy items of the last execute's last pass run by the bulk-staged
                                  kernel (reshard_copy_staged_kernel: misaligned rows < 4 KiB) */
-  int64_t gather_items;       /* gather items of the direct and unpack passes: destination rows
-                                 assembled from two source pieces side by side (reshard_plan_items
-                                 sets 6 and 8) */
-  int64_t last_gather_items;  /* gather items run by the last execute (reshard_copy_gather_kernel) */
+  int64_t gather_items;       /* pair items of all passes (reshard_plan_items sets 6-8): destination
+                                 rows of two source pieces (direct, unpack) and source rows into two
+                                 message blocks (pack) */
+  int64_t last_gather_items;  /* pair items run by the last execute (reshard_copy_gather_kernel,
+                                 reshard_copy_scatter_kernel) */
 } reshard_stats_t;
 
 /* One point-to-point transfer of a partitioned plan (see reshard_plan_transfers). */
@@ -374,8 +378,7 @@ int reshard_plan_group_members(const reshard_plan_t *plan, int64_t g, int64_t ca
 /*
  * reshard_plan_items -- copy a device work-item table for inspection. set 0/1/2: the strided
  * copy items of the direct / pack / unpack pass; set 3/4/5: the transposing items of the same
- * passes (64 bytes each); set 6/7/8: the gather items of the same passes (80 bytes each; the
- * pack pass has none).
+ * passes (64 bytes each); set 6/7/8: the pair items of the same passes (96 bytes each).
  * Copy item: int64 src_off, dst_off, src_pitch, dst_pitch (elements); int32 rows, run (elements
  * per row), src (pointer-table index), group, esize (bytes), 3 x int32 padding. It moves `rows`
  * rows of `run` elements from src_off + r * src_pitch of pointer `src` to
@@ -383,14 +386,15 @@ int reshard_plan_group_members(const reshard_plan_t *plan, int64_t g, int64_t ca
  * Transposing item: int64 src_off, dst_off, src_pitch, dst_pitch; int32 rows, cols, src, group,
  * esize, slab, x, y. Element (r, c) moves from src_off + r * src_pitch + c to
  * member_offset + dst_off + c * dst_pitch + r; (x, y) are (c = 0, r = 0) in slab coordinates.
- * Gather item: int64 src_off[2], src_pitch[2], dst_off, dst_pitch; int32 run[2], src[2], rows,
- * group, esize, padding. Destination row r is piece 0's run[0] elements from
- * src_off[0] + r * src_pitch[0] of pointer src[0], then piece 1's run[1] elements from
- * src_off[1] + r * src_pitch[1] of pointer src[1], written at member_offset + dst_off +
- * r * dst_pitch of every member of `group` (in the unpack pass both pieces are read from the
- * receive buffer's entry). A pass's copy items that a gather item covers carry 1 in their first
- * padding word; the copy walkers skip them when gather items run, and every other walk of the copy
- * items (MXFP8, the allocation-free entry point) takes them.
+ * Pair item: int64 src_off[2], src_pitch[2], dst_off[2], dst_pitch[2]; int32 run[2], src[2],
+ * rows, group, esize, kind. Row r of piece p is run[p] elements read at src_off[p] + r *
+ * src_pitch[p] of pointer src[p] and written at member_offset + dst_off[p] + r * dst_pitch[p] of
+ * every member of `group`. kind 0 (gather row; direct and unpack passes): one destination row of
+ * two source pieces side by side (dst_off[1] = dst_off[0] + run[0]; in the unpack pass both pieces
+ * are read from the receive buffer's entry). kind 1 (scatter row; pack pass): one source row into
+ * two message blocks (src_off[1] = src_off[0] + run[0]). A pass's copy items that a pair item
+ * covers carry 1 in their first padding word; the copy walkers skip them when pair items run,
+ * and every other walk of the copy items (MXFP8, the allocation-free entry point) takes them.
  * Pointer table: [sources | destination data | destination scales | send buffer | receive
  * buffer] (pack items write the send buffer's group, unpack items read the receive buffer). Up to
  * cap items go to `items` (may be NULL); *n_out gets the count. Copy items are ordered largest

@@ -2,10 +2,11 @@
 
 Each copy item moves `rows` rows of `run` elements from its source pointer to every member of
 its group; each transposing item moves element (r, c) from src_off + r * src_pitch + c to
-member offset + dst_off + c * dst_pitch + r; each gather item writes `rows` destination rows of
-run[0] + run[1] elements, piece 0's elements then piece 1's, each piece read from its own source
-pointer. Pointer-table entries are given as (array name, byte offset of the entry's buffer in
-that array, end offset).
+member offset + dst_off + c * dst_pitch + r; each pair item moves `rows` rows of its two pieces,
+piece p's run[p] elements from src_off[p] + r * src_pitch[p] of pointer src[p] to member offset +
+dst_off[p] + r * dst_pitch[p] of every member (a gather row's pieces land side by side in one
+destination row, a scatter row's in two message blocks). Pointer-table entries are given as
+(array name, byte offset of the entry's buffer in that array, end offset).
 """
 import numpy as np
 
@@ -14,8 +15,8 @@ import dtensor_resharding_gb300 as R
 
 def run_items(plan, which, table, arrays, gather=False):
     """Apply pass `which` (0 direct, 1 pack, 2 unpack) of `plan` to the named host arrays. With
-    `gather`, the pass runs as the executor runs it when it has gather items: the gather items,
-    and the copy items they do not cover (pad[0] == 0)."""
+    `gather`, the pass runs as the executor runs it when it has pair items: the pair items, and
+    the copy items they do not cover (pad[0] == 0)."""
     items, gs, mp, mo = R.reshard_plan_items(plan, which + 3)
     for it in items:
         e = int(it["esize"])
@@ -33,18 +34,16 @@ def run_items(plan, which, table, arrays, gather=False):
         skip_flagged = len(gitems) > 0
         for it in gitems:
             e = int(it["esize"])
-            n0, n1 = int(it["run"][0]) * e, int(it["run"][1]) * e
-            k0, b0, _ = table[it["src"][0]]
-            k1, b1, _ = table[it["src"][1]]
             for m in range(gs[it["group"]], gs[it["group"] + 1]):
                 dkind, dbase, _ = table[mp[m]]
                 darr = arrays[dkind]
-                for r in range(int(it["rows"])):
-                    s0 = b0 + (int(it["src_off"][0]) + r * int(it["src_pitch"][0])) * e
-                    s1 = b1 + (int(it["src_off"][1]) + r * int(it["src_pitch"][1])) * e
-                    d0 = dbase + (int(mo[m]) + int(it["dst_off"]) + r * int(it["dst_pitch"])) * e
-                    darr[d0: d0 + n0] = arrays[k0][s0: s0 + n0]
-                    darr[d0 + n0: d0 + n0 + n1] = arrays[k1][s1: s1 + n1]
+                for q in (0, 1):
+                    n = int(it["run"][q]) * e
+                    sk, sb, _ = table[it["src"][q]]
+                    for r in range(int(it["rows"])):
+                        s0 = sb + (int(it["src_off"][q]) + r * int(it["src_pitch"][q])) * e
+                        d0 = dbase + (int(mo[m]) + int(it["dst_off"][q]) + r * int(it["dst_pitch"][q])) * e
+                        darr[d0: d0 + n] = arrays[sk][s0: s0 + n]
     items, gs, mp, mo = R.reshard_plan_items(plan, which)
     for it in items:
         if skip_flagged and int(it["pad"][0]) == 1:

@@ -120,6 +120,25 @@ def test_view_capacity_overflow():
     assert "overflows its buffer" in str(e.value)
 
 
+def test_destination_views_whose_elements_alias_are_refused():
+    """A destination view that maps two elements to one offset (a row pitch shorter than its
+    rows, a zero stride) is refused with the view named; the same strides on a source view (read
+    only) plan, and so do padded, transposed and interleaved destination strides."""
+    for strides in ((1, 1), (0, 1), (1, 2)):        # local shape (8, 2): rows overlap
+        bad = S.TensorDesc("w", (8, 8), "bf16", (2,), ("S0",), (4,), ("S1",), [S.View(0), S.View(1)],
+                           [S.View(0, 0, strides)] + [S.View(i) for i in range(1, 4)])
+        with pytest.raises(R.ReshardError) as e:
+            R.reshard_plan_create(bad)
+        assert e.value.code == R.RESHARD_ERR_INVALID_ARG and "dst view 0 maps two elements to one offset" in str(e.value)
+    src_alias = S.TensorDesc("w", (8, 8), "bf16", (1,), ("R",), (4,), ("S1",), [S.View(0, 0, (0, 1))],
+                             [S.View(i) for i in range(4)])
+    R.reshard_plan_create(src_alias)                # every row of the source reads one buffer row
+    for strides in ((3, 1), (1, 8), (4, 1)):        # padded rows, column-major, rows two apart
+        ok = S.TensorDesc("w", (8, 8), "bf16", (2,), ("S0",), (4,), ("S1",), [S.View(0), S.View(1)],
+                          [S.View(0, 0, strides)] + [S.View(i) for i in range(1, 4)])
+        R.reshard_plan_create(ok)
+
+
 def test_negative_stride_rejected_and_transposed_view_planned():
     bad = S.TensorDesc("w", (8, 8), "bf16", (2,), ("S0",), (4,), ("S1",),
                        [S.View(0, 0, (8, -1)), S.View(1)], [S.View(i) for i in range(4)])

@@ -110,12 +110,12 @@ def check_transpose_bounds(wl, lay, plan, which, ws=None):
 
 
 def check_gather_bounds(wl, lay, plan, ws=None, which=None):
-    """Gather items of the direct and unpack passes (or of pass `which`): both pieces' reads and
-    every row's writes stay in their buffers, and a pass's gather items carry exactly the bytes
-    of its copy items flagged as theirs."""
+    """Pair items of every pass (or of pass `which`): each kind where it belongs (gather rows in
+    the direct and unpack passes, scatter rows in the pack pass) with its own invariant, both
+    pieces' reads and writes inside their buffers, and a pass's pair items carrying exactly the
+    bytes of its copy items flagged as theirs."""
     if which is None:
-        assert len(R.reshard_plan_items(plan, 6 + PACK)[0]) == 0
-        for w in (DIRECT, UNPACK):
+        for w in (DIRECT, PACK, UNPACK):
             check_gather_bounds(wl, lay, plan, ws, w)
         return
     items, gs, mp, mo = R.reshard_plan_items(plan, 6 + which)
@@ -128,25 +128,32 @@ def check_gather_bounds(wl, lay, plan, ws=None, which=None):
     es = items["esize"].astype(np.int64)
     rows = items["rows"].astype(np.int64)
     assert (rows > 0).all() and (items["run"] >= 2).all()
+    if which == PACK:   # one source row into two message blocks
+        assert (items["kind"] == 1).all()
+        assert (items["src"][:, 1] == items["src"][:, 0]).all()
+        assert (items["src_off"][:, 1] == items["src_off"][:, 0] + items["run"][:, 0]).all()
+    else:               # one destination row of two pieces side by side
+        assert (items["kind"] == 0).all()
+        assert (items["dst_off"][:, 1] == items["dst_off"][:, 0] + items["run"][:, 0]).all()
+        assert (items["dst_pitch"][:, 1] == items["dst_pitch"][:, 0]).all()
     assert int((rows * (items["run"][:, 0] + items["run"][:, 1]) * es).sum()) == \
         int((flagged["rows"].astype(np.int64) * flagged["run"] * flagged["esize"]).sum())
     table = _ranges(wl, lay, plan, ws)
     lo = np.array([r[1] for r in table], np.int64)
     hi = np.array([r[2] for r in table], np.int64)
+    counts = gs[items["group"] + 1] - gs[items["group"]]
     for p in (0, 1):
         sp = items["src"][:, p]
         s0 = lo[sp] + items["src_off"][:, p] * es
         s1 = lo[sp] + (items["src_off"][:, p] + (rows - 1) * items["src_pitch"][:, p] + items["run"][:, p]) * es
-        assert (s0 >= lo[sp]).all() and (s1 <= hi[sp]).all(), "gather read out of bounds"
-    counts = gs[items["group"] + 1] - gs[items["group"]]
-    for k in range(int(counts.max())):
-        sel = counts > k
-        m = gs[items["group"][sel]] + k
-        ptr, off, it = mp[m], mo[m], items[sel]
-        run = it["run"][:, 0].astype(np.int64) + it["run"][:, 1]
-        d0 = lo[ptr] + (off + it["dst_off"]) * es[sel]
-        d1 = lo[ptr] + (off + it["dst_off"] + (rows[sel] - 1) * it["dst_pitch"] + run) * es[sel]
-        assert (d0 >= lo[ptr]).all() and (d1 <= hi[ptr]).all(), "gather write out of bounds"
+        assert (s0 >= lo[sp]).all() and (s1 <= hi[sp]).all(), "pair item read out of bounds"
+        for k in range(int(counts.max())):
+            sel = counts > k
+            m = gs[items["group"][sel]] + k
+            ptr, off, it = mp[m], mo[m], items[sel]
+            d0 = lo[ptr] + (off + it["dst_off"][:, p]) * es[sel]
+            d1 = lo[ptr] + (off + it["dst_off"][:, p] + (rows[sel] - 1) * it["dst_pitch"][:, p] + it["run"][:, p]) * es[sel]
+            assert (d0 >= lo[ptr]).all() and (d1 <= hi[ptr]).all(), "pair item write out of bounds"
 
 
 def emulate(wl, lay, plan, mode, gather=False):
@@ -244,10 +251,16 @@ def test_gather_items_where_rows_are_split_and_misaligned(name):
     plan = R.plan_workload(wl)
     items = R.reshard_plan_items(plan, 6)[0]
     unpack = R.reshard_plan_items(plan, 8)[0]
-    assert R.reshard_plan_stats(plan)["gather_items"] == len(items) + len(unpack)
+    pack = R.reshard_plan_items(plan, 7)[0]
+    assert R.reshard_plan_stats(plan)["gather_items"] == len(items) + len(pack) + len(unpack)
     if name not in GATHER_EXPECT:
         assert len(items) == 0 and len(unpack) == 0, name
         return
+    # the pack pass splits each source row that feeds two destinations (the (2,4) source's
+    # 1024-column shards 1 and 2: 684 + 1364 and 1368 + 680 bytes) into its two message blocks
+    es_p = pack["esize"].astype(np.int64)
+    assert {(int(a), int(b)) for a, b in zip(pack["run"][:, 0] * es_p, pack["run"][:, 1] * es_p)} == \
+        {(684, 1364), (1368, 680)}
     # the unpack pass pairs the same rows (pieces read from the received message)
     es = unpack["esize"].astype(np.int64)
     assert {(int(a), int(b)) for a, b in zip(unpack["run"][:, 0] * es, unpack["run"][:, 1] * es)} == GATHER_EXPECT[name]
@@ -255,7 +268,7 @@ def test_gather_items_where_rows_are_split_and_misaligned(name):
     es = items["esize"].astype(np.int64)
     got = {(int(a), int(b)) for a, b in zip(items["run"][:, 0] * es, items["run"][:, 1] * es)}
     assert got == GATHER_EXPECT[name]
-    assert (items["dst_pitch"] * es == (items["run"][:, 0] + items["run"][:, 1]) * es).all()
+    assert (items["dst_pitch"][:, 0] * es == (items["run"][:, 0] + items["run"][:, 1]) * es).all()
     t = wl.tensors[0]
     n_rep = int(np.prod(t.dst_mesh)) // 3
     gs = R.reshard_plan_items(plan, 6)[1]
@@ -320,7 +333,7 @@ def test_gather_items_merge_outer_dims():
     assert np.array_equal(emulate(wl, lay, plan, "packed", gather=True), _oracle(wl, lay))
     # destination shards with a padded outer stride: the outer dim is walked explicitly
     t = wl.tensors[0]
-    cols = [334, 333, 333]
+    cols = [334, 334, 332]   # torch.chunk of 1000 columns into 3
     t.dst_views = [S.View(i, 0, (3 * c + 8, c, 1)) for i, c in enumerate(cols)]
     wl = S.workloads._size_buffers(S.Workload("padded", [t]), 4, 3)
     plan = R.plan_workload(wl)
