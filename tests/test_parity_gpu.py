@@ -515,13 +515,14 @@ def test_gather_rows_bit_exact(name, misalign):
     if misalign % S.DTYPES[wl.tensors[0].dtype][1]:
         pytest.skip("shift not a multiple of the element size")
     lay, plan = run_gpu(wl, misalign=misalign)
-    n_direct, n_unpack = len(R.reshard_plan_items(plan, 6)[0]), len(R.reshard_plan_items(plan, 8)[0])
+    n_direct, n_pack, n_unpack = (len(R.reshard_plan_items(plan, k)[0]) for k in (6, 7, 8))
     st = R.reshard_plan_stats(plan)
-    assert n_direct > 0 and st["last_gather_items"] == n_direct and st["gather_items"] == n_direct + n_unpack
+    assert n_direct > 0 and st["last_gather_items"] == n_direct and st["gather_items"] == n_direct + n_pack + n_unpack
     assert_matches_oracle(wl, lay)
-    # packed: pack items into messages, then the unpack pass's gather items out of them
+    # packed: the pack pass (scatter items where one source row feeds two message blocks), then
+    # the unpack pass's gather items out of the messages
     lay, plan = run_gpu(wl, mode="packed", misalign=misalign, plan=plan)
-    assert n_unpack > 0 and R.reshard_plan_stats(plan)["last_gather_items"] == n_unpack
+    assert n_unpack > 0 and R.reshard_plan_stats(plan)["last_gather_items"] == n_pack + n_unpack
     assert_matches_oracle(wl, lay)
 
 
